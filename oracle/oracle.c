@@ -1,0 +1,282 @@
+/*
+ * Oracle for the fused row-normalisation family -- TEST INFRASTRUCTURE ONLY.
+ *
+ * A plain, slow, single-threaded CPU definition of what each op computes, in
+ * double precision, with rounding to the storage dtype (bf16 or f32) only where
+ * the method stores a value.  Nothing here is blocked, fused or reordered beyond
+ * what the definitions state, so each function can be checked by eye against the
+ * passage it cites.  It shares no code with the CUDA library and includes none
+ * of its headers; only tests/, __graft_entry__.smoke() and bench.py's CPU
+ * baseline leg may load it.
+ *
+ * Sources (page title, then the section on that page):
+ *   [VT]  vllm.cpp, src/vt/cuda/cuda_ops.cu
+ *           - "f32 load/store overloads" (bf16 stores are round-to-nearest-even)
+ *           - "ResRound" (residual rounded to its storage dtype before squaring)
+ *           - "rmsnorm: one block per row" (RmsNormRowKernel: eps inside the
+ *             sqrt, mean over h, gemma uses w+1)
+ *           - "rope_neox" (RopeNeoxKernel: freq = base^(-2*pair/rot) in double,
+ *             angle = pos*freq, rotate-half pairing (i, i+rot/2))
+ *           - "attn_qk_norm_rope_gate" (per-(token, head) RMSNorm over head_dim,
+ *             then the rotation, with no bf16 rounding in between)
+ *           - "silu_and_mul" (gate = first half, up = second half)
+ *   [PAN2] FastVideo compare view feat/pan2-inference-optimizations, PAN2 docs,
+ *          "Performance switches" table, row dit_fused_kernels: names the fused
+ *          LayerNorm + modulation without printing its formula.  The oracle uses
+ *          the plain adaLN reading out = LN(x)*(1+scale)+shift with the biased
+ *          (1/N) variance, eps inside the sqrt and no affine weight or bias.
+ *
+ * Storage dtype codes: 0 = f32, 1 = bf16 (bf16 values travel as uint16 bits).
+ *
+ * Besides the stored result every op can return y, the exact (double)
+ * pre-rounding value of each output.  The two ops whose last step adds terms
+ * that can cancel (the RoPE rotation and the LayerNorm modulation) can also
+ * return mag, the sum of magnitudes of the quantities combined into that output;
+ * comparisons use it to size the f32 evaluation error a GPU makes there.
+ */
+#include <fenv.h>
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#define NRO_F32 0
+#define NRO_BF16 1
+
+/* ------------------------------------------------------------------------ */
+/* bf16 storage                                                              */
+/* ------------------------------------------------------------------------ */
+
+/* Exact value of a bf16 bit pattern: bf16 is the top half of an f32. */
+double nro_bf16_value(uint16_t bits) {
+  uint32_t u = (uint32_t)bits << 16;
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return (double)f;
+}
+
+/* Round a double straight to bf16, round-to-nearest, ties-to-even ([VT]
+ * "f32 load/store overloads").  Rounds once, from the double, never via f32.
+ * bf16 keeps 8 significant bits; its normal exponents reach down to 2^-126 and
+ * below that the grid is the fixed subnormal step 2^-133. */
+uint16_t nro_bf16_round(double d) {
+  if (isnan(d)) return (uint16_t)0x7FC0;
+  const uint16_t sign = signbit(d) ? (uint16_t)0x8000 : (uint16_t)0;
+  const double a = fabs(d);
+  if (isinf(a)) return (uint16_t)(sign | 0x7F80);
+  if (a == 0.0) return sign;
+  int e;
+  frexp(a, &e);               /* a = m * 2^e, 0.5 <= m < 1, so a in [2^(e-1), 2^e) */
+  int quantum_exp = (e - 1) - 7;  /* spacing of 8-significant-bit numbers there */
+  if (quantum_exp < -133) quantum_exp = -133;
+  const double scaled = ldexp(a, -quantum_exp);  /* exact: power-of-two scaling */
+  const double n = nearbyint(scaled);            /* default mode: ties to even */
+  const double r = ldexp(n, quantum_exp);
+  if (r >= 0x1p128) return (uint16_t)(sign | 0x7F80); /* overflow to infinity */
+  const float rf = (float)r; /* exact: every bf16 value is an f32 value */
+  uint32_t u;
+  memcpy(&u, &rf, sizeof u);
+  return (uint16_t)(sign | (uint16_t)(u >> 16));
+}
+
+/* nro_bf16_round over an array (for exhaustive checks of the rounding). */
+void nro_bf16_round_array(const double* d, uint16_t* bits, int64_t n) {
+  for (int64_t i = 0; i < n; i++) bits[i] = nro_bf16_round(d[i]);
+}
+
+/* Value of element i of a stored array of the given dtype, as a double. */
+static double load(int dtype, const void* p, int64_t i) {
+  if (dtype == NRO_BF16) return nro_bf16_value(((const uint16_t*)p)[i]);
+  return (double)((const float*)p)[i];
+}
+
+/* Round v to the storage dtype and return the stored value as a double. */
+static double round_to(int dtype, double v) {
+  if (dtype == NRO_BF16) return nro_bf16_value(nro_bf16_round(v));
+  return (double)(float)v; /* C conversion: round to nearest even */
+}
+
+/* Store v (rounded to the dtype) at element i. */
+static void store(int dtype, void* p, int64_t i, double v) {
+  if (dtype == NRO_BF16)
+    ((uint16_t*)p)[i] = nro_bf16_round(v);
+  else
+    ((float*)p)[i] = (float)v;
+}
+
+/* ------------------------------------------------------------------------ */
+/* RMSNorm, optionally with the fused residual add ([VT] "rmsnorm: one block  */
+/* per row", "ResRound").                                                     */
+/*                                                                            */
+/*   with a residual: v_j = round_dtype(x_j + res_j), and res_j <- v_j        */
+/*   without one:     v_j = x_j                                               */
+/*   ms  = (sum_j v_j^2) / hidden                                             */
+/*   inv = 1 / sqrt(ms + eps)                                                 */
+/*   y_j = v_j * inv * (w_j + 1 if gemma else w_j);  out_j = round_dtype(y_j) */
+/* ------------------------------------------------------------------------ */
+void nro_rmsnorm(int dtype, int64_t rows, int64_t hidden, const void* x, const void* w,
+                 const void* res_in, double eps, int gemma, void* out, void* res_out,
+                 double* y) {
+  for (int64_t r = 0; r < rows; r++) {
+    const int64_t base = r * hidden;
+    double sum_sq = 0.0;
+    for (int64_t j = 0; j < hidden; j++) {
+      double v = load(dtype, x, base + j);
+      if (res_in != NULL) {
+        /* The exact sum of two stored values, rounded once to the residual's
+         * storage dtype: the value written back and the value squared. */
+        v = round_to(dtype, v + load(dtype, res_in, base + j));
+        store(dtype, res_out, base + j, v);
+      }
+      sum_sq += v * v;
+    }
+    const double ms = sum_sq / (double)hidden;
+    const double inv = 1.0 / sqrt(ms + eps);
+    for (int64_t j = 0; j < hidden; j++) {
+      const double v = (res_in != NULL) ? load(dtype, res_out, base + j) : load(dtype, x, base + j);
+      double wj = load(dtype, w, j);
+      if (gemma) wj += 1.0;
+      const double yj = v * inv * wj;
+      store(dtype, out, base + j, yj);
+      if (y != NULL) y[base + j] = yj;
+    }
+  }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Per-head Q/K RMSNorm followed by NeoX RoPE ([VT] "attn_qk_norm_rope_gate",  */
+/* "rope_neox").  For token t and head h of a tensor with its own norm weight */
+/* w (one vector of length D, shared by all heads):                           */
+/*                                                                            */
+/*   inv = 1 / sqrt(mean_j v_j^2 + eps),   n_j = v_j * inv * w_j (w_j+1 gemma)  */
+/*   for i < D/2:  f_i = theta^(-2i/D)   (double)                             */
+/*                 a   = pos_t * f_i     (double);  c = cos a, s = sin a      */
+/*                 y_i       = n_i c - n_{i+D/2} s                            */
+/*                 y_{i+D/2} = n_i s + n_{i+D/2} c                            */
+/*   out = round_dtype(y)  (one rounding: the normed values are not stored)   */
+/*                                                                            */
+/* The rotary dimension is the whole head_dim.  Element (t, h, j) of an input */
+/* or output lives at t*tok_stride + h*D + j; outputs share the input strides. */
+/* mag_i = mag_{i+D/2} = |n_i| + |n_{i+D/2}| bounds every term of the rotation. */
+/* ------------------------------------------------------------------------ */
+static void norm_rope_one(int dtype, int w_dtype, int64_t tokens, int64_t heads, int64_t D,
+                          const void* src, int64_t tok_stride, const void* w,
+                          const int32_t* pos, double eps, double theta, int gemma, void* dst,
+                          double* y, double* mag) {
+  const int64_t half = D / 2;
+  double n[1024];
+  for (int64_t t = 0; t < tokens; t++) {
+    for (int64_t h = 0; h < heads; h++) {
+      const int64_t base = t * tok_stride + h * D;
+      double sum_sq = 0.0;
+      for (int64_t j = 0; j < D; j++) {
+        const double v = load(dtype, src, base + j);
+        sum_sq += v * v;
+      }
+      const double inv = 1.0 / sqrt(sum_sq / (double)D + eps);
+      for (int64_t j = 0; j < D; j++) {
+        double wj = load(w_dtype, w, j);
+        if (gemma) wj += 1.0;
+        n[j] = load(dtype, src, base + j) * inv * wj;
+      }
+      for (int64_t i = 0; i < half; i++) {
+        const double freq = pow(theta, -2.0 * (double)i / (double)D);
+        const double angle = (double)pos[t] * freq;
+        const double c = cos(angle);
+        const double s = sin(angle);
+        const double first = n[i] * c - n[i + half] * s;
+        const double second = n[i] * s + n[i + half] * c;
+        store(dtype, dst, base + i, first);
+        store(dtype, dst, base + i + half, second);
+        if (y != NULL) {
+          y[base + i] = first;
+          y[base + i + half] = second;
+        }
+        if (mag != NULL) {
+          mag[base + i] = fabs(n[i]) + fabs(n[i + half]);
+          mag[base + i + half] = fabs(n[i]) + fabs(n[i + half]);
+        }
+      }
+    }
+  }
+}
+
+/* Returns 0 on success, -1 when head_dim is odd or above the oracle's bound. */
+int nro_qk_norm_rope(int dtype, int w_dtype, int64_t tokens, int64_t hq, int64_t hk,
+                     int64_t head_dim, const void* q, int64_t q_tok_stride, const void* k,
+                     int64_t k_tok_stride, const void* wq, const void* wk, const int32_t* pos,
+                     double eps, double theta, int gemma, void* q_out, void* k_out, double* q_y,
+                     double* k_y, double* q_mag, double* k_mag) {
+  if (head_dim <= 0 || head_dim % 2 != 0 || head_dim > 1024) return -1;
+  norm_rope_one(dtype, w_dtype, tokens, hq, head_dim, q, q_tok_stride, wq, pos, eps, theta, gemma,
+                q_out, q_y, q_mag);
+  norm_rope_one(dtype, w_dtype, tokens, hk, head_dim, k, k_tok_stride, wk, pos, eps, theta, gemma,
+                k_out, k_y, k_mag);
+  return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* LayerNorm (no affine) + adaLN modulation ([PAN2]; formula as read above).   */
+/*                                                                            */
+/*   mu = mean_j x_j;  var = mean_j (x_j - mu)^2   (two passes, biased)       */
+/*   xhat_j = (x_j - mu) / sqrt(var + eps)                                    */
+/*   y_j = xhat_j * (1 + scale_j) + shift_j;  out_j = round_dtype(y_j)        */
+/*                                                                            */
+/* shift and scale hold one row per sample; row r uses sample r / rows_per_sample. */
+/* mag_j = (|x_j - mu| + mean_k |x_k|) / sqrt(var + eps) * |1 + scale_j| + |shift_j| */
+/* bounds the terms of the last step, including the error a rounded mean      */
+/* carries into x_j - mu.                                                     */
+/* ------------------------------------------------------------------------ */
+void nro_ln_modulate(int dtype, int64_t rows, int64_t hidden, int64_t rows_per_sample,
+                     const void* x, const void* shift, const void* scale, double eps, void* out,
+                     double* y, double* mag) {
+  for (int64_t r = 0; r < rows; r++) {
+    const int64_t base = r * hidden;
+    const int64_t sample = (r / rows_per_sample) * hidden;
+    double sum = 0.0, sum_abs = 0.0;
+    for (int64_t j = 0; j < hidden; j++) {
+      sum += load(dtype, x, base + j);
+      sum_abs += fabs(load(dtype, x, base + j));
+    }
+    const double mu = sum / (double)hidden;
+    double sum_dev = 0.0;
+    for (int64_t j = 0; j < hidden; j++) {
+      const double d = load(dtype, x, base + j) - mu;
+      sum_dev += d * d;
+    }
+    const double var = sum_dev / (double)hidden;
+    const double rstd = 1.0 / sqrt(var + eps);
+    for (int64_t j = 0; j < hidden; j++) {
+      const double d = load(dtype, x, base + j) - mu;
+      const double xhat = d * rstd;
+      const double g = 1.0 + load(dtype, scale, sample + j);
+      const double sh = load(dtype, shift, sample + j);
+      const double yj = xhat * g + sh;
+      store(dtype, out, base + j, yj);
+      if (y != NULL) y[base + j] = yj;
+      if (mag != NULL)
+        mag[base + j] = (fabs(d) + sum_abs / (double)hidden) * rstd * fabs(g) + fabs(sh);
+    }
+  }
+}
+
+/* ------------------------------------------------------------------------ */
+/* silu_and_mul ([VT] "silu_and_mul").  x is [rows, 2*inter]:                 */
+/*   a = x[r, j] (gate, first half), b = x[r, inter + j] (up, second half)    */
+/*   y = a / (1 + exp(-a)) * b;  out[r, j] = round_dtype(y)                   */
+/* ------------------------------------------------------------------------ */
+void nro_silu_and_mul(int dtype, int64_t rows, int64_t inter, const void* x, void* out,
+                      double* y) {
+  for (int64_t r = 0; r < rows; r++) {
+    for (int64_t j = 0; j < inter; j++) {
+      const double a = load(dtype, x, r * 2 * inter + j);
+      const double b = load(dtype, x, r * 2 * inter + inter + j);
+      const double yj = a / (1.0 + exp(-a)) * b;
+      store(dtype, out, r * inter + j, yj);
+      if (y != NULL) y[r * inter + j] = yj;
+    }
+  }
+}
+
+/* Rounding mode guard: the oracle's nearbyint and conversions assume the
+ * default round-to-nearest mode; callers can check it. */
+int nro_rounding_mode_is_nearest(void) { return fegetround() == FE_TONEAREST; }

@@ -1,0 +1,106 @@
+"""The pins must catch plausible slips in the oracle.
+
+Each case below plants one mistake in a copy of oracle.c (a dropped term, a
+wrong sign, index or divisor, a misplaced eps, a missing rounding), compiles it
+on the CPU, points the oracle module at the mutant and runs every pin in
+test_oracle_pins.py.  At least one pin must fail for every mutant; the real
+oracle is restored afterwards.
+
+Rounding the residual sum to f32 before bf16 is deliberately absent: for two
+bf16 operands it is an equivalent program (f32 keeps at least 2*8+2 bits, so
+the second rounding cannot move), which is also why the GPU's f32 add is exact
+against the oracle's single rounding.
+"""
+import ctypes
+import inspect
+import os
+
+import pytest
+
+import oracle
+from tests import test_oracle_pins as pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
+
+# (name, text in oracle.c, replacement)
+MUTANTS = [
+    ("bf16 ties away from zero", "nearbyint(scaled)", "floor(scaled + 0.5)"),
+    ("bf16 truncation", "nearbyint(scaled)", "trunc(scaled)"),
+    ("bf16 wrong significand width", "(e - 1) - 7", "(e - 1) - 8"),
+    ("eps outside the sqrt", "1.0 / sqrt(ms + eps)", "1.0 / (sqrt(ms) + eps)"),
+    ("mean over h-1", "sum_sq / (double)hidden", "sum_sq / (double)(hidden - 1)"),
+    ("gemma dropped", "if (gemma) wj += 1.0;\n      const double yj",
+     "if (gemma) wj += 0.0;\n      const double yj"),
+    ("residual not rounded before squaring",
+     "v = round_to(dtype, v + load(dtype, res_in, base + j));",
+     "store(dtype, res_out, base + j, v + load(dtype, res_in, base + j)); v = v + load(dtype, res_in, base + j);"),
+    ("output stored via f32 (double rounding)", "((uint16_t*)p)[i] = nro_bf16_round(v);",
+     "((uint16_t*)p)[i] = nro_bf16_round((float)v);"),
+    ("rope rotates the other way", "const double first = n[i] * c - n[i + half] * s;\n        const double second = n[i] * s + n[i + half] * c;",
+     "const double first = n[i] * c + n[i + half] * s;\n        const double second = -n[i] * s + n[i + half] * c;"),
+    ("rope sign slip in one half", "const double second = n[i] * s + n[i + half] * c;",
+     "const double second = n[i] * s - n[i + half] * c;"),
+    ("rope interleaved pairing", "n[i + half]", "n[(2 * i + 1) % D]"),
+    ("rope frequency exponent -i/D", "-2.0 * (double)i / (double)D", "-(double)i / (double)D"),
+    ("rope position off by one", "(double)pos[t] * freq", "(double)(pos[t] + 1) * freq"),
+    ("rope weight reversed", "double wj = load(w_dtype, w, j);", "double wj = load(w_dtype, w, D - 1 - j);"),
+    ("rope head norm over D-1", "sum_sq / (double)D + eps", "sum_sq / (double)(D - 1) + eps"),
+    ("rope head stride", "const int64_t base = t * tok_stride + h * D;",
+     "const int64_t base = t * tok_stride + h * half;"),
+    ("ln unbiased variance", "sum_dev / (double)hidden", "sum_dev / (double)(hidden - 1)"),
+    ("ln scale without the 1", "const double g = 1.0 + load(dtype, scale, sample + j);",
+     "const double g = load(dtype, scale, sample + j);"),
+    ("ln shift sign", "const double yj = xhat * g + sh;", "const double yj = xhat * g - sh;"),
+    ("ln sample index", "(r / rows_per_sample) * hidden", "(r % rows_per_sample) * hidden"),
+    ("ln eps outside the sqrt", "1.0 / sqrt(var + eps)", "1.0 / (sqrt(var) + eps)"),
+    ("silu exponent sign", "a / (1.0 + exp(-a)) * b", "a / (1.0 + exp(a)) * b"),
+    ("silu gate and up swapped", "const double a = load(dtype, x, r * 2 * inter + j);\n      const double b = load(dtype, x, r * 2 * inter + inter + j);",
+     "const double b = load(dtype, x, r * 2 * inter + j);\n      const double a = load(dtype, x, r * 2 * inter + inter + j);"),
+]
+
+
+def _pin_calls():
+    calls = []
+    for name, fn in inspect.getmembers(pins, inspect.isfunction):
+        if not name.startswith("test_"):
+            continue
+        marks = [m for m in getattr(fn, "pytestmark", []) if m.name == "parametrize"]
+        if marks:
+            argname, values = marks[0].args[0], marks[0].args[1]
+            for v in values:
+                calls.append((name, fn, {argname: v}))
+        else:
+            calls.append((name, fn, {}))
+    return calls
+
+
+def _caught(lib) -> list:
+    saved = oracle._lib
+    oracle._lib = lib
+    failed = []
+    try:
+        for name, fn, kw in _pin_calls():
+            try:
+                fn(**kw)
+            except (AssertionError, ValueError):
+                failed.append(name)
+    finally:
+        oracle._lib = saved
+    return failed
+
+
+def test_real_oracle_passes_all_pins():
+    assert _caught(oracle._load()) == []
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_mutant_is_caught(name, old, new, tmp_path):
+    src = open(SRC).read()
+    assert src.count(old) >= 1, "mutation anchor not found: %r" % old
+    mutated = src.replace(old, new)
+    path = tmp_path / "mutant.c"
+    path.write_text(mutated)
+    lib_path = oracle.compile_source(str(path), str(tmp_path / "libmutant.so"))
+    lib = oracle.configure(ctypes.CDLL(lib_path))
+    failed = _caught(lib)
+    assert failed, "no pin caught the mutant '%s'" % name

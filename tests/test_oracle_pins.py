@@ -1,0 +1,489 @@
+"""Pins for the CPU oracle: closed forms, invariants, library special cases and
+exact brute force, each chosen so that a plausible slip in the oracle (a dropped
+term, a wrong sign, index or operand order, a misplaced eps, a missing rounding)
+fails at least one of them.  The oracle is never compared with itself here.
+
+Sources (page, section): vllm.cpp src/vt/cuda/cuda_ops.cu -- "f32 load/store
+overloads", "ResRound", "rmsnorm: one block per row", "rope_neox",
+"attn_qk_norm_rope_gate", "silu_and_mul"; FastVideo PAN2 docs, "Performance
+switches" (dit_fused_kernels: LayerNorm + modulation).
+"""
+import math
+import os
+from fractions import Fraction
+
+import mpmath
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from tests.parity import bf16_to_f64
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def bf16(vals):
+    """bf16 bits of values that are exactly representable (asserted)."""
+    t = torch.tensor(vals, dtype=torch.float64)
+    b = t.to(torch.bfloat16)
+    assert torch.equal(b.double(), t), "value not exactly representable in bf16"
+    return b.view(torch.int16).numpy().view(np.uint16)
+
+
+def f32(vals):
+    return np.asarray(vals, dtype=np.float32)
+
+
+# --------------------------------------------------------------------------
+# bf16 rounding
+# --------------------------------------------------------------------------
+def test_bf16_rounding_golden_cases():
+    n = 0
+    with open(os.path.join(GOLDEN, "bf16_rounding.txt")) as f:
+        for line in f:
+            if not line.strip() or line.startswith("#"):
+                continue
+            hexval, bits, _ = line.split(None, 2)
+            d = float.fromhex(hexval)
+            assert oracle.bf16_round(d) == int(bits, 16), line
+            n += 1
+    assert n >= 12
+
+
+def test_bf16_rounding_matches_torch_on_f32_values():
+    """For values that are f32, rounding the double straight to bf16 must agree
+    with torch's f32 -> bf16 conversion (a library round-to-nearest-even)."""
+    rng = np.random.default_rng(7)
+    hi = np.arange(0, 1 << 16, dtype=np.uint32)
+    hi = hi[(hi & 0x7F80) != 0x7F80]  # finite values only
+    lows = [0x0000, 0x7FFF, 0x8000, 0x8001, 0xFFFF]
+    words = np.concatenate([(hi << 16) | np.uint32(lo) for lo in lows]
+                           + [(hi << 16) | rng.integers(0, 1 << 16, hi.size).astype(np.uint32)])
+    f = words.view(np.float32)
+    ours = oracle.bf16_round_array(f.astype(np.float64))
+    ref = torch.from_numpy(f.copy()).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    mism = np.nonzero(ours != ref)[0]
+    assert mism.size == 0, "first mismatch: f32 bits 0x%08x" % words[mism[0]]
+
+
+def _nearest_bf16_exact(d: float) -> int:
+    """Brute force: the bf16 pattern nearest to d in exact rational arithmetic,
+    ties to the even pattern, among the patterns around torch's f32 guess."""
+    guess = int(torch.tensor([d], dtype=torch.float32).to(torch.bfloat16)
+                .view(torch.int16).item()) & 0xFFFF
+    x = Fraction(d)
+    best = None
+    for b in range(max(guess - 3, 0), guess + 4):
+        if ((b >> 7) & 0xFF) == 0xFF or (b & 0x8000) != (guess & 0x8000):
+            continue
+        v = Fraction(bf16_to_f64(np.array([b], np.uint16))[0])
+        key = (abs(v - x), b & 1)
+        if best is None or key < best[0]:
+            best = (key, b)
+    return best[1]
+
+
+def test_bf16_rounding_exact_brute_force_on_doubles():
+    rng = np.random.default_rng(11)
+    d = rng.standard_normal(4000) * np.exp2(rng.integers(-120, 120, 4000))
+    # add doubles sitting just off bf16 midpoints, where rounding via f32 would differ
+    mids = bf16_to_f64(rng.integers(0x0100, 0x7E00, 500).astype(np.uint16)) * (1 + 2.0 ** -8)
+    d = np.concatenate([d, mids * (1 + 2.0 ** -40), mids * (1 - 2.0 ** -40)])
+    ours = oracle.bf16_round_array(d)
+    for i in range(d.size):
+        assert ours[i] == _nearest_bf16_exact(float(d[i])), d[i]
+
+
+# --------------------------------------------------------------------------
+# residual add
+# --------------------------------------------------------------------------
+def _random_bf16_pairs(n, seed):
+    """bf16 pairs spread over every exponent gap between the operands."""
+    rng = np.random.default_rng(seed)
+    a = rng.standard_normal(n) * np.exp2(rng.integers(-30, 30, n))
+    b = rng.standard_normal(n) * np.exp2(rng.integers(-30, 30, n))
+    ab = torch.from_numpy(a).to(torch.bfloat16)
+    bb = torch.from_numpy(b).to(torch.bfloat16)
+    return ab, bb
+
+
+def test_residual_add_is_one_exact_rounding():
+    """res <- round_bf16(x + res), the exact sum rounded once.  Checked against
+    exact rational rounding, and against torch's f32 add followed by its bf16
+    conversion (the GPU's evaluation: f32 keeps 24 >= 2*8+2 bits, so rounding
+    through f32 first cannot change the result)."""
+    xa, ra = _random_bf16_pairs(8 * 512, 3)
+    x = synth.to_oracle(xa).reshape(512, 8)
+    r = synth.to_oracle(ra).reshape(512, 8)
+    w = bf16([1.0] * 8)
+    _, res_out, _ = oracle.rmsnorm(x, w, residual=r, eps=1e-6)
+    via_f32 = (xa.float() + ra.float()).to(torch.bfloat16)
+    assert np.array_equal(res_out.reshape(-1), synth.to_oracle(via_f32))
+    xs, rs = bf16_to_f64(x.reshape(-1)), bf16_to_f64(r.reshape(-1))
+    for i in range(0, xs.size, 7):
+        assert res_out.reshape(-1)[i] == _nearest_bf16_exact(float(Fraction(xs[i]) + Fraction(rs[i])))
+
+
+def test_residual_add_f32_is_ieee_add():
+    rng = np.random.default_rng(5)
+    x = (rng.standard_normal((64, 8)) * np.exp2(rng.integers(-40, 40, (64, 8)))).astype(np.float32)
+    r = (rng.standard_normal((64, 8)) * np.exp2(rng.integers(-40, 40, (64, 8)))).astype(np.float32)
+    _, res_out, _ = oracle.rmsnorm(x, f32([1.0] * 8), residual=r)
+    assert np.array_equal(res_out, x + r)  # numpy's f32 add is the IEEE add
+
+
+def test_residual_is_rounded_before_it_is_squared():
+    """x = 1, res = 2^-9 rounds to exactly 1 in bf16, so a row of such sums has
+    mean square exactly 1 and, with eps = 0, out = w exactly.  Squaring the
+    unrounded sum 1 + 2^-9 would give a different y."""
+    x = bf16([[1.0] * 8])
+    r = bf16([[2.0 ** -9] + [0.0] * 7])
+    wv = [0.5, 0.75, 1.0, 1.25, 1.5, 1.75, 2.0, 2.25]
+    out, res_out, y = oracle.rmsnorm(x, bf16(wv), residual=r, eps=0.0, want_y=True)
+    assert np.array_equal(res_out, bf16([[1.0] * 8]))
+    assert np.array_equal(y[0], np.array(wv))
+
+
+# --------------------------------------------------------------------------
+# RMSNorm
+# --------------------------------------------------------------------------
+W8 = [0.5, -0.75, 1.0, 1.25, -1.5, 1.75, 2.0, 0.125]
+
+
+@pytest.mark.parametrize("dt", ["bf16", "f32"])
+def test_rmsnorm_constant_row_gives_w(dt):
+    """A row of 2s has mean square 4; with eps = 0, out = 2/2 * w = w (catches a
+    1/(h-1) mean, a wrong weight index)."""
+    mk = bf16 if dt == "bf16" else f32
+    _, _, y = oracle.rmsnorm(mk([[2.0] * 8] * 4), mk(W8), eps=0.0, want_y=True)
+    assert np.array_equal(y, np.tile(np.array(W8), (4, 1)))
+
+
+def test_rmsnorm_output_rounds_once_from_the_exact_value():
+    """x = e_0 of length 8 and w = 1 give y_0 = 1/sqrt(1/8 + eps).  eps is set so
+    that y_0 sits 2^-30 (relative) above the bf16 midpoint 1 + 2^-8: the single
+    rounding goes up to 1 + 2^-7 (0x3f81); rounding through f32 first would land
+    on the midpoint and tie down to 1.0.  Just below the midpoint it goes down."""
+    x = bf16([[1.0] + [0.0] * 7])
+    w = bf16([1.0] * 8)
+    for target, bits in (((1 + 2.0 ** -8) * (1 + 2.0 ** -30), 0x3F81),
+                         ((1 + 2.0 ** -8) * (1 - 2.0 ** -30), 0x3F80)):
+        eps = 1.0 / target ** 2 - 1.0 / 8
+        out, _, y = oracle.rmsnorm(x, w, eps=eps, want_y=True)
+        assert abs(y[0, 0] / target - 1) < 1e-14
+        assert out[0, 0] == bits
+
+
+def test_rmsnorm_alternating_row():
+    """[a, -a, a, -a, ...] has mean square a^2: out_j = sign_j * w_j."""
+    a = 3.0
+    x = bf16([[a if j % 2 == 0 else -a for j in range(8)]])
+    _, _, y = oracle.rmsnorm(x, bf16(W8), eps=0.0, want_y=True)
+    assert np.allclose(y[0], [w if j % 2 == 0 else -w for j, w in enumerate(W8)], rtol=0,
+                       atol=1e-15)
+
+
+def test_rmsnorm_eps_inside_the_sqrt():
+    """Constant row c = 1 with eps = 3: inv = 1/sqrt(1 + 3) = 1/2 exactly.
+    eps outside the sqrt (1/(1+3)) or added to the rms would give 1/4."""
+    _, _, y = oracle.rmsnorm(bf16([[1.0] * 8]), bf16(W8), eps=3.0, want_y=True)
+    assert np.array_equal(y[0], np.array(W8) / 2)
+
+
+def test_rmsnorm_gemma_adds_one_to_w():
+    """gemma with w equals plain with w + 1 (values chosen so w + 1 is exact)."""
+    xs, _, _ = synth.rmsnorm_inputs(6, 64, 9, torch.bfloat16, residual=False)
+    x = synth.to_oracle(xs)
+    w = np.arange(64) / 64.0 - 0.5
+    o1, _, y1 = oracle.rmsnorm(x, bf16(list(w)), gemma=True, want_y=True)
+    o2, _, y2 = oracle.rmsnorm(x, bf16(list(w + 1.0)), gemma=False, want_y=True)
+    assert np.array_equal(o1, o2) and np.array_equal(y1, y2)
+    o3, _, _ = oracle.rmsnorm(x, bf16(list(w)), gemma=False)
+    assert not np.array_equal(o1, o3)
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_rmsnorm_zero_residual_reduces_to_plain(dtype):
+    x, _, w = synth.rmsnorm_inputs(16, 96, 12, dtype, residual=False)
+    zero = torch.zeros_like(x)
+    o1, r1, y1 = oracle.rmsnorm(synth.to_oracle(x), synth.to_oracle(w),
+                                residual=synth.to_oracle(zero), want_y=True)
+    o2, _, y2 = oracle.rmsnorm(synth.to_oracle(x), synth.to_oracle(w), want_y=True)
+    assert np.array_equal(o1, o2) and np.array_equal(y1, y2)
+    assert np.array_equal(r1, synth.to_oracle(x))
+
+
+def test_rmsnorm_scale_invariance():
+    """With eps = 0, RMSNorm(4x) = RMSNorm(x) exactly (power-of-two scaling)."""
+    x, _, w = synth.rmsnorm_inputs(8, 40, 13, torch.float32, residual=False)
+    _, _, y1 = oracle.rmsnorm(synth.to_oracle(x), synth.to_oracle(w), eps=0.0, want_y=True)
+    _, _, y2 = oracle.rmsnorm(synth.to_oracle(x * 4), synth.to_oracle(w), eps=0.0, want_y=True)
+    assert np.allclose(y1, y2, rtol=1e-15, atol=0)
+
+
+def test_rmsnorm_brute_force_4x8():
+    """4x8 random rows against a 50-digit evaluation of sum/sqrt, element by element."""
+    mpmath.mp.dps = 50
+    xt, rt, wt = synth.rmsnorm_inputs(4, 8, 21, torch.bfloat16)
+    x, r, w = synth.to_oracle(xt), synth.to_oracle(rt), synth.to_oracle(wt)
+    out, res_out, y = oracle.rmsnorm(x, w, residual=r, eps=1e-6, gemma=True, want_y=True)
+    xv, rv, wv = bf16_to_f64(x), bf16_to_f64(r), bf16_to_f64(w)
+    for i in range(4):
+        v = [_nearest_bf16_exact(float(Fraction(xv[i, j]) + Fraction(rv[i, j]))) for j in range(8)]
+        assert list(res_out[i]) == v
+        vals = [mpmath.mpf(float(bf16_to_f64(np.array([b], np.uint16))[0])) for b in v]
+        ms = sum(t * t for t in vals) / 8
+        inv = 1 / mpmath.sqrt(ms + mpmath.mpf(1e-6))
+        for j in range(8):
+            exact = vals[j] * inv * (mpmath.mpf(float(wv[j])) + 1)
+            assert abs(y[i, j] - float(exact)) <= 4e-16 * abs(float(exact))
+
+
+# --------------------------------------------------------------------------
+# Q/K RMSNorm + NeoX RoPE
+# --------------------------------------------------------------------------
+def _qk_small(tokens=3, hq=2, hk=1, D=16, seed=31):
+    q, k, wq, wk, pos = synth.qk_inputs(tokens, hq, hk, D, seed, torch.bfloat16, torch.float32)
+    return (synth.to_oracle(q), synth.to_oracle(k), synth.to_oracle(wq), synth.to_oracle(wk),
+            pos.numpy())
+
+
+def test_rope_position_zero_is_the_plain_head_norm():
+    """At position 0 every angle is 0: the output is the per-head RMSNorm
+    (checked against the separately pinned RMSNorm of the same head rows)."""
+    q, k, wq, wk, _ = _qk_small(tokens=4, hq=3, hk=2, D=32)
+    wqb = synth.to_oracle(torch.from_numpy(wq).to(torch.bfloat16))
+    wkb = synth.to_oracle(torch.from_numpy(wk).to(torch.bfloat16))
+    qo, ko, qy, ky, _, _ = oracle.qk_norm_rope(q, k, wqb, wkb, np.zeros(4, np.int32), want_y=True)
+    ro, _, ry = oracle.rmsnorm(q.reshape(-1, 32), wqb, want_y=True)
+    assert np.array_equal(qo.reshape(-1, 32), ro) and np.array_equal(qy.reshape(-1, 32), ry)
+    ro, _, ry = oracle.rmsnorm(k.reshape(-1, 32), wkb, want_y=True)
+    assert np.array_equal(ko.reshape(-1, 32), ro) and np.array_equal(ky.reshape(-1, 32), ry)
+
+
+def test_rope_preserves_each_pair_norm():
+    q, k, wq, wk, _ = _qk_small(tokens=5, hq=2, hk=2, D=64)
+    pos = np.array([0, 1, 77, 4096, 26597], np.int32)
+    _, _, qy, ky, _, _ = oracle.qk_norm_rope(q, k, wq, wk, pos, want_y=True)
+    _, _, q0, k0, _, _ = oracle.qk_norm_rope(q, k, wq, wk, np.zeros(5, np.int32), want_y=True)
+    for yr, y0 in ((qy, q0), (ky, k0)):
+        a = yr[..., :32] ** 2 + yr[..., 32:] ** 2
+        b = y0[..., :32] ** 2 + y0[..., 32:] ** 2
+        assert np.allclose(a, b, rtol=1e-12, atol=0)
+
+
+def _onehot_case(idx, p, D=128, theta=10000.0, wq=None):
+    """One q head whose only nonzero element is at idx (value 1), eps = 0, so the
+    normed vector is sqrt(D) * w_idx at idx."""
+    q = np.zeros((1, 1, D), np.float32)
+    q[0, 0, idx] = 1.0
+    q = synth.to_oracle(torch.from_numpy(q).to(torch.bfloat16))
+    k = q.copy()
+    if wq is None:
+        wq = (1.0 + np.arange(D) / 256.0).astype(np.float32)  # w_i != w_{i+D/2}
+    _, _, qy, _, _, _ = oracle.qk_norm_rope(q, k, wq, wq, np.array([p], np.int32), eps=0.0,
+                                            theta=theta, want_y=True)
+    return qy[0, 0], wq
+
+
+def test_rope_rotation_direction_and_pairing():
+    """One-hot at i = 0 (frequency 1) and position 1: the pair (0, 64) becomes
+    n*(cos 1, sin 1) -- rotate-half pairing, positive sine on the second half,
+    weight of the first element (norm before rotation); all else stays 0."""
+    y, w = _onehot_case(0, 1)
+    n = math.sqrt(128) * float(w[0])
+    assert abs(y[0] - n * math.cos(1.0)) < 1e-13 and abs(y[64] - n * math.sin(1.0)) < 1e-13
+    rest = np.delete(y, [0, 64])
+    assert np.all(rest == 0)
+
+
+def test_rope_second_half_rotates_the_other_way():
+    """One-hot at 64 + 5: y_5 = -n sin(a), y_69 = n cos(a) with a = p * theta^(-10/128)."""
+    p = 3
+    y, w = _onehot_case(69, p)
+    n = math.sqrt(128) * float(w[69])
+    a = p * 10000.0 ** (-10 / 128)
+    assert abs(y[5] + n * math.sin(a)) < 1e-13 and abs(y[69] - n * math.cos(a)) < 1e-13
+
+
+def test_rope_frequency_exponent():
+    """i = 32 of D = 128: freq = 10000^(-64/128) = 1/100, so position 100 turns
+    the pair (32, 96) by exactly 1 radian; theta = 500, i = 16: freq = 500^(-1/4)."""
+    y, w = _onehot_case(32, 100)
+    n = math.sqrt(128) * float(w[32])
+    assert abs(y[32] - n * math.cos(1.0)) < 1e-12 and abs(y[96] - n * math.sin(1.0)) < 1e-12
+    y, w = _onehot_case(16, 7, theta=500.0)
+    n = math.sqrt(128) * float(w[16])
+    a = 7 * 500.0 ** -0.25
+    assert abs(y[16] - n * math.cos(a)) < 1e-12 and abs(y[80] - n * math.sin(a)) < 1e-12
+
+
+def test_rope_q_and_k_use_their_own_weights_and_heads():
+    """Two q heads and one k head with one-hot inputs at distinct indices and
+    distinct weights: each output is the closed form with its own tensor's weight."""
+    D = 16
+    q = np.zeros((2, 2, D), np.float32)
+    k = np.zeros((2, 1, D), np.float32)
+    q[:, 0, 1] = 1.0
+    q[:, 1, 2] = 1.0
+    k[:, 0, 3] = 1.0
+    qb = synth.to_oracle(torch.from_numpy(q).to(torch.bfloat16))
+    kb = synth.to_oracle(torch.from_numpy(k).to(torch.bfloat16))
+    wq = (1.0 + np.arange(D) / 32.0).astype(np.float32)
+    wk = (2.0 - np.arange(D) / 32.0).astype(np.float32)
+    pos = np.array([5, 9], np.int32)
+    _, _, qy, ky, _, _ = oracle.qk_norm_rope(qb, kb, wq, wk, pos, eps=0.0, theta=10.0, want_y=True)
+    s = math.sqrt(D)
+    for t, p in enumerate(pos):
+        for (y, i, wv) in ((qy[t, 0], 1, wq), (qy[t, 1], 2, wq), (ky[t, 0], 3, wk)):
+            a = p * 10.0 ** (-2 * i / D)
+            assert abs(y[i] - s * float(wv[i]) * math.cos(a)) < 1e-12
+            assert abs(y[i + D // 2] - s * float(wv[i]) * math.sin(a)) < 1e-12
+
+
+def test_rope_relative_position_invariance():
+    """<R(p+s) q, R(p'+s) k> = <R(p) q, R(p') k> for every head pair."""
+    q, k, wq, wk, _ = _qk_small(tokens=2, hq=2, hk=2, D=32, seed=41)
+
+    def dots(p0, p1):
+        _, _, qy, ky, _, _ = oracle.qk_norm_rope(q[:1], k[1:], wq, wk, np.array([p0], np.int32),
+                                                 want_y=True)
+        _, _, _, ky1, _, _ = oracle.qk_norm_rope(q[:1], k[1:], wq, wk, np.array([p1], np.int32),
+                                                 want_y=True)
+        return np.einsum("hd,gd->hg", qy[0], ky1[0])
+
+    base = dots(10, 3)
+    for s in (1, 250, 9000):
+        assert np.allclose(dots(10 + s, 3 + s), base, rtol=0, atol=1e-9)
+
+
+def test_rope_strided_input_matches_dense():
+    """q/k given as views into a wider row (token stride > heads*D)."""
+    q, k, wq, wk, pos = _qk_small(tokens=3, hq=2, hk=2, D=16)
+    wide = np.zeros((3, 7, 16), np.uint16)
+    wide[:, 1:3] = q
+    wide[:, 4:6] = k
+    a = oracle.qk_norm_rope(q, k, wq, wk, pos)
+    b = oracle.qk_norm_rope(wide[:, 1:3], wide[:, 4:6], wq, wk, pos)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+def test_rope_brute_force_4_tokens():
+    """4 tokens x 1 head x 8 dims (pairs (i, i+4)) against a 50-digit evaluation."""
+    mpmath.mp.dps = 50
+    q, k, wq, wk, _ = _qk_small(tokens=4, hq=1, hk=1, D=8, seed=51)
+    pos = np.array([0, 3, 1000, 26597], np.int32)
+    _, _, qy, _, _, _ = oracle.qk_norm_rope(q, k, wq, wk, pos, eps=1e-6, theta=10000.0,
+                                            want_y=True)
+    qv = bf16_to_f64(q)
+    for t in range(4):
+        v = [mpmath.mpf(float(a)) for a in qv[t, 0]]
+        inv = 1 / mpmath.sqrt(sum(a * a for a in v) / 8 + mpmath.mpf(1e-6))
+        n = [v[j] * inv * mpmath.mpf(float(wq[j])) for j in range(8)]
+        for i in range(4):
+            # the frequency is the double pow result (the method's own rounding)
+            f = mpmath.mpf(10000.0 ** (-2.0 * i / 8))
+            a = int(pos[t]) * f
+            e0 = n[i] * mpmath.cos(a) - n[i + 4] * mpmath.sin(a)
+            e1 = n[i] * mpmath.sin(a) + n[i + 4] * mpmath.cos(a)
+            assert abs(qy[t, 0, i] - float(e0)) < 1e-11
+            assert abs(qy[t, 0, i + 4] - float(e1)) < 1e-11
+
+
+# --------------------------------------------------------------------------
+# LayerNorm + adaLN modulation
+# --------------------------------------------------------------------------
+def test_ln_row_1_to_8_closed_form():
+    """x = 1..8: mean 4.5, biased variance 5.25; with eps = 1, sqrt(6.25) = 2.5,
+    so xhat_j = (j - 4.5) / 2.5 (an unbiased variance or eps outside the sqrt
+    would differ)."""
+    x = bf16([[float(j) for j in range(1, 9)]])
+    zero = bf16([0.0] * 8)
+    _, y, _ = oracle.ln_modulate(x, zero, zero, eps=1.0, want_y=True)
+    assert np.allclose(y[0], (np.arange(1, 9) - 4.5) / 2.5, rtol=0, atol=1e-15)
+    _, y, _ = oracle.ln_modulate(x, zero, zero, eps=0.0, want_y=True)
+    assert np.allclose(y[0], (np.arange(1, 9) - 4.5) / math.sqrt(5.25), rtol=0, atol=1e-15)
+
+
+def test_ln_rows_have_mean_zero_and_variance_var_over_var_plus_eps():
+    xt, _, _ = synth.ln_inputs(32, 3072, 61, torch.bfloat16)
+    x = synth.to_oracle(xt)
+    zero = bf16([0.0] * 3072)
+    eps = 1e-2
+    _, y, _ = oracle.ln_modulate(x, zero, zero, eps=eps, want_y=True)
+    xv = bf16_to_f64(x)
+    var = xv.var(axis=1)
+    assert np.all(np.abs(y.mean(axis=1)) < 1e-12)
+    assert np.allclose(y.var(axis=1), var / (var + eps), rtol=1e-12, atol=0)
+
+
+def test_ln_scale_minus_one_gives_shift_and_constant_row_gives_shift():
+    xt, st, _ = synth.ln_inputs(4, 64, 62, torch.bfloat16, samples=2)
+    x, shift = synth.to_oracle(xt), synth.to_oracle(st)
+    minus1 = bf16([[-1.0] * 64] * 2)
+    out, y, _ = oracle.ln_modulate(x, shift, minus1, rows_per_sample=2, want_y=True)
+    assert np.array_equal(out, shift[[0, 0, 1, 1]])  # row r uses sample r // 2
+    const = bf16([[0.75] * 64] * 4)
+    scale = synth.to_oracle(synth.tensor(62, 99, (2, 64), torch.bfloat16, std=0.1))
+    out, y, _ = oracle.ln_modulate(const, shift, scale, rows_per_sample=2, want_y=True)
+    assert np.array_equal(out, shift[[0, 0, 1, 1]])
+
+
+def test_ln_zero_modulation_is_plain_ln_and_shift_invariant():
+    """scale = shift = 0 gives plain LN: odd in x and invariant to adding a
+    constant (to 1e-12), with the mean/variance pins above fixing its values."""
+    xt, _, _ = synth.ln_inputs(8, 256, 63, torch.float32)
+    x = synth.to_oracle(xt)
+    zero = f32([0.0] * 256)
+    _, y, _ = oracle.ln_modulate(x, zero, zero, want_y=True)
+    _, yn, _ = oracle.ln_modulate(-x, zero, zero, want_y=True)
+    _, ys, _ = oracle.ln_modulate(x + np.float32(8.0), zero, zero, want_y=True)
+    assert np.array_equal(yn, -y)
+    assert np.allclose(ys, y, rtol=0, atol=1e-5)  # x + 8 is rounded to f32 once
+
+
+def test_ln_modulation_uses_one_plus_scale():
+    """y = xhat * (1 + scale) + shift: with scale = 1, shift = 0.5 the result is
+    2 * xhat + 0.5 (scale used alone would give xhat + 0.5)."""
+    x = bf16([[float(j) for j in range(1, 9)]])
+    _, y, _ = oracle.ln_modulate(x, bf16([0.5] * 8), bf16([1.0] * 8), eps=1.0, want_y=True)
+    assert np.allclose(y[0], 2 * (np.arange(1, 9) - 4.5) / 2.5 + 0.5, rtol=0, atol=1e-15)
+
+
+# --------------------------------------------------------------------------
+# silu_and_mul
+# --------------------------------------------------------------------------
+def test_silu_closed_forms_and_operand_order():
+    """Row layout [gate | up].  silu(0) = 0; up = 0 gives 0; up = 1 gives
+    silu(gate); silu(ln 3) = (3/4) ln 3 (with e^{+a} it would be ln3/4)."""
+    ln3 = math.log(3.0)
+    a = [0.0, ln3, -2.0, 40.0]
+    x = np.array([a + [1.0, 1.0, 1.0, 1.0], a + [0.0, 0.0, 0.0, 0.0]], np.float32)
+    out, y = oracle.silu_and_mul(x, want_y=True)
+    assert y[0, 0] == 0.0
+    # the stored gate is ln 3 rounded to f32 (off by < 6e-8; silu' < 1 there)
+    assert abs(y[0, 1] - 0.75 * ln3) < 1e-7
+    assert abs(y[0, 2] - (-2.0 / (1 + math.e ** 2))) < 1e-15
+    assert abs(y[0, 3] - 40.0 * (1 - math.exp(-40.0))) < 1e-12
+    assert np.all(y[1] == 0.0)
+
+
+def test_silu_odd_part_identity():
+    """silu(a) - silu(-a) = a for every a (catches a sign slip in the exponent)."""
+    g = synth.tensor(71, 0, (1, 64), torch.float32).numpy()
+    ones = np.ones_like(g)
+    _, yp = oracle.silu_and_mul(np.concatenate([g, ones], axis=1), want_y=True)
+    _, ym = oracle.silu_and_mul(np.concatenate([-g, ones], axis=1), want_y=True)
+    assert np.allclose(yp - ym, g.astype(np.float64), rtol=1e-15, atol=1e-15)
+
+
+def test_silu_up_multiplies():
+    """out is linear in up: doubling the up half doubles y exactly."""
+    x = synth.tensor(72, 0, (3, 32), torch.float32).numpy()
+    x2 = x.copy()
+    x2[:, 16:] *= 2
+    _, y1 = oracle.silu_and_mul(x, want_y=True)
+    _, y2 = oracle.silu_and_mul(x2, want_y=True)
+    assert np.array_equal(y2, 2 * y1)

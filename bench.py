@@ -1,0 +1,582 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused row-normalisation path on GB300.
+
+One step = one pass of the whole hot path, each op on its full synthetic
+workload, all launched through the C ABI (via the Python binding) on one
+stream:
+  1. RMSNorm f32 [64, 1024]                     (no residual, gemma off)
+  2. add + RMSNorm bf16 [8192, 5120], gemma off  (residual updated in place)
+  3. add + RMSNorm bf16 [8192, 5120], gemma on   (a second buffer set)
+  4. Q/K RMSNorm + NeoX RoPE bf16, Q and K [26598, 24, 128], theta 1e4
+  5. LayerNorm + adaLN modulation bf16 [26598, 3072]
+  6. add + RMSNorm bf16 [256, 8192]             (largest decode cell)
+  7. silu_and_mul bf16 [256, 2 * 24576]         (largest decode cell)
+The metric is achieved HBM throughput: algorithmic bytes (each input read
+once, each output written once) per second, summed over the step; rows/s and
+per-kernel GB/s with their fractions of the HBM peak are reported beside it.
+The step's footprint (~1.7 GB) is far larger than the 129 MB L2 and every
+large kernel's operands exceed it, so every launch starts from HBM.
+
+Usage:  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+N > 1 runs under torchrun, one rank per GPU, each rank on its own shard (weak
+scaling; RoPE positions continue across ranks).  --impl reference times the CPU
+oracle (the plain double-precision definition) on the host instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "achieved HBM GB/s and % of GB300 peak per fused norm kernel; rows/sec"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+KERNEL_SOURCES = {
+    "qk_norm_rope": "normalisation_rope_transformers_gb300/csrc/qk_norm_rope.cu",
+    "add_rmsnorm": "normalisation_rope_transformers_gb300/csrc/rmsnorm.cu",
+    "rmsnorm": "normalisation_rope_transformers_gb300/csrc/rmsnorm.cu",
+    "ln_modulate": "normalisation_rope_transformers_gb300/csrc/ln_modulate.cu",
+    "silu_and_mul": "normalisation_rope_transformers_gb300/csrc/silu_and_mul.cu",
+}
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=3000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--e2e-steps", type=int, default=10)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-decode-sweep", action="store_true")
+    return p.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# Workload
+# ---------------------------------------------------------------------------
+class Call:
+    """One launch of the step: its inputs, outputs, byte count and row count."""
+
+    def __init__(self, name, kernel, fn, inputs, outputs, nbytes, rows, rows_unit):
+        self.name, self.kernel, self.fn = name, kernel, fn
+        self.inputs, self.outputs = inputs, outputs  # dicts name -> device tensor
+        self.nbytes, self.rows, self.rows_unit = nbytes, rows, rows_unit
+
+
+def nbytes(*ts):
+    return sum(t.numel() * t.element_size() for t in ts if t is not None)
+
+
+def build_step(nr, synth, torch, device, rank):
+    """Device buffers and the seven calls of one step for this rank."""
+    bf16, f32 = torch.bfloat16, torch.float32
+    calls = []
+
+    c = synth.RMSNORM_F32
+    x, _, w = synth.rmsnorm_inputs(c["rows"], c["hidden"], c["seed"], f32, residual=False)
+    x, w = x.to(device), w.to(device)
+    out = torch.empty_like(x)
+    calls.append(Call("rmsnorm_f32_64x1024", "rmsnorm",
+                      lambda x=x, w=w, out=out, eps=c["eps"]: nr.rmsnorm(x, w, eps=eps, out=out),
+                      {"x": x, "w": w}, {"out": out}, nbytes(x, w, out), c["rows"], "rows"))
+
+    c = synth.ADD_RMSNORM
+    for gemma in (False, True):
+        x, res, w = synth.rmsnorm_inputs(c["rows"], c["hidden"], c["seed"], bf16)
+        x, res, w = x.to(device), res.to(device), w.to(device)
+        out = torch.empty_like(x)
+        calls.append(Call("add_rmsnorm_bf16_8192x5120_gemma%d" % gemma, "add_rmsnorm",
+                          lambda x=x, w=w, res=res, out=out, g=gemma, eps=c["eps"]:
+                          nr.rmsnorm(x, w, residual=res, eps=eps, gemma=g, out=out),
+                          {"x": x, "w": w, "residual": res}, {"out": out, "residual": res},
+                          nbytes(x, w, res) + nbytes(out, res), c["rows"], "rows"))
+
+    c = synth.QK_NORM_ROPE
+    q, k, wq, wk, pos = synth.qk_inputs(c["tokens"], c["hq"], c["hk"], c["head_dim"], c["seed"],
+                                        bf16, f32, pos_start=rank * c["tokens"])
+    q, k, wq, wk, pos = (t.to(device) for t in (q, k, wq, wk, pos))
+    qo, ko = torch.empty_like(q), torch.empty_like(k)
+    calls.append(Call("qk_norm_rope_bf16_26598x24x128", "qk_norm_rope",
+                      lambda q=q, k=k, wq=wq, wk=wk, pos=pos, qo=qo, ko=ko, eps=c["eps"],
+                      theta=c["theta"]: nr.qk_norm_rope(q, k, wq, wk, pos, eps=eps, theta=theta,
+                                                        q_out=qo, k_out=ko),
+                      {"q": q, "k": k, "wq": wq, "wk": wk, "positions": pos},
+                      {"q_out": qo, "k_out": ko}, nbytes(q, k, wq, wk, pos, qo, ko),
+                      c["tokens"] * (c["hq"] + c["hk"]), "head rows"))
+
+    c = synth.LN_MODULATE
+    x, sh, sc = synth.ln_inputs(c["rows"], c["hidden"], c["seed"], bf16)
+    x, sh, sc = x.to(device), sh.to(device), sc.to(device)
+    out = torch.empty_like(x)
+    calls.append(Call("ln_modulate_bf16_26598x3072", "ln_modulate",
+                      lambda x=x, sh=sh, sc=sc, out=out, eps=c["eps"]:
+                      nr.ln_modulate(x, sh, sc, eps=eps, out=out),
+                      {"x": x, "shift": sh, "scale": sc}, {"out": out}, nbytes(x, sh, sc, out),
+                      c["rows"], "rows"))
+
+    c = synth.DECODE
+    rows, hidden = max(c["rows"]), max(c["hidden"])
+    x, res, w = synth.rmsnorm_inputs(rows, hidden, c["seed"], bf16)
+    x, res, w = x.to(device), res.to(device), w.to(device)
+    out = torch.empty_like(x)
+    calls.append(Call("add_rmsnorm_bf16_256x8192", "add_rmsnorm",
+                      lambda x=x, w=w, res=res, out=out, eps=c["eps"]:
+                      nr.rmsnorm(x, w, residual=res, eps=eps, out=out),
+                      {"x": x, "w": w, "residual": res}, {"out": out, "residual": res},
+                      nbytes(x, w, res) + nbytes(out, res), rows, "rows"))
+    g = synth.silu_inputs(rows, 3 * hidden, c["seed"], bf16).to(device)
+    out = torch.empty((rows, 3 * hidden), dtype=bf16, device=device)
+    calls.append(Call("silu_and_mul_bf16_256x49152", "silu_and_mul",
+                      lambda g=g, out=out: nr.silu_and_mul(g, out=out), {"x": g}, {"out": out},
+                      nbytes(g, out), rows, "rows"))
+    return calls
+
+
+# ---------------------------------------------------------------------------
+# Clocks during the timed region
+# ---------------------------------------------------------------------------
+CLOCK_FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+                "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+                "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+
+class ClockSampler:
+    def __init__(self, gpu_id):
+        self.gpu_id = gpu_id
+        self.lines = []
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_id), "--query-gpu=" + ",".join(CLOCK_FIELDS),
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self):
+        return time.time()
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ts, line in self.lines:
+            if not (t0 <= ts <= t1):
+                continue
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) != len(CLOCK_FIELDS):
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def gpu_id_for(torch, device):
+    try:
+        u = torch.cuda.get_device_properties(device).uuid
+        s = str(u)
+        return s if s.startswith("GPU-") else "GPU-" + s
+    except Exception:
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        return vis.split(",")[device.index or 0] if vis else str(device.index or 0)
+
+
+# ---------------------------------------------------------------------------
+# Peaks and ncu traffic
+# ---------------------------------------------------------------------------
+def hbm_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def source_hash(rel):
+    h = hashlib.sha256()
+    for path in (rel, "normalisation_rope_transformers_gb300/csrc/nr_common.cuh"):
+        with open(os.path.join(ROOT, path), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel, units):
+    """DRAM bytes per launch of `kernel` from the committed ncu capture, scaled
+    to `units` if the capture ran a smaller case; None if the kernel's source
+    changed since the capture."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            rec = json.load(f)[kernel]
+    except (OSError, KeyError, ValueError):
+        return None
+    if rec.get("source_hash") != source_hash(KERNEL_SOURCES[kernel]):
+        return None
+    return rec["dram_bytes_per_launch"] * units / rec["units"]
+
+
+# ---------------------------------------------------------------------------
+# Our arm
+# ---------------------------------------------------------------------------
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+
+    import normalisation_rope_transformers_gb300 as nr
+    import synth
+
+    calls = build_step(nr, synth, torch, device, rank)
+    step_bytes = sum(c.nbytes for c in calls)
+    stream = torch.cuda.current_stream(device)
+
+    def step():
+        for c in calls:
+            c.fn()
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(device)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    barrier()
+
+    # Timed region: K steps, events around each call (on the launching stream).
+    K = args.steps
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in calls] for _ in range(K)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for row in ev:  # create the CUDA events now, outside the timed region
+        for a, b in row:
+            a.record(stream)
+            b.record(stream)
+    barrier()
+    sampler = ClockSampler(gpu_id_for(torch, device))
+    with sampler:
+        barrier()
+        t_wall0 = time.time()
+        start.record(stream)
+        for i in range(K):
+            for j, c in enumerate(calls):
+                ev[i][j][0].record(stream)
+                c.fn()
+                ev[i][j][1].record(stream)
+        end.record(stream)
+        barrier()
+        t_wall1 = time.time()
+    clocks = sampler.summary(t_wall0, t_wall1)
+    elapsed_ms = start.elapsed_time(end)
+    per_call_ms = [statistics.fmean(ev[i][j][0].elapsed_time(ev[i][j][1]) for i in range(K))
+                   for j in range(len(calls))]
+    if world > 1:
+        t = torch.tensor([elapsed_ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = t.item()
+
+    ms_per_step = elapsed_ms / K
+    value = world * step_bytes * K / (elapsed_ms * 1e-3) / 1e9
+    peak, peak_kind = hbm_peak()
+
+    kernels = {}
+    for c, ms in zip(calls, per_call_ms):
+        gbs = c.nbytes / (ms * 1e-3) / 1e9
+        kernels[c.name] = {"us": round(ms * 1e3, 2), "bytes": c.nbytes, "GB_s": round(gbs, 1),
+                           "frac_of_measured": round(gbs / peak, 4),
+                           "frac_of_nominal_8TBs": round(gbs / NOMINAL_HBM_GBS, 4),
+                           "rows_per_s": round(c.rows / (ms * 1e-3), 1), "rows_unit": c.rows_unit}
+    # dominant kernel: largest share of the step's device time
+    dom = max(range(len(calls)), key=lambda j: per_call_ms[j])
+    dc = calls[dom]
+    achieved = dc.nbytes / (per_call_ms[dom] * 1e-3) / 1e9
+    traffic = ncu_traffic(dc.kernel, dc.rows)
+
+    e2e = run_e2e(args, torch, calls, device, world, barrier, step_bytes)
+
+    result = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": K,
+        "warmup": max(args.warmup, 3), "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": "dit_norm_step: " + " + ".join(c.name for c in calls),
+                   "storage": "bf16 (f32 for the 64x1024 RMSNorm)",
+                   "bytes_per_step": step_bytes,
+                   "rows_per_step": {c.name: c.rows for c in calls},
+                   "l2": "no flush: step footprint %.2f GB >> 129 MB L2; each large call's "
+                         "operands exceed L2" % (step_bytes / 1e9),
+                   "parallelism": "dp%d (independent row/token shards, no collective)" % world},
+        "roofline": {"bound": "hbm", "kernel": dc.name, "achieved": round(achieved, 1),
+                     "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4),
+                     "traffic": None if traffic is None else int(traffic),
+                     "algorithmic_bytes": dc.nbytes},
+        "kernels": kernels,
+        "rows_per_s": round(world * sum(c.rows for c in calls) / (ms_per_step * 1e-3), 1),
+        "e2e": e2e,
+        "gpu_launches": K * len(calls),
+        "clocks": clocks,
+    }
+    if rank == 0 and not args.no_decode_sweep:
+        result["decode_sweep"] = decode_sweep(nr, synth, torch, device)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(fraction=0.5)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+
+
+def run_e2e(args, torch, calls, device, world, barrier, step_bytes):
+    """Same step through the public API with inputs in pinned host memory: each
+    step copies every input host->device, runs the seven calls and copies every
+    output device->host, all inside the timed region."""
+    h_in = [{k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True).copy_(v.cpu())
+             for k, v in c.inputs.items()} for c in calls]
+    h_out = [{k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in c.outputs.items()}
+             for c in calls]
+    h2d = sum(nbytes(*d.values()) for d in h_in)
+    d2h = sum(nbytes(*d.values()) for d in h_out)
+
+    def step():
+        for c, hi, ho in zip(calls, h_in, h_out):
+            for k, v in hi.items():
+                c.inputs[k].copy_(v, non_blocking=True)
+            c.fn()
+            for k, v in ho.items():
+                v.copy_(c.outputs[k], non_blocking=True)
+
+    step()
+    barrier()
+    n = max(args.e2e_steps, 1)
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(n):
+        step()
+    e.record()
+    barrier()
+    ms = s.elapsed_time(e)
+    if world > 1:
+        import torch.distributed as dist
+
+        t = torch.tensor([ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = t.item()
+    return {"value": round(world * step_bytes * n / (ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n,
+            "ms_per_step": round(ms / n, 3)}
+
+
+def decode_sweep(nr, synth, torch, device):
+    """Latency per call of add+RMSNorm and silu_and_mul over the decode grid:
+    hot (back-to-back, L2-warm) and cold (a 256 MB buffer written between calls,
+    only the call itself timed)."""
+    c = synth.DECODE
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+    out = {}
+    for rows in c["rows"]:
+        for hidden in c["hidden"]:
+            x, res, w = synth.rmsnorm_inputs(rows, hidden, c["seed"], torch.bfloat16)
+            x, res, w = x.to(device), res.to(device), w.to(device)
+            o = torch.empty_like(x)
+            g = synth.silu_inputs(rows, 3 * hidden, c["seed"], torch.bfloat16).to(device)
+            go = torch.empty((rows, 3 * hidden), dtype=torch.bfloat16, device=device)
+            for name, fn, nb in (
+                    ("add_rmsnorm", lambda: nr.rmsnorm(x, w, residual=res, out=o),
+                     nbytes(x, w, res) + nbytes(o, res)),
+                    ("silu_and_mul", lambda: nr.silu_and_mul(g, out=go), nbytes(g, go))):
+                for _ in range(5):
+                    fn()
+                torch.cuda.synchronize()
+                n = 200
+                s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                s.record()
+                for _ in range(n):
+                    fn()
+                e.record()
+                torch.cuda.synchronize()
+                hot_us = s.elapsed_time(e) * 1e3 / n
+                cold = []
+                for _ in range(20):
+                    flush.fill_(1)
+                    s.record()
+                    fn()
+                    e.record()
+                    torch.cuda.synchronize()
+                    cold.append(s.elapsed_time(e) * 1e3)
+                cold_us = statistics.median(cold)
+                out["%s_%dx%d" % (name, rows, hidden)] = {
+                    "hot_us": round(hot_us, 2), "cold_us": round(cold_us, 2), "bytes": nb,
+                    "hot_GB_s": round(nb / (hot_us * 1e-6) / 1e9, 1),
+                    "cold_GB_s": round(nb / (cold_us * 1e-6) / 1e9, 1)}
+    return out
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (cpu_baseline leg and the reference arm)
+# ---------------------------------------------------------------------------
+def prepare_oracle_step(fraction):
+    """Oracle calls over the first `fraction` of each workload's rows (at least
+    one row).  The generator is counter-based, so these inputs are exactly the
+    leading rows of the full workloads.  Returns [(fn, algorithmic bytes)], desc."""
+    import torch
+
+    import oracle
+    import synth
+
+    bf16, f32 = torch.bfloat16, torch.float32
+    o = synth.to_oracle
+    todo, desc = [], []
+
+    def rows_of(n):
+        return max(1, min(n, int(round(n * fraction))))
+
+    c = synth.RMSNORM_F32
+    r = rows_of(c["rows"])
+    x, _, w = synth.rmsnorm_inputs(r, c["hidden"], c["seed"], f32, residual=False)
+    todo.append((lambda a=o(x), b=o(w): oracle.rmsnorm(a, b), 2 * x.numel() * 4 + w.numel() * 4))
+    desc.append("rmsnorm_f32 %d/%d rows" % (r, c["rows"]))
+    c = synth.ADD_RMSNORM
+    r = rows_of(c["rows"])
+    x, res, w = synth.rmsnorm_inputs(r, c["hidden"], c["seed"], bf16)
+    for gemma in (False, True):
+        todo.append((lambda a=o(x), b=o(w), rr=o(res), g=gemma:
+                     oracle.rmsnorm(a, b, residual=rr, gemma=g),
+                     4 * r * c["hidden"] * 2 + c["hidden"] * 2))
+        desc.append("add_rmsnorm gemma%d %d/%d rows" % (gemma, r, c["rows"]))
+    c = synth.QK_NORM_ROPE
+    t = rows_of(c["tokens"])
+    q, k, wq, wk, pos = synth.qk_inputs(t, c["hq"], c["hk"], c["head_dim"], c["seed"], bf16, f32)
+    todo.append((lambda a=o(q), b=o(k), wa=o(wq), wb=o(wk), p=pos.numpy(), th=c["theta"]:
+                 oracle.qk_norm_rope(a, b, wa, wb, p, theta=th),
+                 4 * t * c["hq"] * c["head_dim"] * 2 + t * 4 + 2 * c["head_dim"] * 4))
+    desc.append("qk_norm_rope %d/%d tokens" % (t, c["tokens"]))
+    c = synth.LN_MODULATE
+    r = rows_of(c["rows"])
+    x, sh, sc = synth.ln_inputs(r, c["hidden"], c["seed"], bf16)
+    todo.append((lambda a=o(x), s1=o(sh), s2=o(sc): oracle.ln_modulate(a, s1, s2),
+                 2 * r * c["hidden"] * 2 + 2 * c["hidden"] * 2))
+    desc.append("ln_modulate %d/%d rows" % (r, c["rows"]))
+    c = synth.DECODE
+    rows, hidden = max(c["rows"]), max(c["hidden"])
+    r = rows_of(rows)
+    x, res, w = synth.rmsnorm_inputs(r, hidden, c["seed"], bf16)
+    todo.append((lambda a=o(x), b=o(w), rr=o(res): oracle.rmsnorm(a, b, residual=rr),
+                 4 * r * hidden * 2 + hidden * 2))
+    desc.append("add_rmsnorm %d/%d rows of 8192" % (r, rows))
+    g = synth.silu_inputs(r, 3 * hidden, c["seed"], bf16)
+    todo.append((lambda a=o(g): oracle.silu_and_mul(a), 3 * r * 3 * hidden * 2))
+    desc.append("silu_and_mul %d/%d rows" % (r, rows))
+    oracle._load()
+    return todo, "; ".join(desc)
+
+
+def time_oracle(todo):
+    secs, nb = 0.0, 0
+    for fn, b in todo:
+        t0 = time.perf_counter()
+        fn()
+        secs += time.perf_counter() - t0
+        nb += b
+    return secs, nb
+
+
+def cpu_baseline(fraction):
+    todo, desc = prepare_oracle_step(fraction)
+    secs, nb = time_oracle(todo)
+    return {"value": round(nb / secs / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": "one pass of the step over %.0f%% of each workload's rows (%s), "
+                      "single-threaded C oracle in double, %.1f s" % (100 * fraction, desc, secs)}
+
+
+def run_reference(args):
+    """The CPU oracle as the reference arm: each step is the oracle over a
+    sample of every workload in the step, sized so the whole run stays within
+    about two minutes."""
+    if int(os.environ.get("RANK", "0")) != 0:
+        return
+    steps, warm = args.steps, max(args.warmup, 3)
+    probe_fraction = 1.0 / 256
+    todo, _ = prepare_oracle_step(probe_fraction)
+    probe_s, _ = time_oracle(todo)
+    per_step_budget = min(2.0, 120.0 / (steps + warm))
+    fraction = max(1.0 / 26598, min(0.5, probe_fraction * per_step_budget / max(probe_s, 1e-6)))
+    todo, desc = prepare_oracle_step(fraction)
+    for _ in range(warm):
+        time_oracle(todo)
+    total_s, total_b = 0.0, 0
+    for _ in range(steps):
+        s, b = time_oracle(todo)
+        total_s += s
+        total_b += b
+    value = total_b / total_s / 1e9
+    sample = "each step: %s (%.3g of each workload's rows), single-threaded C oracle" % (
+        desc, fraction)
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": steps, "warmup": warm,
+        "ms_per_step": round(1e3 * total_s / steps, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "dit_norm_step (oracle on a row sample of each call)"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

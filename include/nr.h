@@ -1,0 +1,172 @@
+/*
+ * nr.h -- C ABI of the fused row-normalisation library (libnormrope.so).
+ *
+ * Four ops that sit between a transformer's GEMMs, as hand-written CUDA
+ * kernels for sm_103a:
+ *   nr_rmsnorm        RMSNorm, optionally with the fused residual add (gemma w+1)
+ *   nr_qk_norm_rope   per-head Q/K RMSNorm fused with NeoX rotary embedding
+ *   nr_ln_modulate    LayerNorm (no affine) fused with DiT adaLN modulation
+ *   nr_silu_and_mul   silu(gate) * up
+ *
+ * Conventions shared by every entry point
+ *   - Pointers are DEVICE pointers (CUDA global memory) owned by the caller; the
+ *     library allocates nothing, keeps no state between calls and frees nothing.
+ *   - Every pointer must be 16-byte aligned, and every row start (row stride in
+ *     bytes) a multiple of 16, so that each thread moves 128-bit vectors.
+ *   - Work is enqueued asynchronously on `stream` (0 = the legacy default
+ *     stream); the call returns once the kernel is launched.
+ *   - All arithmetic is f32 (bf16 values are widened exactly); each stored
+ *     output is rounded once, to nearest even, to its storage dtype.
+ *   - Arguments are validated on the host before anything is launched.  A
+ *     rejected call launches nothing and returns a non-zero nr_status; the
+ *     reason is available from nr_last_error_message() on the same thread.
+ *     A call with zero rows (tokens) returns NR_OK without launching and
+ *     without looking at its pointers.  No C++ exception crosses this ABI.
+ *   - NR_ERR_CUDA reports a failed launch (cudaGetLastError after it); like
+ *     any CUDA error it can also surface a fault left by earlier work.
+ *
+ * Citations name the page and the section each operation follows.
+ */
+#ifndef NR_H
+#define NR_H
+
+#include <stdint.h>
+
+#include <cuda_runtime_api.h> /* cudaStream_t */
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum nr_status {
+  NR_OK = 0,
+  NR_ERR_NULL = 1,        /* a required pointer is NULL */
+  NR_ERR_SHAPE = 2,       /* a size is negative or zero where it must be positive, or too large */
+  NR_ERR_DTYPE = 3,       /* unknown dtype code, or a dtype combination that is not offered */
+  NR_ERR_ALIGN = 4,       /* a pointer or row stride is not a multiple of 16 bytes */
+  NR_ERR_ALIAS = 5,       /* an output overlaps an input (or another output) it may not overlap */
+  NR_ERR_UNSUPPORTED = 6, /* a valid size the kernels do not cover (e.g. hidden % 8 for bf16) */
+  NR_ERR_CUDA = 7,        /* the launch failed; see nr_last_error_message() */
+  NR_ERR_VALUE = 8        /* a scalar is out of range (eps < 0 or not finite, theta <= 0) */
+} nr_status;
+
+typedef enum nr_dtype {
+  NR_F32 = 0, /* IEEE binary32 */
+  NR_BF16 = 1 /* bfloat16: 1 sign, 8 exponent, 7 fraction bits */
+} nr_dtype;
+
+/*
+ * RMSNorm of each row, with the optional fused residual add.
+ *
+ * Follows vllm.cpp src/vt/cuda/cuda_ops.cu, "rmsnorm: one block per row"
+ * (RmsNormRowKernel) and "ResRound" (the residual is rounded to its storage
+ * dtype before it is squared, and that rounded value is what is written back).
+ * For row r of x [rows, hidden] (row-major, contiguous):
+ *     with a residual:  v_j = round(x_j + residual_j);  residual_j <- v_j   (in place)
+ *     without one:      v_j = x_j
+ *     inv   = 1 / sqrt(mean_j v_j^2 + eps)
+ *     out_j = round(v_j * inv * (gemma ? w_j + 1 : w_j))
+ *
+ * out       [rows, hidden], dtype `dtype`; may be x itself (then x is overwritten).
+ * x         [rows, hidden], dtype `dtype`.
+ * w         [hidden], dtype `dtype` (the weight dtype equals x's, as on the page).
+ * residual  [rows, hidden], dtype `dtype`, read and written in place; NULL for
+ *           plain RMSNorm.  It may not overlap x, w or out.
+ * hidden    > 0; a multiple of 8 (bf16) or 4 (f32).
+ * eps       finite, >= 0.
+ * gemma     0 or 1.
+ * Errors: NR_ERR_NULL, NR_ERR_SHAPE, NR_ERR_DTYPE, NR_ERR_ALIGN, NR_ERR_ALIAS,
+ *         NR_ERR_UNSUPPORTED, NR_ERR_VALUE, NR_ERR_CUDA.
+ */
+nr_status nr_rmsnorm(void* out, const void* x, const void* w, void* residual, int64_t rows,
+                     int64_t hidden, nr_dtype dtype, float eps, int gemma, cudaStream_t stream);
+
+/*
+ * Per-head RMSNorm of Q and K followed by NeoX rotary embedding, in one pass.
+ *
+ * Follows vllm.cpp src/vt/cuda/cuda_ops.cu, "attn_qk_norm_rope_gate" (RMSNorm
+ * over head_dim per (token, head), then the rotation, with no rounding between
+ * them) and "rope_neox" (freq_i = theta^(-2i/head_dim), angle = pos * freq_i,
+ * rotate-half pairing (i, i + head_dim/2)).  For token t, head h of Q (and of K
+ * with wk):
+ *     inv  = 1 / sqrt(mean_j v_j^2 + eps);   n_j = v_j * inv * (gemma ? w_j + 1 : w_j)
+ *     out_i        = round(n_i cos(a_i) - n_{i+D/2} sin(a_i))
+ *     out_{i+D/2}  = round(n_i sin(a_i) + n_{i+D/2} cos(a_i)),   a_i = pos_t * freq_i
+ * The rotary dimension is the whole head_dim.  The angle p * freq_i is reduced
+ * modulo 2*pi exactly in 64-bit fixed point before sin/cos, so large positions
+ * keep full accuracy.
+ *
+ * Layout: element (t, h, d) of q lives at q + t*q_tok_stride + h*head_dim + d
+ * (elements, not bytes), heads contiguous within a token; k likewise with
+ * k_tok_stride.  q_out/k_out use the same strides as q/k.  q_out may be q and
+ * k_out may be k (in place); otherwise outputs may not overlap any input or
+ * each other (Q and K may be interleaved views of one fused buffer).
+ *
+ * q_out, q   [tokens, hq, head_dim] strided as above, dtype `dtype`.
+ * k_out, k   [tokens, hk, head_dim], dtype `dtype`; may be NULL when hk == 0.
+ * wq, wk     [head_dim], dtype `w_dtype` (NR_F32 or NR_BF16), one vector per
+ *            tensor shared by all its heads; wk may be NULL when hk == 0.
+ * positions  [tokens] int32, device memory; any value (negative too).
+ * tokens >= 0, hq >= 1, hk >= 0.
+ * head_dim   bf16: 16, 32, 64, 128, 256 or 512;  f32: 8, 16, 32, 64, 128 or 256.
+ * q_tok_stride >= hq*head_dim and k_tok_stride >= hk*head_dim, each a multiple
+ *            of 16 bytes.
+ * eps finite >= 0;  theta > 0 and finite;  gemma 0 or 1.
+ * Errors: as nr_rmsnorm.
+ */
+nr_status nr_qk_norm_rope(void* q_out, void* k_out, const void* q, const void* k, const void* wq,
+                          const void* wk, nr_dtype w_dtype, const int32_t* positions,
+                          int64_t tokens, int64_t hq, int64_t hk, int64_t head_dim,
+                          int64_t q_tok_stride, int64_t k_tok_stride, float eps, double theta,
+                          int gemma, nr_dtype dtype, cudaStream_t stream);
+
+/*
+ * LayerNorm (no affine) fused with adaLN modulation.
+ *
+ * The pages name this fusion (FastVideo compare view
+ * feat/pan2-inference-optimizations, PAN2 docs, "Performance switches",
+ * dit_fused_kernels) without printing it; this is the plain adaLN reading:
+ *     mu = mean_j x_j;  var = mean_j (x_j - mu)^2   (biased)
+ *     out_j = round((x_j - mu) / sqrt(var + eps) * (1 + scale_j) + shift_j)
+ * with f32 statistics.
+ *
+ * out, x        [rows, hidden], dtype `dtype`; out may be x.
+ * shift, scale  [samples, hidden], dtype `dtype`; row r uses sample
+ *               r / rows_per_sample (rows_per_sample >= rows: one sample for all rows;
+ *               1: per-row modulation).
+ * hidden > 0, a multiple of 8 (bf16) or 4 (f32);  eps finite >= 0.
+ * Errors: as nr_rmsnorm.
+ */
+nr_status nr_ln_modulate(void* out, const void* x, const void* shift, const void* scale,
+                         int64_t rows, int64_t hidden, int64_t rows_per_sample, float eps,
+                         nr_dtype dtype, cudaStream_t stream);
+
+/*
+ * silu_and_mul: out[r, j] = silu(x[r, j]) * x[r, inter + j],  silu(a) = a / (1 + e^-a).
+ *
+ * Follows vllm.cpp src/vt/cuda/cuda_ops.cu, "silu_and_mul" (gate is the first
+ * half of each row, up the second; math in f32).
+ *
+ * out  [rows, inter], dtype `dtype`; may not overlap x.
+ * x    [rows, 2*inter], dtype `dtype`.
+ * inter > 0, a multiple of 8 (bf16) or 4 (f32).
+ * Errors: as nr_rmsnorm.
+ */
+nr_status nr_silu_and_mul(void* out, const void* x, int64_t rows, int64_t inter, nr_dtype dtype,
+                          cudaStream_t stream);
+
+/* Static, human-readable name of a status code. */
+const char* nr_status_string(nr_status s);
+
+/* Detail of the last non-OK status returned on the calling thread ("" if none).
+ * The pointer stays valid until the next library call on this thread. */
+const char* nr_last_error_message(void);
+
+/* Library ABI version (major * 10000 + minor * 100 + patch). */
+int nr_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NR_H */

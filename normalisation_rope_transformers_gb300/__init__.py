@@ -1,0 +1,161 @@
+"""Fused row-normalisation kernels for GB300 (sm_103a): Python binding.
+
+Thin ctypes binding over the C ABI in ``include/nr.h`` (``libnormrope.so``).
+Each function marshals torch CUDA tensors into device pointers, sizes and the
+current CUDA stream, calls the entry point of the same name, and raises on a
+non-OK status.  Every step of the computation runs in the library's kernels;
+there is no CPU or PyTorch fallback.  Importing fails loudly when the library
+has not been built (``python -m normalisation_rope_transformers_gb300.build``
+or ``__graft_entry__.build()``).
+
+    rmsnorm(x, w, residual=None, eps=1e-6, gemma=False, out=None)
+    qk_norm_rope(q, k, wq, wk, positions, eps=1e-6, theta=10000.0, gemma=False,
+                 q_out=None, k_out=None)
+    ln_modulate(x, shift, scale, eps=1e-6, rows_per_sample=None, out=None)
+    silu_and_mul(x, out=None)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libnormrope.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError("%s is missing: build the CUDA library first "
+                      "(python -m normalisation_rope_transformers_gb300.build)" % LIB_PATH)
+
+lib = ctypes.CDLL(LIB_PATH)
+
+_vp, _i64, _f32, _f64, _int = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_float, ctypes.c_double,
+                                ctypes.c_int)
+lib.nr_rmsnorm.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _int, _f32, _int, _vp]
+lib.nr_rmsnorm.restype = _int
+lib.nr_qk_norm_rope.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _int, _vp, _i64, _i64, _i64, _i64,
+                                _i64, _i64, _f32, _f64, _int, _int, _vp]
+lib.nr_qk_norm_rope.restype = _int
+lib.nr_ln_modulate.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _f32, _int, _vp]
+lib.nr_ln_modulate.restype = _int
+lib.nr_silu_and_mul.argtypes = [_vp, _vp, _i64, _i64, _int, _vp]
+lib.nr_silu_and_mul.restype = _int
+lib.nr_status_string.argtypes = [_int]
+lib.nr_status_string.restype = ctypes.c_char_p
+lib.nr_last_error_message.argtypes = []
+lib.nr_last_error_message.restype = ctypes.c_char_p
+lib.nr_version.argtypes = []
+lib.nr_version.restype = _int
+
+NR_F32 = 0
+NR_BF16 = 1
+ENTRY_POINTS = ("nr_rmsnorm", "nr_qk_norm_rope", "nr_ln_modulate", "nr_silu_and_mul",
+                "nr_status_string", "nr_last_error_message", "nr_version")
+
+
+class NrError(RuntimeError):
+    """A non-OK nr_status from the library."""
+
+    def __init__(self, status: int, message: str):
+        super().__init__("%s: %s" % (lib.nr_status_string(status).decode(), message))
+        self.status = status
+
+
+def _check(status: int):
+    if status != 0:
+        raise NrError(status, lib.nr_last_error_message().decode())
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return NR_BF16
+    if t.dtype == torch.float32:
+        return NR_F32
+    raise TypeError("tensors are bfloat16 or float32, got %s" % t.dtype)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(t: torch.Tensor):
+    return ctypes.c_void_p(torch.cuda.current_stream(t.device).cuda_stream)
+
+
+def _cuda(*ts):
+    for t in ts:
+        if t is not None and not t.is_cuda:
+            raise ValueError("tensors must be on a CUDA device")
+
+
+def rmsnorm(x, w, residual=None, eps=1e-6, gemma=False, out=None):
+    """RMSNorm of each row of x [rows, hidden]; with `residual`, first
+    residual <- round(x + residual) in place.  Returns out."""
+    _cuda(x, w, residual, out)
+    if x.dim() != 2 or not x.is_contiguous():
+        raise ValueError("x must be a contiguous [rows, hidden] tensor")
+    if out is None:
+        out = torch.empty_like(x)
+    _check(lib.nr_rmsnorm(_ptr(out), _ptr(x), _ptr(w), _ptr(residual), x.shape[0], x.shape[1],
+                          _dtype_code(x), float(eps), int(bool(gemma)), _stream(x)))
+    return out
+
+
+def qk_norm_rope(q, k, wq, wk, positions, eps=1e-6, theta=10000.0, gemma=False, q_out=None,
+                 k_out=None):
+    """Per-head RMSNorm + NeoX RoPE of q [tokens, hq, D] and k [tokens, hk, D].
+    q and k may be token-strided views (last two axes contiguous); outputs share
+    their strides (q_out=q / k_out=k for in place).  Returns (q_out, k_out)."""
+    _cuda(q, k, wq, wk, positions, q_out, k_out)
+    for t in (q, k):
+        if t.dim() != 3 or t.stride(2) != 1 or t.stride(1) != t.shape[2]:
+            raise ValueError("q/k must be [tokens, heads, head_dim] with contiguous heads")
+    if positions.dtype != torch.int32 or positions.dim() != 1:
+        raise TypeError("positions must be a 1-D int32 tensor")
+    if q_out is None:
+        q_out = torch.empty_strided(q.shape, q.stride(), dtype=q.dtype, device=q.device)
+    if k_out is None:
+        k_out = torch.empty_strided(k.shape, k.stride(), dtype=k.dtype, device=k.device)
+    if q_out.stride() != q.stride() or k_out.stride() != k.stride():
+        raise ValueError("q_out/k_out must have the strides of q/k")
+    if wq.dtype != wk.dtype:
+        raise TypeError("wq and wk share one dtype")
+    _check(lib.nr_qk_norm_rope(_ptr(q_out), _ptr(k_out), _ptr(q), _ptr(k), _ptr(wq), _ptr(wk),
+                               _dtype_code(wq), _ptr(positions), q.shape[0], q.shape[1],
+                               k.shape[1], q.shape[2], q.stride(0), k.stride(0), float(eps),
+                               float(theta), int(bool(gemma)), _dtype_code(q), _stream(q)))
+    return q_out, k_out
+
+
+def ln_modulate(x, shift, scale, eps=1e-6, rows_per_sample=None, out=None):
+    """LayerNorm (no affine) of x [rows, hidden] then * (1 + scale) + shift,
+    with shift/scale [samples, hidden] (row r uses sample r // rows_per_sample).
+    Returns out."""
+    _cuda(x, shift, scale, out)
+    if x.dim() != 2 or not x.is_contiguous():
+        raise ValueError("x must be a contiguous [rows, hidden] tensor")
+    if rows_per_sample is None:
+        rows_per_sample = max(x.shape[0], 1)
+    if out is None:
+        out = torch.empty_like(x)
+    _check(lib.nr_ln_modulate(_ptr(out), _ptr(x), _ptr(shift), _ptr(scale), x.shape[0],
+                              x.shape[1], int(rows_per_sample), float(eps), _dtype_code(x),
+                              _stream(x)))
+    return out
+
+
+def silu_and_mul(x, out=None):
+    """silu(x[:, :I]) * x[:, I:] for x [rows, 2I].  Returns out [rows, I]."""
+    _cuda(x, out)
+    if x.dim() != 2 or not x.is_contiguous() or x.shape[1] % 2:
+        raise ValueError("x must be a contiguous [rows, 2*inter] tensor")
+    inter = x.shape[1] // 2
+    if out is None:
+        out = torch.empty((x.shape[0], inter), dtype=x.dtype, device=x.device)
+    _check(lib.nr_silu_and_mul(_ptr(out), _ptr(x), x.shape[0], inter, _dtype_code(x), _stream(x)))
+    return out
+
+
+__all__ = ["rmsnorm", "qk_norm_rope", "ln_modulate", "silu_and_mul", "NrError", "lib",
+           "LIB_PATH", "ENTRY_POINTS", "NR_F32", "NR_BF16"]

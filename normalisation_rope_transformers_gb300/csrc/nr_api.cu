@@ -1,0 +1,256 @@
+// C ABI of the fused row-normalisation library: argument validation, the
+// per-call rotary constants, and status reporting.  Every check runs on the
+// host before any launch; a rejected call touches no device memory.
+#include <math.h>
+#include <stdarg.h>
+#include <stdint.h>
+#include <stdio.h>
+
+#include "../../include/nr.h"
+#include "nr_internal.h"
+
+namespace {
+
+thread_local char g_message[512];
+
+nr_status fail(nr_status s, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_message, sizeof g_message, fmt, ap);
+  va_end(ap);
+  return s;
+}
+
+nr_status ok() {
+  g_message[0] = '\0';
+  return NR_OK;
+}
+
+nr_status from_cuda(cudaError_t e, const char* what) {
+  if (e == cudaSuccess) return ok();
+  return fail(NR_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorString(e), cudaGetErrorName(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int elem_size(nr_dtype d) { return d == NR_BF16 ? 2 : 4; }
+int vec_elems(nr_dtype d) { return d == NR_BF16 ? 8 : 4; }
+bool valid_dtype(int d) { return d == NR_F32 || d == NR_BF16; }
+
+// `count` rows of `span` bytes, `stride` bytes apart, starting at `base`.
+struct Region {
+  uintptr_t base;
+  int64_t stride;
+  int64_t span;
+  int64_t count;
+};
+
+Region dense(const void* p, int64_t bytes) {
+  return Region{reinterpret_cast<uintptr_t>(p), bytes, bytes, 1};
+}
+
+// Conservative overlap test: false only when the two regions are provably
+// disjoint (disjoint address ranges, or equal strides with rows that interleave
+// without touching -- e.g. Q and K heads inside one fused QKV row).
+bool overlap(const Region& a, const Region& b) {
+  if (a.count <= 0 || b.count <= 0 || a.span <= 0 || b.span <= 0) return false;
+  const uintptr_t a_end = a.base + static_cast<uintptr_t>((a.count - 1) * a.stride + a.span);
+  const uintptr_t b_end = b.base + static_cast<uintptr_t>((b.count - 1) * b.stride + b.span);
+  if (a_end <= b.base || b_end <= a.base) return false;
+  if (a.stride == b.stride && a.stride >= a.span && a.stride >= b.span) {
+    const int64_t s = a.stride;
+    const int64_t diff = static_cast<int64_t>(b.base - a.base);  // two's complement
+    const int64_t delta = ((diff % s) + s) % s;                   // b's row start inside a's period
+    if (a.span <= delta && delta + b.span <= s) return false;
+  }
+  return true;
+}
+
+bool eps_ok(float eps) { return isfinite(eps) && eps >= 0.0f; }
+
+}  // namespace
+
+extern "C" {
+
+int nr_version(void) { return 100; }
+
+const char* nr_last_error_message(void) { return g_message; }
+
+const char* nr_status_string(nr_status s) {
+  switch (s) {
+    case NR_OK: return "NR_OK";
+    case NR_ERR_NULL: return "NR_ERR_NULL";
+    case NR_ERR_SHAPE: return "NR_ERR_SHAPE";
+    case NR_ERR_DTYPE: return "NR_ERR_DTYPE";
+    case NR_ERR_ALIGN: return "NR_ERR_ALIGN";
+    case NR_ERR_ALIAS: return "NR_ERR_ALIAS";
+    case NR_ERR_UNSUPPORTED: return "NR_ERR_UNSUPPORTED";
+    case NR_ERR_CUDA: return "NR_ERR_CUDA";
+    case NR_ERR_VALUE: return "NR_ERR_VALUE";
+  }
+  return "NR_ERR_UNKNOWN";
+}
+
+nr_status nr_rmsnorm(void* out, const void* x, const void* w, void* residual, int64_t rows,
+                     int64_t hidden, nr_dtype dtype, float eps, int gemma, cudaStream_t stream) {
+  if (!valid_dtype(dtype)) return fail(NR_ERR_DTYPE, "nr_rmsnorm: unknown dtype %d", (int)dtype);
+  if (rows < 0) return fail(NR_ERR_SHAPE, "nr_rmsnorm: rows = %lld < 0", (long long)rows);
+  if (hidden <= 0) return fail(NR_ERR_SHAPE, "nr_rmsnorm: hidden = %lld <= 0", (long long)hidden);
+  if (!eps_ok(eps)) return fail(NR_ERR_VALUE, "nr_rmsnorm: eps must be finite and >= 0");
+  if (gemma != 0 && gemma != 1) return fail(NR_ERR_VALUE, "nr_rmsnorm: gemma must be 0 or 1");
+  if (rows == 0) return ok();
+  if (!out || !x || !w) return fail(NR_ERR_NULL, "nr_rmsnorm: out, x and w must be non-NULL");
+  const int vec = vec_elems(dtype);
+  if (hidden % vec != 0)
+    return fail(NR_ERR_UNSUPPORTED, "nr_rmsnorm: hidden = %lld is not a multiple of %d",
+                (long long)hidden, vec);
+  if (rows > INT32_MAX || hidden / vec > INT32_MAX)
+    return fail(NR_ERR_SHAPE, "nr_rmsnorm: rows or hidden too large");
+  if (!aligned16(out) || !aligned16(x) || !aligned16(w) || (residual && !aligned16(residual)))
+    return fail(NR_ERR_ALIGN, "nr_rmsnorm: pointers must be 16-byte aligned");
+  const int64_t row_bytes = hidden * elem_size(dtype);
+  const Region ro = dense(out, rows * row_bytes), rx = dense(x, rows * row_bytes);
+  const Region rw = dense(w, row_bytes);
+  if (out != x && overlap(ro, rx))
+    return fail(NR_ERR_ALIAS, "nr_rmsnorm: out partially overlaps x (only out == x is allowed)");
+  if (overlap(ro, rw)) return fail(NR_ERR_ALIAS, "nr_rmsnorm: out overlaps w");
+  if (residual) {
+    const Region rr = dense(residual, rows * row_bytes);
+    if (overlap(rr, rx) || overlap(rr, ro) || overlap(rr, rw))
+      return fail(NR_ERR_ALIAS, "nr_rmsnorm: residual overlaps x, out or w");
+  }
+  return from_cuda(nr::launch_rmsnorm(out, x, w, residual, rows, hidden, dtype == NR_BF16, eps,
+                                      gemma, stream),
+                   "nr_rmsnorm launch");
+}
+
+nr_status nr_qk_norm_rope(void* q_out, void* k_out, const void* q, const void* k, const void* wq,
+                          const void* wk, nr_dtype w_dtype, const int32_t* positions,
+                          int64_t tokens, int64_t hq, int64_t hk, int64_t head_dim,
+                          int64_t q_tok_stride, int64_t k_tok_stride, float eps, double theta,
+                          int gemma, nr_dtype dtype, cudaStream_t stream) {
+  if (!valid_dtype(dtype) || !valid_dtype(w_dtype))
+    return fail(NR_ERR_DTYPE, "nr_qk_norm_rope: unknown dtype (%d, weights %d)", (int)dtype,
+                (int)w_dtype);
+  if (tokens < 0 || hq < 1 || hk < 0 || head_dim <= 0)
+    return fail(NR_ERR_SHAPE, "nr_qk_norm_rope: need tokens >= 0, hq >= 1, hk >= 0, head_dim > 0");
+  if (head_dim % 2 != 0) return fail(NR_ERR_SHAPE, "nr_qk_norm_rope: head_dim must be even");
+  const int vec = vec_elems(dtype);
+  const int64_t lanes = head_dim / (2 * vec);
+  if (head_dim % (2 * vec) != 0 || lanes > 32 || (lanes & (lanes - 1)) != 0)
+    return fail(NR_ERR_UNSUPPORTED,
+                "nr_qk_norm_rope: head_dim %lld not supported for this dtype (bf16: 16..512, "
+                "f32: 8..256, powers of two)",
+                (long long)head_dim);
+  if (!eps_ok(eps)) return fail(NR_ERR_VALUE, "nr_qk_norm_rope: eps must be finite and >= 0");
+  if (!(isfinite(theta) && theta > 0.0))
+    return fail(NR_ERR_VALUE, "nr_qk_norm_rope: theta must be finite and > 0");
+  if (gemma != 0 && gemma != 1) return fail(NR_ERR_VALUE, "nr_qk_norm_rope: gemma must be 0 or 1");
+  if (q_tok_stride < hq * head_dim || (hk > 0 && k_tok_stride < hk * head_dim))
+    return fail(NR_ERR_SHAPE, "nr_qk_norm_rope: token stride smaller than heads * head_dim");
+  if (tokens > INT32_MAX || hq + hk > 65536)
+    return fail(NR_ERR_SHAPE, "nr_qk_norm_rope: tokens or head count too large");
+  if (tokens == 0) return ok();
+  if (!q_out || !q || !wq || !positions)
+    return fail(NR_ERR_NULL, "nr_qk_norm_rope: q_out, q, wq and positions must be non-NULL");
+  if (hk > 0 && (!k_out || !k || !wk))
+    return fail(NR_ERR_NULL, "nr_qk_norm_rope: k_out, k and wk must be non-NULL when hk > 0");
+  const int es = elem_size(dtype);
+  if ((q_tok_stride * es) % 16 != 0 || (hk > 0 && (k_tok_stride * es) % 16 != 0))
+    return fail(NR_ERR_ALIGN, "nr_qk_norm_rope: token strides must be multiples of 16 bytes");
+  if (!aligned16(q_out) || !aligned16(q) || !aligned16(wq) ||
+      (hk > 0 && (!aligned16(k_out) || !aligned16(k) || !aligned16(wk))) ||
+      (reinterpret_cast<uintptr_t>(positions) & 3u))
+    return fail(NR_ERR_ALIGN,
+                "nr_qk_norm_rope: q/k/weights must be 16-byte aligned, positions 4-byte aligned");
+
+  const Region rq{reinterpret_cast<uintptr_t>(q), q_tok_stride * es, hq * head_dim * es, tokens};
+  const Region rqo{reinterpret_cast<uintptr_t>(q_out), q_tok_stride * es, hq * head_dim * es,
+                   tokens};
+  const Region rk{reinterpret_cast<uintptr_t>(k), k_tok_stride * es, hk * head_dim * es,
+                  hk > 0 ? tokens : 0};
+  const Region rko{reinterpret_cast<uintptr_t>(k_out), k_tok_stride * es, hk * head_dim * es,
+                   hk > 0 ? tokens : 0};
+  const int ws = elem_size(w_dtype);
+  const Region rwq = dense(wq, head_dim * ws);
+  const Region rwk = dense(wk, hk > 0 ? head_dim * ws : 0);
+  const Region rpos = dense(positions, tokens * 4);
+  if ((q_out != q && overlap(rqo, rq)) || overlap(rqo, rk) || overlap(rqo, rwq) ||
+      overlap(rqo, rwk) || overlap(rqo, rpos) || overlap(rqo, rko))
+    return fail(NR_ERR_ALIAS, "nr_qk_norm_rope: q_out overlaps an input or k_out");
+  if ((k_out != k && overlap(rko, rk)) || overlap(rko, rq) || overlap(rko, rwq) ||
+      overlap(rko, rwk) || overlap(rko, rpos))
+    return fail(NR_ERR_ALIAS, "nr_qk_norm_rope: k_out overlaps an input");
+
+  // turn_i = frac(freq_i / 2pi) * 2^64 with freq_i = theta^(-2i/D) in double.
+  // Positions are integers, so pos * freq_i mod 2pi = pos * frac-part mod 2pi.
+  nr::RopeTurns turns;
+  const int64_t half = head_dim / 2;
+  for (int64_t i = 0; i < nr::kMaxHalfDim; i++) turns.turn[i] = 0;
+  for (int64_t i = 0; i < half; i++) {
+    const double freq = pow(theta, -2.0 * static_cast<double>(i) / static_cast<double>(head_dim));
+    const double turns_per_step = freq / (2.0 * M_PI);
+    const double frac = turns_per_step - floor(turns_per_step);
+    const double scaled = ldexp(frac, 64);
+    turns.turn[i] = scaled >= 18446744073709551616.0 ? 0ull : static_cast<unsigned long long>(scaled);
+  }
+  return from_cuda(nr::launch_qk_norm_rope(q_out, k_out, q, k, wq, wk, w_dtype == NR_BF16,
+                                           positions, tokens, hq, hk, head_dim, q_tok_stride,
+                                           k_tok_stride, eps, turns, gemma, dtype == NR_BF16,
+                                           stream),
+                   "nr_qk_norm_rope launch");
+}
+
+nr_status nr_ln_modulate(void* out, const void* x, const void* shift, const void* scale,
+                         int64_t rows, int64_t hidden, int64_t rows_per_sample, float eps,
+                         nr_dtype dtype, cudaStream_t stream) {
+  if (!valid_dtype(dtype)) return fail(NR_ERR_DTYPE, "nr_ln_modulate: unknown dtype %d", (int)dtype);
+  if (rows < 0 || hidden <= 0 || rows_per_sample < 1)
+    return fail(NR_ERR_SHAPE, "nr_ln_modulate: need rows >= 0, hidden > 0, rows_per_sample >= 1");
+  if (!eps_ok(eps)) return fail(NR_ERR_VALUE, "nr_ln_modulate: eps must be finite and >= 0");
+  if (rows == 0) return ok();
+  if (!out || !x || !shift || !scale)
+    return fail(NR_ERR_NULL, "nr_ln_modulate: out, x, shift and scale must be non-NULL");
+  const int vec = vec_elems(dtype);
+  if (hidden % vec != 0)
+    return fail(NR_ERR_UNSUPPORTED, "nr_ln_modulate: hidden = %lld is not a multiple of %d",
+                (long long)hidden, vec);
+  if (rows > INT32_MAX || hidden / vec > INT32_MAX)
+    return fail(NR_ERR_SHAPE, "nr_ln_modulate: rows or hidden too large");
+  if (!aligned16(out) || !aligned16(x) || !aligned16(shift) || !aligned16(scale))
+    return fail(NR_ERR_ALIGN, "nr_ln_modulate: pointers must be 16-byte aligned");
+  const int64_t row_bytes = hidden * elem_size(dtype);
+  const int64_t samples = (rows + rows_per_sample - 1) / rows_per_sample;
+  const Region ro = dense(out, rows * row_bytes), rx = dense(x, rows * row_bytes);
+  if (out != x && overlap(ro, rx))
+    return fail(NR_ERR_ALIAS, "nr_ln_modulate: out partially overlaps x (only out == x is allowed)");
+  if (overlap(ro, dense(shift, samples * row_bytes)) || overlap(ro, dense(scale, samples * row_bytes)))
+    return fail(NR_ERR_ALIAS, "nr_ln_modulate: out overlaps shift or scale");
+  return from_cuda(nr::launch_ln_modulate(out, x, shift, scale, rows, hidden, rows_per_sample,
+                                          dtype == NR_BF16, eps, stream),
+                   "nr_ln_modulate launch");
+}
+
+nr_status nr_silu_and_mul(void* out, const void* x, int64_t rows, int64_t inter, nr_dtype dtype,
+                          cudaStream_t stream) {
+  if (!valid_dtype(dtype)) return fail(NR_ERR_DTYPE, "nr_silu_and_mul: unknown dtype %d", (int)dtype);
+  if (rows < 0 || inter <= 0)
+    return fail(NR_ERR_SHAPE, "nr_silu_and_mul: need rows >= 0 and inter > 0");
+  if (rows == 0) return ok();
+  if (!out || !x) return fail(NR_ERR_NULL, "nr_silu_and_mul: out and x must be non-NULL");
+  const int vec = vec_elems(dtype);
+  if (inter % vec != 0)
+    return fail(NR_ERR_UNSUPPORTED, "nr_silu_and_mul: inter = %lld is not a multiple of %d",
+                (long long)inter, vec);
+  if (inter / vec > INT32_MAX / 2)
+    return fail(NR_ERR_SHAPE, "nr_silu_and_mul: inter too large");
+  if (!aligned16(out) || !aligned16(x))
+    return fail(NR_ERR_ALIGN, "nr_silu_and_mul: pointers must be 16-byte aligned");
+  const int64_t es = elem_size(dtype);
+  if (overlap(dense(out, rows * inter * es), dense(x, rows * 2 * inter * es)))
+    return fail(NR_ERR_ALIAS, "nr_silu_and_mul: out overlaps x");
+  return from_cuda(nr::launch_silu_and_mul(out, x, rows, inter, dtype == NR_BF16, stream),
+                   "nr_silu_and_mul launch");
+}
+
+}  // extern "C"

@@ -1,0 +1,146 @@
+// Shared device helpers for the row-normalisation kernels (sm_103a).
+//
+// Every kernel moves data as 128-bit vectors (8 bf16 or 4 f32 values per
+// thread per access), so a warp covers 512 contiguous bytes per instruction.
+// Streaming data is read with L1::no_allocate (it is touched once) and written
+// with the .cs (evict-first) hint; parameters reused by every row (weights,
+// shift, scale) use the default caching path so they stay L1/L2 resident.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace nr {
+
+constexpr int kWarp = 32;
+
+// ---------------------------------------------------------------------------
+// 128-bit global memory access
+// ---------------------------------------------------------------------------
+// Read-once data (x, residual, q, k): no L1 allocation, and ask L2 to fetch the
+// whole 256-byte sector group.  Only used on data that no thread of the same
+// launch writes before reading it (each thread reads its own elements before it
+// overwrites them in place).
+__device__ __forceinline__ uint4 ld_stream(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// Data shared by all rows (weights, shift, scale): normal cached read-only path.
+__device__ __forceinline__ uint4 ld_param(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// Coherent read (for data this launch may already have written, e.g. the
+// residual re-read by the multi-pass kernels for very long rows).
+__device__ __forceinline__ uint4 ld_coherent(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p)
+               : "memory");
+  return v;
+}
+
+// Streaming store: evict-first, the result is not re-read by this launch.
+__device__ __forceinline__ void st_stream(void* p, uint4 v) {
+  asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+// Plain store (for data a later pass of the same launch reads back).
+__device__ __forceinline__ void st_plain(void* p, uint4 v) {
+  asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// Element types: a 128-bit vector holds VEC values of T.
+// ---------------------------------------------------------------------------
+template <typename T>
+struct Vec;
+
+template <>
+struct Vec<float> {
+  static constexpr int N = 4;
+  __device__ __forceinline__ static void unpack(const uint4& v, float (&f)[4]) {
+    f[0] = __uint_as_float(v.x);
+    f[1] = __uint_as_float(v.y);
+    f[2] = __uint_as_float(v.z);
+    f[3] = __uint_as_float(v.w);
+  }
+  __device__ __forceinline__ static uint4 pack(const float (&f)[4]) {
+    return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]),
+                      __float_as_uint(f[3]));
+  }
+};
+
+// bf16 pair in one 32-bit word: element 2k in the low half, 2k+1 in the high
+// half.  Widening is exact (bf16 is the top half of an f32).
+__device__ __forceinline__ float bf16_lo(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
+
+// Round two f32 values to bf16 (round to nearest even) and pack them.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+template <>
+struct Vec<__nv_bfloat16> {
+  static constexpr int N = 8;
+  __device__ __forceinline__ static void unpack(const uint4& v, float (&f)[8]) {
+    f[0] = bf16_lo(v.x);
+    f[1] = bf16_hi(v.x);
+    f[2] = bf16_lo(v.y);
+    f[3] = bf16_hi(v.y);
+    f[4] = bf16_lo(v.z);
+    f[5] = bf16_hi(v.z);
+    f[6] = bf16_lo(v.w);
+    f[7] = bf16_hi(v.w);
+  }
+  __device__ __forceinline__ static uint4 pack(const float (&f)[8]) {
+    return make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
+                      pack_bf16x2(f[6], f[7]));
+  }
+};
+
+// ---------------------------------------------------------------------------
+// Reductions
+// ---------------------------------------------------------------------------
+// Butterfly sum over groups of `width` consecutive lanes (width a power of two
+// <= 32); every lane of the group ends with the same value.
+template <int width>
+__device__ __forceinline__ float group_sum(float v) {
+#pragma unroll
+  for (int m = width / 2; m > 0; m >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, m);
+  return v;
+}
+
+// Sum over the whole thread block.  `scratch` holds one float per warp; every
+// thread returns the same total, summed in warp order.  Contains one barrier;
+// callers that reuse `scratch` must separate the uses with another barrier or
+// use distinct arrays.
+__device__ __forceinline__ float block_sum(float v, float* scratch) {
+  v = group_sum<kWarp>(v);
+  const int warp = threadIdx.x / kWarp;
+  const int lane = threadIdx.x % kWarp;
+  if (lane == 0) scratch[warp] = v;
+  __syncthreads();
+  const int nwarps = (blockDim.x + kWarp - 1) / kWarp;
+  float total = 0.0f;
+  for (int i = 0; i < nwarps; i++) total += scratch[i];
+  return total;
+}
+
+}  // namespace nr

@@ -1,0 +1,66 @@
+// Internal launcher interface between the C ABI (nr_api.cu) and the kernels.
+// Arguments reaching these functions have been validated by the ABI layer.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace nr {
+
+// Geometry of the row-resident kernels: one block per row, `threads` threads,
+// each owning up to `vpt` 128-bit vectors.  vpt == 0 selects the multi-pass
+// kernel for rows longer than the register budget.
+struct RowLaunch {
+  int vpt;
+  int threads;
+};
+
+constexpr int kRowMaxThreads = 256;
+constexpr int kRowVpts[] = {1, 2, 3, 4, 5, 6, 8, 12, 16};
+
+// Pick the vectors-per-thread count that covers the row with at most
+// kRowMaxThreads threads and the fewest idle vector slots (ties: fewer vectors
+// per thread, i.e. more threads).
+inline RowLaunch pick_row_launch(int64_t nvec) {
+  RowLaunch best{0, 1024};
+  int64_t best_waste = -1;
+  for (int v : kRowVpts) {
+    const int64_t need = (nvec + v - 1) / v;
+    const int64_t threads = ((need + 31) / 32) * 32;
+    if (threads > kRowMaxThreads) continue;
+    const int64_t waste = threads * v - nvec;
+    if (best_waste < 0 || waste < best_waste) {
+      best_waste = waste;
+      best = RowLaunch{v, static_cast<int>(threads)};
+    }
+  }
+  return best;
+}
+
+cudaError_t launch_rmsnorm(void* out, const void* x, const void* w, void* residual, int64_t rows,
+                           int64_t hidden, int is_bf16, float eps, int gemma,
+                           cudaStream_t stream);
+
+cudaError_t launch_ln_modulate(void* out, const void* x, const void* shift, const void* scale,
+                               int64_t rows, int64_t hidden, int64_t rows_per_sample,
+                               int is_bf16, float eps, cudaStream_t stream);
+
+cudaError_t launch_silu_and_mul(void* out, const void* x, int64_t rows, int64_t inter,
+                                int is_bf16, cudaStream_t stream);
+
+// Per-call rotary constants: turn[i] = frac(freq_i / (2*pi)) * 2^64, freq_i =
+// theta^(-2i/head_dim), so that (pos * turn[i]) mod 2^64 is the angle pos*freq_i
+// as a fraction of a full turn.
+constexpr int kMaxHalfDim = 256;
+struct RopeTurns {
+  unsigned long long turn[kMaxHalfDim];
+};
+
+cudaError_t launch_qk_norm_rope(void* q_out, void* k_out, const void* q, const void* k,
+                                const void* wq, const void* wk, int w_is_bf16,
+                                const int32_t* positions, int64_t tokens, int64_t hq, int64_t hk,
+                                int64_t head_dim, int64_t q_tok_stride, int64_t k_tok_stride,
+                                float eps, const RopeTurns& turns, int gemma, int is_bf16,
+                                cudaStream_t stream);
+
+}  // namespace nr

@@ -1,0 +1,195 @@
+// RMSNorm with the optional fused residual add, for sm_103a.
+//
+// Computes what vllm.cpp src/vt/cuda/cuda_ops.cu describes in "rmsnorm: one
+// block per row" and "ResRound": v = round(x + residual) (written back in
+// place), inv = 1/sqrt(mean(v^2) + eps), out = round(v * inv * (w [+1])).
+//
+// Design (not the page's): the page's kernel walks a row twice with scalar
+// loads and a 256-wide shared-memory tree.  Here each row is held in
+// registers: a block owns one row, each thread loads VPT 128-bit vectors of x
+// (and of the residual) once, writes the rounded residual back immediately,
+// and the row's sum of squares is reduced with warp shuffles plus one
+// shared-memory step.  Each row is read from HBM once and written once.
+// Rows longer than the register budget use a two-pass kernel that re-reads
+// the (L2-resident) row.
+#include "nr_common.cuh"
+#include "nr_internal.h"
+
+namespace nr {
+namespace {
+
+// One block per row; thread t owns vectors t, t + blockDim, ..., (VPT of them).
+template <typename T, int VPT, bool RES>
+__global__ void __launch_bounds__(kRowMaxThreads) rmsnorm_row_kernel(T* __restrict__ out,
+                                                           const T* __restrict__ x,
+                                                           const T* __restrict__ w,
+                                                           T* __restrict__ res, int nvec,
+                                                           float hidden_f, float eps,
+                                                           float w_add) {
+  constexpr int N = Vec<T>::N;
+  __shared__ float scratch[32];
+  const int64_t row_off = static_cast<int64_t>(blockIdx.x) * nvec;  // in vectors
+  const uint4* xr = reinterpret_cast<const uint4*>(x) + row_off;
+  uint4* rr = RES ? reinterpret_cast<uint4*>(res) + row_off : nullptr;
+  uint4* orow = reinterpret_cast<uint4*>(out) + row_off;
+  const uint4* wv = reinterpret_cast<const uint4*>(w);
+
+  uint4 xv[VPT];
+  uint4 rv[VPT];
+#pragma unroll
+  for (int k = 0; k < VPT; k++) {
+    const int vi = threadIdx.x + k * blockDim.x;
+    if (vi < nvec) {
+      xv[k] = ld_stream(xr + vi);
+      if (RES) rv[k] = ld_stream(rr + vi);
+    }
+  }
+
+  float sum_sq = 0.0f;
+#pragma unroll
+  for (int k = 0; k < VPT; k++) {
+    const int vi = threadIdx.x + k * blockDim.x;
+    if (vi < nvec) {
+      float v[N];
+      Vec<T>::unpack(xv[k], v);
+      if (RES) {
+        float r[N];
+        Vec<T>::unpack(rv[k], r);
+#pragma unroll
+        for (int e = 0; e < N; e++) v[e] += r[e];
+        // Round to the residual's storage dtype; the rounded value is both
+        // written back and squared.  (For bf16, f32 add then one rounding
+        // equals rounding the exact sum: f32 holds >= 2*8+2 bits.)
+        xv[k] = Vec<T>::pack(v);
+        st_stream(rr + vi, xv[k]);
+        Vec<T>::unpack(xv[k], v);
+      }
+#pragma unroll
+      for (int e = 0; e < N; e++) sum_sq = fmaf(v[e], v[e], sum_sq);
+    }
+  }
+
+  const float total = block_sum(sum_sq, scratch);
+  const float inv = 1.0f / sqrtf(__fdiv_rn(total, hidden_f) + eps);
+
+#pragma unroll
+  for (int k = 0; k < VPT; k++) {
+    const int vi = threadIdx.x + k * blockDim.x;
+    if (vi < nvec) {
+      float v[N], wf[N];
+      Vec<T>::unpack(xv[k], v);
+      Vec<T>::unpack(ld_param(wv + vi), wf);
+#pragma unroll
+      for (int e = 0; e < N; e++) v[e] = v[e] * inv * (wf[e] + w_add);
+      st_stream(orow + vi, Vec<T>::pack(v));
+    }
+  }
+}
+
+// Rows too long for registers: pass 1 adds, writes the residual and reduces;
+// pass 2 re-reads the stored values (L2-resident) and normalises.
+template <typename T, bool RES>
+__global__ void __launch_bounds__(1024) rmsnorm_long_row_kernel(T* __restrict__ out,
+                                                                const T* __restrict__ x,
+                                                                const T* __restrict__ w,
+                                                                T* __restrict__ res, int64_t nvec,
+                                                                float hidden_f, float eps,
+                                                                float w_add) {
+  constexpr int N = Vec<T>::N;
+  __shared__ float scratch[32];
+  const int64_t row_off = static_cast<int64_t>(blockIdx.x) * nvec;
+  const uint4* xr = reinterpret_cast<const uint4*>(x) + row_off;
+  uint4* rr = RES ? reinterpret_cast<uint4*>(res) + row_off : nullptr;
+  uint4* orow = reinterpret_cast<uint4*>(out) + row_off;
+  const uint4* wv = reinterpret_cast<const uint4*>(w);
+
+  float sum_sq = 0.0f;
+  for (int64_t vi = threadIdx.x; vi < nvec; vi += blockDim.x) {
+    float v[N];
+    Vec<T>::unpack(ld_coherent(xr + vi), v);
+    if (RES) {
+      float r[N];
+      Vec<T>::unpack(ld_coherent(rr + vi), r);
+#pragma unroll
+      for (int e = 0; e < N; e++) v[e] += r[e];
+      const uint4 packed = Vec<T>::pack(v);
+      st_plain(rr + vi, packed);
+      Vec<T>::unpack(packed, v);
+    }
+#pragma unroll
+    for (int e = 0; e < N; e++) sum_sq = fmaf(v[e], v[e], sum_sq);
+  }
+  const float total = block_sum(sum_sq, scratch);
+  const float inv = 1.0f / sqrtf(__fdiv_rn(total, hidden_f) + eps);
+  // Each thread re-reads only the vectors it wrote itself, so program order
+  // makes its own residual stores visible to it.
+  for (int64_t vi = threadIdx.x; vi < nvec; vi += blockDim.x) {
+    float v[N], wf[N];
+    Vec<T>::unpack(RES ? ld_coherent(rr + vi) : ld_coherent(xr + vi), v);
+    Vec<T>::unpack(ld_param(wv + vi), wf);
+#pragma unroll
+    for (int e = 0; e < N; e++) v[e] = v[e] * inv * (wf[e] + w_add);
+    st_stream(orow + vi, Vec<T>::pack(v));
+  }
+}
+
+template <typename T, int VPT>
+cudaError_t launch_rows(const RowLaunch& g, void* out, const void* x, const void* w, void* res,
+                        int64_t rows, int nvec, float hidden_f, float eps, float w_add,
+                        cudaStream_t s) {
+  const dim3 grid(static_cast<unsigned>(rows));
+  const dim3 block(g.threads);
+  if (res != nullptr)
+    rmsnorm_row_kernel<T, VPT, true><<<grid, block, 0, s>>>(
+        static_cast<T*>(out), static_cast<const T*>(x), static_cast<const T*>(w),
+        static_cast<T*>(res), nvec, hidden_f, eps, w_add);
+  else
+    rmsnorm_row_kernel<T, VPT, false><<<grid, block, 0, s>>>(
+        static_cast<T*>(out), static_cast<const T*>(x), static_cast<const T*>(w), nullptr, nvec,
+        hidden_f, eps, w_add);
+  return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_typed(void* out, const void* x, const void* w, void* res, int64_t rows,
+                         int64_t hidden, float eps, int gemma, cudaStream_t s) {
+  const int64_t nvec = hidden / Vec<T>::N;
+  const float hidden_f = static_cast<float>(hidden);
+  const float w_add = gemma ? 1.0f : 0.0f;
+  const RowLaunch g = pick_row_launch(nvec);
+  switch (g.vpt) {
+    case 1: return launch_rows<T, 1>(g, out, x, w, res, rows, (int)nvec, hidden_f, eps, w_add, s);
+    case 2: return launch_rows<T, 2>(g, out, x, w, res, rows, (int)nvec, hidden_f, eps, w_add, s);
+    case 3: return launch_rows<T, 3>(g, out, x, w, res, rows, (int)nvec, hidden_f, eps, w_add, s);
+    case 4: return launch_rows<T, 4>(g, out, x, w, res, rows, (int)nvec, hidden_f, eps, w_add, s);
+    case 5: return launch_rows<T, 5>(g, out, x, w, res, rows, (int)nvec, hidden_f, eps, w_add, s);
+    case 6: return launch_rows<T, 6>(g, out, x, w, res, rows, (int)nvec, hidden_f, eps, w_add, s);
+    case 8: return launch_rows<T, 8>(g, out, x, w, res, rows, (int)nvec, hidden_f, eps, w_add, s);
+    case 12: return launch_rows<T, 12>(g, out, x, w, res, rows, (int)nvec, hidden_f, eps, w_add, s);
+    case 16: return launch_rows<T, 16>(g, out, x, w, res, rows, (int)nvec, hidden_f, eps, w_add, s);
+    default: break;
+  }
+  // Long rows: 1024 threads stride over the row twice.
+  const dim3 grid(static_cast<unsigned>(rows));
+  if (res != nullptr)
+    rmsnorm_long_row_kernel<T, true><<<grid, 1024, 0, s>>>(
+        static_cast<T*>(out), static_cast<const T*>(x), static_cast<const T*>(w),
+        static_cast<T*>(res), nvec, hidden_f, eps, w_add);
+  else
+    rmsnorm_long_row_kernel<T, false><<<grid, 1024, 0, s>>>(
+        static_cast<T*>(out), static_cast<const T*>(x), static_cast<const T*>(w), nullptr, nvec,
+        hidden_f, eps, w_add);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_rmsnorm(void* out, const void* x, const void* w, void* residual, int64_t rows,
+                           int64_t hidden, int is_bf16, float eps, int gemma,
+                           cudaStream_t stream) {
+  if (is_bf16)
+    return launch_typed<__nv_bfloat16>(out, x, w, residual, rows, hidden, eps, gemma, stream);
+  return launch_typed<float>(out, x, w, residual, rows, hidden, eps, gemma, stream);
+}
+
+}  // namespace nr

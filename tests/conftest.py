@@ -1,3 +1,4 @@
+import importlib.util
 import os
 import sys
 
@@ -12,9 +13,25 @@ def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a); runs the CUDA path")
 
 
+def _build_module():
+    """The library's build script, loaded by path (importing the package itself
+    requires the built library)."""
+    path = os.path.join(ROOT, "normalisation_rope_transformers_gb300", "build.py")
+    spec = importlib.util.spec_from_file_location("_nr_build", path)
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod
+
+
 @pytest.fixture(scope="session")
-def nr():
-    """The CUDA binding (built on first use); GPU tests only."""
+def lib_path():
+    """Path of libnormrope.so, built (cross-compiled for sm_103a) if stale."""
+    return _build_module().build()
+
+
+@pytest.fixture(scope="session")
+def nr(lib_path):
+    """The CUDA binding; GPU tests only."""
     import torch
 
     if not torch.cuda.is_available():

@@ -59,6 +59,10 @@ def parse_args():
     p.add_argument("--e2e-steps", type=int, default=10)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-decode-sweep", action="store_true")
+    p.add_argument("--profile", default=None,
+                   help="run only the named call of the step (e.g. qk_norm_rope) --steps times, "
+                        "for ncu; --rows overrides its row/token count; prints no JSON")
+    p.add_argument("--rows", type=int, default=None)
     return p.parse_args()
 
 
@@ -78,21 +82,28 @@ def nbytes(*ts):
     return sum(t.numel() * t.element_size() for t in ts if t is not None)
 
 
-def build_step(nr, synth, torch, device, rank):
-    """Device buffers and the seven calls of one step for this rank."""
+def build_step(nr, synth, torch, device, rank, only=None):
+    """Device buffers and the seven calls of one step for this rank (only the
+    calls whose name starts with `only`, when given)."""
     bf16, f32 = torch.bfloat16, torch.float32
     calls = []
 
+    def want(name):
+        return only is None or name.startswith(only)
+
     c = synth.RMSNORM_F32
-    x, _, w = synth.rmsnorm_inputs(c["rows"], c["hidden"], c["seed"], f32, residual=False)
-    x, w = x.to(device), w.to(device)
-    out = torch.empty_like(x)
-    calls.append(Call("rmsnorm_f32_64x1024", "rmsnorm",
-                      lambda x=x, w=w, out=out, eps=c["eps"]: nr.rmsnorm(x, w, eps=eps, out=out),
-                      {"x": x, "w": w}, {"out": out}, nbytes(x, w, out), c["rows"], "rows"))
+    if want("rmsnorm_f32_64x1024"):
+        x, _, w = synth.rmsnorm_inputs(c["rows"], c["hidden"], c["seed"], f32, residual=False)
+        x, w = x.to(device), w.to(device)
+        out = torch.empty_like(x)
+        calls.append(Call("rmsnorm_f32_64x1024", "rmsnorm",
+                          lambda x=x, w=w, out=out, eps=c["eps"]: nr.rmsnorm(x, w, eps=eps, out=out),
+                          {"x": x, "w": w}, {"out": out}, nbytes(x, w, out), c["rows"], "rows"))
 
     c = synth.ADD_RMSNORM
     for gemma in (False, True):
+        if not want("add_rmsnorm_bf16_8192x5120_gemma%d" % gemma):
+            continue
         x, res, w = synth.rmsnorm_inputs(c["rows"], c["hidden"], c["seed"], bf16)
         x, res, w = x.to(device), res.to(device), w.to(device)
         out = torch.empty_like(x)
@@ -103,43 +114,47 @@ def build_step(nr, synth, torch, device, rank):
                           nbytes(x, w, res) + nbytes(out, res), c["rows"], "rows"))
 
     c = synth.QK_NORM_ROPE
-    q, k, wq, wk, pos = synth.qk_inputs(c["tokens"], c["hq"], c["hk"], c["head_dim"], c["seed"],
-                                        bf16, f32, pos_start=rank * c["tokens"])
-    q, k, wq, wk, pos = (t.to(device) for t in (q, k, wq, wk, pos))
-    qo, ko = torch.empty_like(q), torch.empty_like(k)
-    calls.append(Call("qk_norm_rope_bf16_26598x24x128", "qk_norm_rope",
-                      lambda q=q, k=k, wq=wq, wk=wk, pos=pos, qo=qo, ko=ko, eps=c["eps"],
-                      theta=c["theta"]: nr.qk_norm_rope(q, k, wq, wk, pos, eps=eps, theta=theta,
-                                                        q_out=qo, k_out=ko),
-                      {"q": q, "k": k, "wq": wq, "wk": wk, "positions": pos},
-                      {"q_out": qo, "k_out": ko}, nbytes(q, k, wq, wk, pos, qo, ko),
-                      c["tokens"] * (c["hq"] + c["hk"]), "head rows"))
+    if want("qk_norm_rope_bf16_26598x24x128"):
+        q, k, wq, wk, pos = synth.qk_inputs(c["tokens"], c["hq"], c["hk"], c["head_dim"],
+                                            c["seed"], bf16, f32, pos_start=rank * c["tokens"])
+        q, k, wq, wk, pos = (t.to(device) for t in (q, k, wq, wk, pos))
+        qo, ko = torch.empty_like(q), torch.empty_like(k)
+        calls.append(Call("qk_norm_rope_bf16_26598x24x128", "qk_norm_rope",
+                          lambda q=q, k=k, wq=wq, wk=wk, pos=pos, qo=qo, ko=ko, eps=c["eps"],
+                          theta=c["theta"]: nr.qk_norm_rope(q, k, wq, wk, pos, eps=eps,
+                                                            theta=theta, q_out=qo, k_out=ko),
+                          {"q": q, "k": k, "wq": wq, "wk": wk, "positions": pos},
+                          {"q_out": qo, "k_out": ko}, nbytes(q, k, wq, wk, pos, qo, ko),
+                          c["tokens"] * (c["hq"] + c["hk"]), "head rows"))
 
     c = synth.LN_MODULATE
-    x, sh, sc = synth.ln_inputs(c["rows"], c["hidden"], c["seed"], bf16)
-    x, sh, sc = x.to(device), sh.to(device), sc.to(device)
-    out = torch.empty_like(x)
-    calls.append(Call("ln_modulate_bf16_26598x3072", "ln_modulate",
-                      lambda x=x, sh=sh, sc=sc, out=out, eps=c["eps"]:
-                      nr.ln_modulate(x, sh, sc, eps=eps, out=out),
-                      {"x": x, "shift": sh, "scale": sc}, {"out": out}, nbytes(x, sh, sc, out),
-                      c["rows"], "rows"))
+    if want("ln_modulate_bf16_26598x3072"):
+        x, sh, sc = synth.ln_inputs(c["rows"], c["hidden"], c["seed"], bf16)
+        x, sh, sc = x.to(device), sh.to(device), sc.to(device)
+        out = torch.empty_like(x)
+        calls.append(Call("ln_modulate_bf16_26598x3072", "ln_modulate",
+                          lambda x=x, sh=sh, sc=sc, out=out, eps=c["eps"]:
+                          nr.ln_modulate(x, sh, sc, eps=eps, out=out),
+                          {"x": x, "shift": sh, "scale": sc}, {"out": out},
+                          nbytes(x, sh, sc, out), c["rows"], "rows"))
 
     c = synth.DECODE
     rows, hidden = max(c["rows"]), max(c["hidden"])
-    x, res, w = synth.rmsnorm_inputs(rows, hidden, c["seed"], bf16)
-    x, res, w = x.to(device), res.to(device), w.to(device)
-    out = torch.empty_like(x)
-    calls.append(Call("add_rmsnorm_bf16_256x8192", "add_rmsnorm",
-                      lambda x=x, w=w, res=res, out=out, eps=c["eps"]:
-                      nr.rmsnorm(x, w, residual=res, eps=eps, out=out),
-                      {"x": x, "w": w, "residual": res}, {"out": out, "residual": res},
-                      nbytes(x, w, res) + nbytes(out, res), rows, "rows"))
-    g = synth.silu_inputs(rows, 3 * hidden, c["seed"], bf16).to(device)
-    out = torch.empty((rows, 3 * hidden), dtype=bf16, device=device)
-    calls.append(Call("silu_and_mul_bf16_256x49152", "silu_and_mul",
-                      lambda g=g, out=out: nr.silu_and_mul(g, out=out), {"x": g}, {"out": out},
-                      nbytes(g, out), rows, "rows"))
+    if want("add_rmsnorm_bf16_256x8192"):
+        x, res, w = synth.rmsnorm_inputs(rows, hidden, c["seed"], bf16)
+        x, res, w = x.to(device), res.to(device), w.to(device)
+        out = torch.empty_like(x)
+        calls.append(Call("add_rmsnorm_bf16_256x8192", "add_rmsnorm",
+                          lambda x=x, w=w, res=res, out=out, eps=c["eps"]:
+                          nr.rmsnorm(x, w, residual=res, eps=eps, out=out),
+                          {"x": x, "w": w, "residual": res}, {"out": out, "residual": res},
+                          nbytes(x, w, res) + nbytes(out, res), rows, "rows"))
+    if want("silu_and_mul_bf16_256x49152"):
+        g = synth.silu_inputs(rows, 3 * hidden, c["seed"], bf16).to(device)
+        out = torch.empty((rows, 3 * hidden), dtype=bf16, device=device)
+        calls.append(Call("silu_and_mul_bf16_256x49152", "silu_and_mul",
+                          lambda g=g, out=out: nr.silu_and_mul(g, out=out), {"x": g},
+                          {"out": out}, nbytes(g, out), rows, "rows"))
     return calls
 
 
@@ -413,47 +428,59 @@ def run_e2e(args, torch, calls, device, world, barrier, step_bytes):
 
 
 def decode_sweep(nr, synth, torch, device):
-    """Latency per call of add+RMSNorm and silu_and_mul over the decode grid:
-    hot (back-to-back, L2-warm) and cold (a 256 MB buffer written between calls,
-    only the call itself timed)."""
+    """Latency per call of add+RMSNorm and silu_and_mul over the decode grid,
+    both from CUDA graphs of back-to-back calls (so host launch overhead is not
+    in the figure): hot = the same buffers every call (L2-warm); cold = the
+    calls cycle through enough copies of the buffers to span > 2x the 129 MB
+    L2, so every call reads from HBM."""
     c = synth.DECODE
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+    span = 320 << 20
     out = {}
+
+    def graph_us(fns):
+        for f in fns[:3]:
+            f()
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for f in fns:
+                f()
+        graph.replay()
+        torch.cuda.synchronize()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        graph.replay()
+        e.record()
+        torch.cuda.synchronize()
+        return s.elapsed_time(e) * 1e3 / len(fns)
+
     for rows in c["rows"]:
         for hidden in c["hidden"]:
             x, res, w = synth.rmsnorm_inputs(rows, hidden, c["seed"], torch.bfloat16)
-            x, res, w = x.to(device), res.to(device), w.to(device)
-            o = torch.empty_like(x)
-            g = synth.silu_inputs(rows, 3 * hidden, c["seed"], torch.bfloat16).to(device)
-            go = torch.empty((rows, 3 * hidden), dtype=torch.bfloat16, device=device)
-            for name, fn, nb in (
-                    ("add_rmsnorm", lambda: nr.rmsnorm(x, w, residual=res, out=o),
-                     nbytes(x, w, res) + nbytes(o, res)),
-                    ("silu_and_mul", lambda: nr.silu_and_mul(g, out=go), nbytes(g, go))):
-                for _ in range(5):
-                    fn()
-                torch.cuda.synchronize()
-                n = 200
-                s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                s.record()
-                for _ in range(n):
-                    fn()
-                e.record()
-                torch.cuda.synchronize()
-                hot_us = s.elapsed_time(e) * 1e3 / n
-                cold = []
-                for _ in range(20):
-                    flush.fill_(1)
-                    s.record()
-                    fn()
-                    e.record()
-                    torch.cuda.synchronize()
-                    cold.append(s.elapsed_time(e) * 1e3)
-                cold_us = statistics.median(cold)
+            g = synth.silu_inputs(rows, 3 * hidden, c["seed"], torch.bfloat16)
+            rms_bytes = nbytes(x, w, res) * 2 - nbytes(w)  # read x, res, w; write out, res
+            silu_bytes = nbytes(g) * 3 // 2
+            for name, nb in (("add_rmsnorm", rms_bytes), ("silu_and_mul", silu_bytes)):
+                sets = int(min(4096, max(2, span // nb)))
+                if name == "add_rmsnorm":
+                    xs = x.to(device).repeat(sets, 1).view(sets, rows, hidden)
+                    rs = res.to(device).repeat(sets, 1).view(sets, rows, hidden)
+                    os_ = torch.empty_like(xs)
+                    wd = w.to(device)
+                    fns = [lambda i=i: nr.rmsnorm(xs[i], wd, residual=rs[i], out=os_[i])
+                           for i in range(sets)]
+                else:
+                    gs = g.to(device).repeat(sets, 1).view(sets, rows, 6 * hidden)
+                    os_ = torch.empty((sets, rows, 3 * hidden), dtype=torch.bfloat16,
+                                      device=device)
+                    fns = [lambda i=i: nr.silu_and_mul(gs[i], out=os_[i]) for i in range(sets)]
+                hot_us = graph_us([fns[0]] * 100)
+                cold_us = graph_us(fns)
                 out["%s_%dx%d" % (name, rows, hidden)] = {
                     "hot_us": round(hot_us, 2), "cold_us": round(cold_us, 2), "bytes": nb,
                     "hot_GB_s": round(nb / (hot_us * 1e-6) / 1e9, 1),
-                    "cold_GB_s": round(nb / (cold_us * 1e-6) / 1e9, 1)}
+                    "cold_GB_s": round(nb / (cold_us * 1e-6) / 1e9, 1), "cold_sets": sets}
+                del fns
     return out
 
 
@@ -570,9 +597,38 @@ def run_reference(args):
     }), flush=True)
 
 
+def run_profile(args):
+    """Run one call of the step (optionally at a smaller row count) --steps
+    times after --warmup calls: the target of the ncu captures."""
+    import torch
+
+    import normalisation_rope_transformers_gb300 as nr
+    import synth
+
+    device = torch.device("cuda", 0)
+    if args.rows is not None:
+        for cfg, key in ((synth.ADD_RMSNORM, "rows"), (synth.QK_NORM_ROPE, "tokens"),
+                         (synth.LN_MODULATE, "rows")):
+            cfg[key] = args.rows
+    calls = build_step(nr, synth, torch, device, 0, only=args.profile)
+    if not calls:
+        raise SystemExit("no call named %s*" % args.profile)
+    c = calls[0]
+    for _ in range(args.warmup):
+        c.fn()
+    torch.cuda.synchronize()
+    for _ in range(args.steps):
+        c.fn()
+    torch.cuda.synchronize()
+    print("profiled %s x%d (%d bytes per launch, %d %s)" % (c.name, args.steps, c.nbytes, c.rows,
+                                                            c.rows_unit))
+
+
 def main():
     args = parse_args()
-    if args.impl == "reference":
+    if args.profile:
+        run_profile(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

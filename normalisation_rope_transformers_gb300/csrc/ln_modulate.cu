@@ -4,59 +4,87 @@
 // dit_fused_kernels: LayerNorm + modulation) without its formula; this computes
 // the plain adaLN reading:
 //   mu = mean(x), var = mean((x - mu)^2)  (biased, f32 statistics)
-//   out = round((x - mu) * rsqrt(var + eps) * (1 + scale) + shift)
+//   out = round((x - mu) / sqrt(var + eps) * (1 + scale) + shift)
 // with shift/scale taken from sample row r / rows_per_sample.
 //
-// Design: one block per row with the row held in registers (read once, written
-// once).  The mean and the centred variance are two reductions over the
-// register-resident values, so the variance does not suffer the cancellation of
-// the one-pass E[x^2] - mu^2 form.  Rows longer than the register budget use a
-// three-pass kernel that re-reads the (L2-resident) row.
+// Design: a row belongs to a group of WPR warps (one warp for rows of up to
+// 512 vectors, e.g. hidden 3072 bf16 = 384 vectors = 12 per lane); a block of
+// 128 threads holds 4 / WPR such groups.  The row is loaded once into
+// registers, the mean and the centred variance are two reductions over the
+// register-resident values (warp shuffles; one shared-memory step only when
+// WPR > 1), and the output is written once.  Rows longer than 16 vectors per
+// thread at WPR = 8 use a three-pass kernel that re-reads the (L2-resident) row.
 #include "nr_common.cuh"
 #include "nr_internal.h"
 
 namespace nr {
 namespace {
 
-template <typename T, int VPT>
-__global__ void __launch_bounds__(kRowMaxThreads) ln_modulate_row_kernel(
+constexpr int kLnThreads = 128;
+
+// Sum over the WPR warps of a row group; every thread of the group gets the
+// same total.  `scratch` holds one float per warp of the block; the caller
+// separates two uses of one scratch array by a barrier (or uses two arrays).
+template <int WPR>
+__device__ __forceinline__ float row_group_sum(float v, float* scratch) {
+  v = group_sum<kWarp>(v);
+  if (WPR == 1) return v;
+  const int warp = threadIdx.x / kWarp;
+  if (threadIdx.x % kWarp == 0) scratch[warp] = v;
+  __syncthreads();
+  const int first = (warp / WPR) * WPR;
+  float total = 0.0f;
+#pragma unroll
+  for (int i = 0; i < WPR; i++) total += scratch[first + i];
+  return total;
+}
+
+template <typename T, int VPT, int WPR>
+__global__ void __launch_bounds__(kLnThreads) ln_modulate_rows_kernel(
     T* __restrict__ out, const T* __restrict__ x, const T* __restrict__ shift,
-    const T* __restrict__ scale, int nvec, int64_t rows_per_sample, float hidden_f, float eps) {
+    const T* __restrict__ scale, int64_t rows, int nvec, int64_t rows_per_sample, float hidden_f,
+    float eps) {
   constexpr int N = Vec<T>::N;
-  __shared__ float scratch_mean[32];
-  __shared__ float scratch_var[32];
-  const int64_t row = blockIdx.x;
-  const uint4* xr = reinterpret_cast<const uint4*>(x) + row * nvec;
-  uint4* orow = reinterpret_cast<uint4*>(out) + row * nvec;
-  const int64_t sample_off = (row / rows_per_sample) * nvec;
+  constexpr int TPR = kWarp * WPR;          // threads per row
+  constexpr int RPB = kLnThreads / TPR;     // rows per block
+  __shared__ float scratch_mean[kLnThreads / kWarp];
+  __shared__ float scratch_var[kLnThreads / kWarp];
+  const int t = threadIdx.x % TPR;
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * RPB + threadIdx.x / TPR;
+  // Rows past the end still take part in the reductions' barriers (WPR > 1).
+  const bool active = row < rows;
+  const int64_t r = active ? row : 0;
+  const uint4* xr = reinterpret_cast<const uint4*>(x) + r * nvec;
+  uint4* orow = reinterpret_cast<uint4*>(out) + r * nvec;
+  const int64_t sample_off = (r / rows_per_sample) * nvec;
   const uint4* shv = reinterpret_cast<const uint4*>(shift) + sample_off;
   const uint4* scv = reinterpret_cast<const uint4*>(scale) + sample_off;
 
   uint4 xv[VPT];
 #pragma unroll
   for (int k = 0; k < VPT; k++) {
-    const int vi = threadIdx.x + k * blockDim.x;
-    if (vi < nvec) xv[k] = ld_stream(xr + vi);
+    const int vi = t + k * TPR;
+    if (active && vi < nvec) xv[k] = ld_stream(xr + vi);
   }
 
   float sum = 0.0f;
 #pragma unroll
   for (int k = 0; k < VPT; k++) {
-    const int vi = threadIdx.x + k * blockDim.x;
-    if (vi < nvec) {
+    const int vi = t + k * TPR;
+    if (active && vi < nvec) {
       float v[N];
       Vec<T>::unpack(xv[k], v);
 #pragma unroll
       for (int e = 0; e < N; e++) sum += v[e];
     }
   }
-  const float mu = __fdiv_rn(block_sum(sum, scratch_mean), hidden_f);
+  const float mu = __fdiv_rn(row_group_sum<WPR>(sum, scratch_mean), hidden_f);
 
   float dev = 0.0f;
 #pragma unroll
   for (int k = 0; k < VPT; k++) {
-    const int vi = threadIdx.x + k * blockDim.x;
-    if (vi < nvec) {
+    const int vi = t + k * TPR;
+    if (active && vi < nvec) {
       float v[N];
       Vec<T>::unpack(xv[k], v);
 #pragma unroll
@@ -66,18 +94,20 @@ __global__ void __launch_bounds__(kRowMaxThreads) ln_modulate_row_kernel(
       }
     }
   }
-  const float rstd = 1.0f / sqrtf(__fdiv_rn(block_sum(dev, scratch_var), hidden_f) + eps);
+  const float rstd = 1.0f / sqrtf(__fdiv_rn(row_group_sum<WPR>(dev, scratch_var), hidden_f) + eps);
+  if (!active) return;
+  const float neg_mu_rstd = -mu * rstd;  // xhat = v * rstd - mu * rstd
 
 #pragma unroll
   for (int k = 0; k < VPT; k++) {
-    const int vi = threadIdx.x + k * blockDim.x;
+    const int vi = t + k * TPR;
     if (vi < nvec) {
       float v[N], sh[N], sc[N];
       Vec<T>::unpack(xv[k], v);
       Vec<T>::unpack(ld_param(shv + vi), sh);
       Vec<T>::unpack(ld_param(scv + vi), sc);
 #pragma unroll
-      for (int e = 0; e < N; e++) v[e] = fmaf((v[e] - mu) * rstd, 1.0f + sc[e], sh[e]);
+      for (int e = 0; e < N; e++) v[e] = fmaf(fmaf(v[e], rstd, neg_mu_rstd), 1.0f + sc[e], sh[e]);
       st_stream(orow + vi, Vec<T>::pack(v));
     }
   }
@@ -117,6 +147,7 @@ __global__ void __launch_bounds__(1024) ln_modulate_long_row_kernel(
     }
   }
   const float rstd = 1.0f / sqrtf(__fdiv_rn(block_sum(dev, scratch_var), hidden_f) + eps);
+  const float neg_mu_rstd = -mu * rstd;
   // out may alias x: each thread overwrites only vectors it has finished reading.
   for (int64_t vi = threadIdx.x; vi < nvec; vi += blockDim.x) {
     float v[N], sh[N], sc[N];
@@ -124,43 +155,77 @@ __global__ void __launch_bounds__(1024) ln_modulate_long_row_kernel(
     Vec<T>::unpack(ld_param(shv + vi), sh);
     Vec<T>::unpack(ld_param(scv + vi), sc);
 #pragma unroll
-    for (int e = 0; e < N; e++) v[e] = fmaf((v[e] - mu) * rstd, 1.0f + sc[e], sh[e]);
+    for (int e = 0; e < N; e++) v[e] = fmaf(fmaf(v[e], rstd, neg_mu_rstd), 1.0f + sc[e], sh[e]);
     st_stream(orow + vi, Vec<T>::pack(v));
   }
 }
 
-template <typename T, int VPT>
-cudaError_t launch_rows(const RowLaunch& g, void* out, const void* x, const void* shift,
-                        const void* scale, int64_t rows, int nvec, int64_t rps, float hidden_f,
-                        float eps, cudaStream_t s) {
-  ln_modulate_row_kernel<T, VPT><<<dim3(static_cast<unsigned>(rows)), dim3(g.threads), 0, s>>>(
-      static_cast<T*>(out), static_cast<const T*>(x), static_cast<const T*>(shift),
-      static_cast<const T*>(scale), nvec, rps, hidden_f, eps);
+struct LnArgs {
+  void* out;
+  const void* x;
+  const void* shift;
+  const void* scale;
+  int64_t rows;
+  int nvec;
+  int64_t rps;
+  float hidden_f;
+  float eps;
+};
+
+template <typename T, int VPT, int WPR>
+cudaError_t launch_rows(const LnArgs& a, cudaStream_t s) {
+  constexpr int RPB = kLnThreads / (kWarp * WPR);
+  const int64_t blocks = (a.rows + RPB - 1) / RPB;
+  ln_modulate_rows_kernel<T, VPT, WPR><<<dim3(static_cast<unsigned>(blocks)), kLnThreads, 0, s>>>(
+      static_cast<T*>(a.out), static_cast<const T*>(a.x), static_cast<const T*>(a.shift),
+      static_cast<const T*>(a.scale), a.rows, a.nvec, a.rps, a.hidden_f, a.eps);
   return cudaGetLastError();
 }
 
+// Vectors per thread offered for one-warp rows, and for rows spread over
+// 2, 4 or 8 warps.
+constexpr int kLnVptOneWarp[] = {1, 2, 3, 4, 6, 8, 10, 12, 16};
+constexpr int kLnVptMultiWarp[] = {8, 12, 16};
+
 template <typename T>
-cudaError_t launch_typed(void* out, const void* x, const void* shift, const void* scale,
-                         int64_t rows, int64_t hidden, int64_t rps, float eps, cudaStream_t s) {
-  const int64_t nvec = hidden / Vec<T>::N;
-  const float hidden_f = static_cast<float>(hidden);
-  const RowLaunch g = pick_row_launch(nvec);
-  const int nv = static_cast<int>(nvec);
-  switch (g.vpt) {
-    case 1: return launch_rows<T, 1>(g, out, x, shift, scale, rows, nv, rps, hidden_f, eps, s);
-    case 2: return launch_rows<T, 2>(g, out, x, shift, scale, rows, nv, rps, hidden_f, eps, s);
-    case 3: return launch_rows<T, 3>(g, out, x, shift, scale, rows, nv, rps, hidden_f, eps, s);
-    case 4: return launch_rows<T, 4>(g, out, x, shift, scale, rows, nv, rps, hidden_f, eps, s);
-    case 5: return launch_rows<T, 5>(g, out, x, shift, scale, rows, nv, rps, hidden_f, eps, s);
-    case 6: return launch_rows<T, 6>(g, out, x, shift, scale, rows, nv, rps, hidden_f, eps, s);
-    case 8: return launch_rows<T, 8>(g, out, x, shift, scale, rows, nv, rps, hidden_f, eps, s);
-    case 12: return launch_rows<T, 12>(g, out, x, shift, scale, rows, nv, rps, hidden_f, eps, s);
-    case 16: return launch_rows<T, 16>(g, out, x, shift, scale, rows, nv, rps, hidden_f, eps, s);
-    default: break;
+cudaError_t launch_typed(const LnArgs& a, cudaStream_t s) {
+  const int64_t nvec = a.nvec;
+  for (int wpr : {1, 2, 4, 8}) {
+    const int64_t need = (nvec + kWarp * wpr - 1) / (kWarp * wpr);
+    if (need > 16) continue;
+    int vpt = 0;
+    if (wpr == 1) {
+      for (int v : kLnVptOneWarp)
+        if (vpt == 0 && v >= need) vpt = v;
+    } else {
+      for (int v : kLnVptMultiWarp)
+        if (vpt == 0 && v >= need) vpt = v;
+    }
+    switch (wpr * 100 + vpt) {
+      case 101: return launch_rows<T, 1, 1>(a, s);
+      case 102: return launch_rows<T, 2, 1>(a, s);
+      case 103: return launch_rows<T, 3, 1>(a, s);
+      case 104: return launch_rows<T, 4, 1>(a, s);
+      case 106: return launch_rows<T, 6, 1>(a, s);
+      case 108: return launch_rows<T, 8, 1>(a, s);
+      case 110: return launch_rows<T, 10, 1>(a, s);
+      case 112: return launch_rows<T, 12, 1>(a, s);
+      case 116: return launch_rows<T, 16, 1>(a, s);
+      case 208: return launch_rows<T, 8, 2>(a, s);
+      case 212: return launch_rows<T, 12, 2>(a, s);
+      case 216: return launch_rows<T, 16, 2>(a, s);
+      case 408: return launch_rows<T, 8, 4>(a, s);
+      case 412: return launch_rows<T, 12, 4>(a, s);
+      case 416: return launch_rows<T, 16, 4>(a, s);
+      case 808: return launch_rows<T, 8, 8>(a, s);
+      case 812: return launch_rows<T, 12, 8>(a, s);
+      case 816: return launch_rows<T, 16, 8>(a, s);
+      default: break;
+    }
   }
-  ln_modulate_long_row_kernel<T><<<dim3(static_cast<unsigned>(rows)), 1024, 0, s>>>(
-      static_cast<T*>(out), static_cast<const T*>(x), static_cast<const T*>(shift),
-      static_cast<const T*>(scale), nvec, rps, hidden_f, eps);
+  ln_modulate_long_row_kernel<T><<<dim3(static_cast<unsigned>(a.rows)), 1024, 0, s>>>(
+      static_cast<T*>(a.out), static_cast<const T*>(a.x), static_cast<const T*>(a.shift),
+      static_cast<const T*>(a.scale), nvec, a.rps, a.hidden_f, a.eps);
   return cudaGetLastError();
 }
 
@@ -169,10 +234,18 @@ cudaError_t launch_typed(void* out, const void* x, const void* shift, const void
 cudaError_t launch_ln_modulate(void* out, const void* x, const void* shift, const void* scale,
                                int64_t rows, int64_t hidden, int64_t rows_per_sample,
                                int is_bf16, float eps, cudaStream_t stream) {
-  if (is_bf16)
-    return launch_typed<__nv_bfloat16>(out, x, shift, scale, rows, hidden, rows_per_sample, eps,
-                                       stream);
-  return launch_typed<float>(out, x, shift, scale, rows, hidden, rows_per_sample, eps, stream);
+  LnArgs a;
+  a.out = out;
+  a.x = x;
+  a.shift = shift;
+  a.scale = scale;
+  a.rows = rows;
+  a.nvec = static_cast<int>(hidden / (is_bf16 ? 8 : 4));
+  a.rps = rows_per_sample;
+  a.hidden_f = static_cast<float>(hidden);
+  a.eps = eps;
+  if (is_bf16) return launch_typed<__nv_bfloat16>(a, stream);
+  return launch_typed<float>(a, stream);
 }
 
 }  // namespace nr

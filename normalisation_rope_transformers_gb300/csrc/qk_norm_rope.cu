@@ -12,13 +12,18 @@
 //    shifted by D/2 -- so both members of every rotated pair sit in the same
 //    lane and the rotation needs no data exchange.  The row's sum of squares
 //    is a butterfly over the L lanes.
-//  * A block handles a tile of tokens (all their Q and K heads).  Each
-//    (token, pair) angle is computed once per tile into shared memory and
-//    reused by every head of that token: the angle pos*freq_i is reduced
-//    modulo one turn exactly, as (pos * turn_i) mod 2^64 with
-//    turn_i = frac(freq_i / 2pi) * 2^64 prepared on the host in double, then
-//    sincospif evaluates the reduced angle.  No f64 math runs on the device
-//    and no cos/sin table is read from HBM.
+//  * A warp owns whole tokens (all their Q and K heads), persistently: warp w
+//    of W takes tokens w, w + W, ...  Its head rows form one flat stream of
+//    iterations (32/L rows per iteration) that crosses token boundaries, and a
+//    rolling register prefetch keeps the next R iterations' loads in flight
+//    while the current one is computed.  There is no block-level barrier
+//    after the weights are staged, so warps never wait for each other.
+//  * Each (token, pair) angle is computed once per warp (a few sincospif per
+//    lane) into a per-warp shared-memory table and reused by all the token's
+//    heads.  The angle pos*freq_i is reduced modulo one turn exactly, as
+//    (pos * turn_i) mod 2^64 with turn_i = frac(freq_i / 2pi) * 2^64 prepared
+//    on the host in double; the top 32 bits feed sincospif.  No f64 math runs
+//    on the device and no cos/sin table is read from HBM.
 //  * Head rows are read once and written once (in place allowed).
 #include "nr_common.cuh"
 #include "nr_internal.h"
@@ -26,8 +31,8 @@
 namespace nr {
 namespace {
 
-constexpr int kQkThreads = 256;
-constexpr int kQkIter = 4;  // head rows per group held in registers at once
+constexpr int kQkThreads = 128;
+constexpr int kQkWarps = kQkThreads / kWarp;
 
 template <typename WT>
 __device__ __forceinline__ float load_w(const WT* w, int i);
@@ -53,70 +58,29 @@ struct QkArgs {
   int64_t k_stride;
   int hq;
   int hk;
-  int tile_tokens;
   float eps;
   float inv_d;
   float w_add;
 };
 
 // T: storage dtype of q/k; WT: weight dtype; L: lanes per head row
-// (head_dim = 2 * L * N with N = 128-bit vector width in elements).
-template <typename T, typename WT, int L>
+// (head_dim = 2 * L * N with N = 128-bit vector width in elements);
+// R: iterations kept in flight per warp.
+template <typename T, typename WT, int L, int R>
 __global__ void __launch_bounds__(kQkThreads) qk_norm_rope_kernel(const QkArgs a,
                                                                   const RopeTurns turns) {
   constexpr int N = Vec<T>::N;
   constexpr int HALF = L * N;
   constexpr int D = 2 * HALF;
-  constexpr int G = kQkThreads / L;  // groups (head rows in flight) per block
+  constexpr int GW = kWarp / L;  // head rows per warp iteration
 
-  extern __shared__ float2 trig[];        // [tile_tokens][HALF] (cos, sin)
-  __shared__ __align__(16) float wsm[2 * D];  // q weights then k weights (+ gemma 1)
+  __shared__ __align__(16) float wsm[2 * D];              // q weights, k weights (+ gemma 1)
+  __shared__ __align__(16) float2 trig[kQkWarps][HALF];   // per-warp (cos, sin) of one token
+  __shared__ unsigned long long turn_sm[HALF];              // the rotary turn constants
 
-  const int tid = threadIdx.x;
-  const int lane = tid % L;
-  const int group = tid / L;
-  const int heads = a.hq + a.hk;
-  const int64_t t0 = static_cast<int64_t>(blockIdx.x) * a.tile_tokens;
-  const int64_t left = a.tokens - t0;
-  const int tc = left < a.tile_tokens ? static_cast<int>(left) : a.tile_tokens;
-  const int rows_in_tile = tc * heads;
-
-  // Issue this group's first head-row loads before the per-tile set-up, so
-  // their latency overlaps the angle computation.
-  uint4 va[kQkIter], vb[kQkIter];
-  auto row_ptrs = [&](int r, const uint4*& src, uint4*& dst) {
-    const int tt = r / heads;
-    const int h = r - tt * heads;
-    const int64_t tok = t0 + tt;
-    if (h < a.hq) {
-      const int64_t off = tok * a.q_stride + static_cast<int64_t>(h) * D;
-      src = reinterpret_cast<const uint4*>(static_cast<const T*>(a.q) + off);
-      dst = reinterpret_cast<uint4*>(static_cast<T*>(a.q_out) + off);
-    } else {
-      const int64_t off = tok * a.k_stride + static_cast<int64_t>(h - a.hq) * D;
-      src = reinterpret_cast<const uint4*>(static_cast<const T*>(a.k) + off);
-      dst = reinterpret_cast<uint4*>(static_cast<T*>(a.k_out) + off);
-    }
-  };
-  auto issue_loads = [&](int chunk) {
-#pragma unroll
-    for (int it = 0; it < kQkIter; it++) {
-      const int r = chunk + group + it * G;
-      if (r < rows_in_tile) {
-        const uint4* src;
-        uint4* dst;
-        row_ptrs(r, src, dst);
-        va[it] = ld_stream(src + lane);
-        vb[it] = ld_stream(src + L + lane);
-      }
-    }
-  };
-  issue_loads(0);
-
-  // Per-tile set-up: weights (with the gemma +1) and the angles.
   const WT* wq = static_cast<const WT*>(a.wq);
   const WT* wk = static_cast<const WT*>(a.wk);
-  for (int i = tid; i < 2 * D; i += kQkThreads) {
+  for (int i = threadIdx.x; i < 2 * D; i += kQkThreads) {
     float wv = 0.0f;
     if (i < D)
       wv = load_w<WT>(wq, i);
@@ -124,70 +88,159 @@ __global__ void __launch_bounds__(kQkThreads) qk_norm_rope_kernel(const QkArgs a
       wv = load_w<WT>(wk, i - D);
     wsm[i] = wv + a.w_add;
   }
-  for (int e = tid; e < tc * HALF; e += kQkThreads) {
-    const int tt = e / HALF;
-    const int i = e - tt * HALF;
-    const int64_t p = a.pos[t0 + tt];
-    // (p * turn_i) mod 2^64: the angle as a fraction of a turn, exact for any
-    // int32 position (two's complement covers negative positions).
-    const unsigned long long prod = static_cast<unsigned long long>(p) * turns.turn[i];
-    const int hi = static_cast<int>(prod >> 32);  // signed turn fraction * 2^32
-    float s, c;
-    sincospif(static_cast<float>(hi) * 0x1p-31f, &s, &c);  // angle = pi * (hi / 2^31)
-    trig[e] = make_float2(c, s);
-  }
-  __syncthreads();
+  for (int i = threadIdx.x; i < HALF; i += kQkThreads) turn_sm[i] = turns.turn[i];
+  __syncthreads();  // the only block-level barrier
 
-  for (int chunk = 0; chunk < rows_in_tile; chunk += G * kQkIter) {
-    if (chunk > 0) issue_loads(chunk);
+  const int warp = threadIdx.x / kWarp;
+  const int lane32 = threadIdx.x % kWarp;
+  const int g = lane32 / L;  // head row within the iteration
+  const int l = lane32 % L;  // vector slot within each half of the row
+  const int64_t gw = static_cast<int64_t>(blockIdx.x) * kQkWarps + warp;
+  const int64_t W = static_cast<int64_t>(gridDim.x) * kQkWarps;
+  if (gw >= a.tokens) return;
+  const int H = a.hq + a.hk;
+  const int IT = (H + GW - 1) / GW;  // iterations per token
+  const int64_t my_tokens = (a.tokens - gw + W - 1) / W;
+  const int64_t J = my_tokens * IT;  // this warp's iterations
+
+  // Where iteration j's row for this lane lives (and whether it exists).
+  auto locate = [&](int64_t j, const uint4*& src, uint4*& dst, int64_t& tok, int& it) -> bool {
+    const int64_t ti = j / IT;
+    it = static_cast<int>(j - ti * IT);
+    tok = gw + ti * W;
+    const int row = it * GW + g;
+    if (row >= H) return false;
+    if (row < a.hq) {
+      const int64_t off = tok * a.q_stride + static_cast<int64_t>(row) * D;
+      src = reinterpret_cast<const uint4*>(static_cast<const T*>(a.q) + off);
+      dst = reinterpret_cast<uint4*>(static_cast<T*>(a.q_out) + off);
+    } else {
+      const int64_t off = tok * a.k_stride + static_cast<int64_t>(row - a.hq) * D;
+      src = reinterpret_cast<const uint4*>(static_cast<const T*>(a.k) + off);
+      dst = reinterpret_cast<uint4*>(static_cast<T*>(a.k_out) + off);
+    }
+    return true;
+  };
+
+  uint4 va[R], vb[R];
+  int pos_at[R];  // position of the slot's token (loaded with its first iteration)
+  auto issue = [&](int64_t j, int slot) {
+    const uint4* src;
+    uint4* dst;
+    int64_t tok;
+    int it;
+    if (locate(j, src, dst, tok, it)) {
+      va[slot] = ld_stream(src + l);
+      vb[slot] = ld_stream(src + L + l);
+    }
+    if (it == 0) pos_at[slot] = __ldg(a.pos + tok);
+  };
+
 #pragma unroll
-    for (int it = 0; it < kQkIter; it++) {
-      const int r = chunk + group + it * G;
-      const bool valid = r < rows_in_tile;
-      float xa[N], xb[N];
-      float ss = 0.0f;
-      if (valid) {
-        Vec<T>::unpack(va[it], xa);
-        Vec<T>::unpack(vb[it], xb);
+  for (int s = 0; s < R; s++)
+    if (s < J) issue(s, s);
+
+  float2 cs[N];  // (cos, sin) of this lane's pairs for the current token
+  for (int64_t base = 0; base < J; base += R) {
 #pragma unroll
-        for (int e = 0; e < N; e++) {
-          ss = fmaf(xa[e], xa[e], ss);
-          ss = fmaf(xb[e], xb[e], ss);
-        }
-      }
-      // Every lane joins the butterfly (full-warp shuffles), valid or not.
-      ss = group_sum<L>(ss);
-      if (valid) {
+    for (int s = 0; s < R; s++) {
+      const int64_t j = base + s;
+      if (j < J) {
         const uint4* src;
         uint4* dst;
-        row_ptrs(r, src, dst);
-        const int tt = r / heads;
-        const bool is_q = (r - tt * heads) < a.hq;
-        const float inv = rsqrtf(ss * a.inv_d + a.eps);
-        const float* w = wsm + (is_q ? 0 : D);
-        const float2* cs = trig + tt * HALF + lane * N;
-        float oa[N], ob[N];
+        int64_t tok;
+        int it;
+        const bool valid = locate(j, src, dst, tok, it);
+        if (it == 0) {
+          // New token: its angles, once per warp, then this lane's N pairs.
+          const unsigned long long p = static_cast<unsigned long long>(
+              static_cast<long long>(pos_at[s]));
+          __syncwarp();
+          for (int i = lane32; i < HALF; i += kWarp) {
+            const unsigned long long prod = p * turn_sm[i];  // angle, in turns, mod 1
+            const int hi = static_cast<int>(prod >> 32);        // signed turn fraction * 2^32
+            float sn, cn;
+            sincospif(static_cast<float>(hi) * 0x1p-31f, &sn, &cn);  // angle = pi * hi / 2^31
+            trig[warp][i] = make_float2(cn, sn);
+          }
+          __syncwarp();
 #pragma unroll
-        for (int e = 0; e < N; e++) {
-          const float na = xa[e] * inv * w[lane * N + e];
-          const float nb = xb[e] * inv * w[HALF + lane * N + e];
-          const float2 t = cs[e];
-          oa[e] = fmaf(na, t.x, -nb * t.y);
-          ob[e] = fmaf(na, t.y, nb * t.x);
+          for (int e = 0; e < N; e++) cs[e] = trig[warp][l * N + e];
         }
-        st_stream(dst + lane, Vec<T>::pack(oa));
-        st_stream(dst + L + lane, Vec<T>::pack(ob));
+        float xa[N], xb[N];
+        float ss = 0.0f;
+        if (valid) {
+          Vec<T>::unpack(va[s], xa);
+          Vec<T>::unpack(vb[s], xb);
+#pragma unroll
+          for (int e = 0; e < N; e++) {
+            ss = fmaf(xa[e], xa[e], ss);
+            ss = fmaf(xb[e], xb[e], ss);
+          }
+        }
+        // The slot is free again: start the load R iterations ahead.
+        if (j + R < J) issue(j + R, s);
+        // Every lane joins the butterfly (full-warp shuffles), valid or not.
+        ss = group_sum<L>(ss);
+        if (valid) {
+          const int row = it * GW + g;
+          const float inv = rsqrtf(ss * a.inv_d + a.eps);
+          const float* w = wsm + (row < a.hq ? 0 : D) + l * N;
+          float oa[N], ob[N];
+#pragma unroll
+          for (int e = 0; e < N; e++) {
+            const float na = xa[e] * inv * w[e];
+            const float nb = xb[e] * inv * w[HALF + e];
+            oa[e] = fmaf(na, cs[e].x, -nb * cs[e].y);
+            ob[e] = fmaf(na, cs[e].y, nb * cs[e].x);
+          }
+          st_stream(dst + l, Vec<T>::pack(oa));
+          st_stream(dst + L + l, Vec<T>::pack(ob));
+        }
       }
     }
   }
 }
 
+// Resident blocks per SM of one kernel instantiation, cached per device.
+template <typename T, typename WT, int L, int R>
+int blocks_per_sm(int device) {
+  static int cached[64] = {0};
+  if (device < 0 || device >= 64) return 1;
+  if (cached[device] == 0) {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, qk_norm_rope_kernel<T, WT, L, R>,
+                                                      kQkThreads, 0) != cudaSuccess ||
+        n < 1)
+      n = 1;
+    cached[device] = n;
+  }
+  return cached[device];
+}
+
+int sm_count(int device) {
+  static int cached[64] = {0};
+  if (device < 0 || device >= 64) return 1;
+  if (cached[device] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, device) != cudaSuccess || n < 1)
+      n = 1;
+    cached[device] = n;
+  }
+  return cached[device];
+}
+
 template <typename T, typename WT, int L>
 cudaError_t launch_l(const QkArgs& a, const RopeTurns& turns, cudaStream_t s) {
-  constexpr int HALF = L * Vec<T>::N;
-  const int64_t tiles = (a.tokens + a.tile_tokens - 1) / a.tile_tokens;
-  const size_t smem = static_cast<size_t>(a.tile_tokens) * HALF * sizeof(float2);
-  qk_norm_rope_kernel<T, WT, L><<<dim3(static_cast<unsigned>(tiles)), kQkThreads, smem, s>>>(
+  constexpr int R = (L >= 16) ? 4 : 6;
+  int device = 0;
+  cudaError_t e = cudaGetDevice(&device);
+  if (e != cudaSuccess) return e;
+  const int64_t resident =
+      static_cast<int64_t>(sm_count(device)) * blocks_per_sm<T, WT, L, R>(device);
+  const int64_t needed = (a.tokens + kQkWarps - 1) / kQkWarps;  // one warp per token at most
+  const int64_t blocks = needed < resident ? needed : resident;
+  qk_norm_rope_kernel<T, WT, L, R><<<dim3(static_cast<unsigned>(blocks)), kQkThreads, 0, s>>>(
       a, turns);
   return cudaGetLastError();
 }
@@ -207,9 +260,6 @@ cudaError_t launch_w(const QkArgs& a, int lanes, const RopeTurns& turns, cudaStr
 
 }  // namespace
 
-// Shared memory for the angle table is kept at or below this per block.
-constexpr int kTrigSmemBytes = 32 * 1024;
-
 cudaError_t launch_qk_norm_rope(void* q_out, void* k_out, const void* q, const void* k,
                                 const void* wq, const void* wk, int w_is_bf16,
                                 const int32_t* positions, int64_t tokens, int64_t hq, int64_t hk,
@@ -218,16 +268,6 @@ cudaError_t launch_qk_norm_rope(void* q_out, void* k_out, const void* q, const v
                                 cudaStream_t stream) {
   const int n = is_bf16 ? 8 : 4;
   const int lanes = static_cast<int>(head_dim / (2 * n));
-  const int groups = kQkThreads / lanes;
-  const int64_t heads = hq + hk;
-  // Tokens per block: enough head rows to fill every group kQkIter times,
-  // bounded by the angle table's shared memory and by the token count.
-  int64_t tile = (static_cast<int64_t>(groups) * kQkIter) / heads;
-  const int64_t tile_max = kTrigSmemBytes / ((head_dim / 2) * static_cast<int64_t>(sizeof(float2)));
-  if (tile > tile_max) tile = tile_max;
-  if (tile > tokens) tile = tokens;
-  if (tile < 1) tile = 1;
-
   QkArgs a;
   a.q_out = q_out;
   a.k_out = k_out;
@@ -241,7 +281,6 @@ cudaError_t launch_qk_norm_rope(void* q_out, void* k_out, const void* q, const v
   a.k_stride = k_tok_stride;
   a.hq = static_cast<int>(hq);
   a.hk = static_cast<int>(hk);
-  a.tile_tokens = static_cast<int>(tile);
   a.eps = eps;
   a.inv_d = 1.0f / static_cast<float>(head_dim);
   a.w_add = gemma ? 1.0f : 0.0f;

@@ -9,7 +9,7 @@
 //
 // Design: a row belongs to a group of WPR warps (one warp for rows of up to
 // 512 vectors, e.g. hidden 3072 bf16 = 384 vectors = 12 per lane); a block of
-// 128 threads holds 4 / WPR such groups.  The row is loaded once into
+// 128 threads holds 4 / WPR such groups (a row of 8 warps is its own block).  The row is loaded once into
 // registers, the mean and the centred variance are two reductions over the
 // register-resident values (warp shuffles; one shared-memory step only when
 // WPR > 1), and the output is written once.  Rows longer than 16 vectors per
@@ -20,7 +20,12 @@
 namespace nr {
 namespace {
 
-constexpr int kLnThreads = 128;
+// Block size of a WPR-warp row group kernel: 128 threads, or one row group
+// when a row needs more than 4 warps.
+template <int WPR>
+__host__ __device__ constexpr int ln_threads() {
+  return WPR > 4 ? kWarp * WPR : 128;
+}
 
 // Sum over the WPR warps of a row group; every thread of the group gets the
 // same total.  `scratch` holds one float per warp of the block; the caller
@@ -40,15 +45,17 @@ __device__ __forceinline__ float row_group_sum(float v, float* scratch) {
 }
 
 template <typename T, int VPT, int WPR>
-__global__ void __launch_bounds__(kLnThreads) ln_modulate_rows_kernel(
+__global__ void __launch_bounds__(ln_threads<WPR>()) ln_modulate_rows_kernel(
     T* __restrict__ out, const T* __restrict__ x, const T* __restrict__ shift,
     const T* __restrict__ scale, int64_t rows, int nvec, int64_t rows_per_sample, float hidden_f,
     float eps) {
   constexpr int N = Vec<T>::N;
-  constexpr int TPR = kWarp * WPR;          // threads per row
-  constexpr int RPB = kLnThreads / TPR;     // rows per block
-  __shared__ float scratch_mean[kLnThreads / kWarp];
-  __shared__ float scratch_var[kLnThreads / kWarp];
+  constexpr int THREADS = ln_threads<WPR>();
+  constexpr int TPR = kWarp * WPR;       // threads per row
+  constexpr int RPB = THREADS / TPR;     // rows per block
+  static_assert(RPB >= 1 && RPB * TPR == THREADS, "row groups must tile the block");
+  __shared__ float scratch_mean[THREADS / kWarp];
+  __shared__ float scratch_var[THREADS / kWarp];
   const int t = threadIdx.x % TPR;
   const int64_t row = static_cast<int64_t>(blockIdx.x) * RPB + threadIdx.x / TPR;
   // Rows past the end still take part in the reductions' barriers (WPR > 1).
@@ -174,9 +181,11 @@ struct LnArgs {
 
 template <typename T, int VPT, int WPR>
 cudaError_t launch_rows(const LnArgs& a, cudaStream_t s) {
-  constexpr int RPB = kLnThreads / (kWarp * WPR);
+  constexpr int THREADS = ln_threads<WPR>();
+  constexpr int RPB = THREADS / (kWarp * WPR);
+  static_assert(RPB >= 1, "row groups must fit the block");
   const int64_t blocks = (a.rows + RPB - 1) / RPB;
-  ln_modulate_rows_kernel<T, VPT, WPR><<<dim3(static_cast<unsigned>(blocks)), kLnThreads, 0, s>>>(
+  ln_modulate_rows_kernel<T, VPT, WPR><<<dim3(static_cast<unsigned>(blocks)), THREADS, 0, s>>>(
       static_cast<T*>(a.out), static_cast<const T*>(a.x), static_cast<const T*>(a.shift),
       static_cast<const T*>(a.scale), a.rows, a.nvec, a.rps, a.hidden_f, a.eps);
   return cudaGetLastError();

@@ -100,22 +100,30 @@ __global__ void __launch_bounds__(kQkThreads) qk_norm_rope_kernel(const QkArgs a
   if (gw >= a.tokens) return;
   const int H = a.hq + a.hk;
   const int IT = (H + GW - 1) / GW;  // iterations per token
-  const int64_t my_tokens = (a.tokens - gw + W - 1) / W;
-  const int64_t J = my_tokens * IT;  // this warp's iterations
 
-  // Where iteration j's row for this lane lives (and whether it exists).
-  auto locate = [&](int64_t j, const uint4*& src, uint4*& dst, int64_t& tok, int& it) -> bool {
-    const int64_t ti = j / IT;
-    it = static_cast<int>(j - ti * IT);
-    tok = gw + ti * W;
-    const int row = it * GW + g;
+  // A cursor walks this warp's iterations: token gw, gw + W, ... and, within
+  // a token, iterations 0 .. IT-1 (rows it*GW .. it*GW + GW-1).  The load
+  // cursor runs R iterations ahead of the compute cursor.
+  struct Cursor {
+    int64_t tok;
+    int it;
+  };
+  auto advance = [&](Cursor& c) {
+    if (++c.it == IT) {
+      c.it = 0;
+      c.tok += W;
+    }
+  };
+  // Where this lane's row of the cursor's iteration lives (false: no row).
+  auto locate = [&](const Cursor& c, const uint4*& src, uint4*& dst) -> bool {
+    const int row = c.it * GW + g;
     if (row >= H) return false;
     if (row < a.hq) {
-      const int64_t off = tok * a.q_stride + static_cast<int64_t>(row) * D;
+      const int64_t off = c.tok * a.q_stride + static_cast<int64_t>(row) * D;
       src = reinterpret_cast<const uint4*>(static_cast<const T*>(a.q) + off);
       dst = reinterpret_cast<uint4*>(static_cast<T*>(a.q_out) + off);
     } else {
-      const int64_t off = tok * a.k_stride + static_cast<int64_t>(row - a.hq) * D;
+      const int64_t off = c.tok * a.k_stride + static_cast<int64_t>(row - a.hq) * D;
       src = reinterpret_cast<const uint4*>(static_cast<const T*>(a.k) + off);
       dst = reinterpret_cast<uint4*>(static_cast<T*>(a.k_out) + off);
     }
@@ -124,41 +132,38 @@ __global__ void __launch_bounds__(kQkThreads) qk_norm_rope_kernel(const QkArgs a
 
   uint4 va[R], vb[R];
   int pos_at[R];  // position of the slot's token (loaded with its first iteration)
-  auto issue = [&](int64_t j, int slot) {
+  Cursor ld{gw, 0}, cc{gw, 0};
+  auto issue = [&](int slot) {
     const uint4* src;
     uint4* dst;
-    int64_t tok;
-    int it;
-    if (locate(j, src, dst, tok, it)) {
+    if (locate(ld, src, dst)) {
       va[slot] = ld_stream(src + l);
       vb[slot] = ld_stream(src + L + l);
     }
-    if (it == 0) pos_at[slot] = __ldg(a.pos + tok);
+    if (ld.it == 0) pos_at[slot] = __ldg(a.pos + ld.tok);
+    advance(ld);
   };
 
 #pragma unroll
   for (int s = 0; s < R; s++)
-    if (s < J) issue(s, s);
+    if (ld.tok < a.tokens) issue(s);
 
   float2 cs[N];  // (cos, sin) of this lane's pairs for the current token
-  for (int64_t base = 0; base < J; base += R) {
+  while (cc.tok < a.tokens) {
 #pragma unroll
     for (int s = 0; s < R; s++) {
-      const int64_t j = base + s;
-      if (j < J) {
+      if (cc.tok < a.tokens) {
         const uint4* src;
         uint4* dst;
-        int64_t tok;
-        int it;
-        const bool valid = locate(j, src, dst, tok, it);
-        if (it == 0) {
+        const bool valid = locate(cc, src, dst);
+        if (cc.it == 0) {
           // New token: its angles, once per warp, then this lane's N pairs.
           const unsigned long long p = static_cast<unsigned long long>(
               static_cast<long long>(pos_at[s]));
           __syncwarp();
           for (int i = lane32; i < HALF; i += kWarp) {
             const unsigned long long prod = p * turn_sm[i];  // angle, in turns, mod 1
-            const int hi = static_cast<int>(prod >> 32);        // signed turn fraction * 2^32
+            const int hi = static_cast<int>(prod >> 32);      // signed turn fraction * 2^32
             float sn, cn;
             sincospif(static_cast<float>(hi) * 0x1p-31f, &sn, &cn);  // angle = pi * hi / 2^31
             trig[warp][i] = make_float2(cn, sn);
@@ -179,11 +184,11 @@ __global__ void __launch_bounds__(kQkThreads) qk_norm_rope_kernel(const QkArgs a
           }
         }
         // The slot is free again: start the load R iterations ahead.
-        if (j + R < J) issue(j + R, s);
+        if (ld.tok < a.tokens) issue(s);
         // Every lane joins the butterfly (full-warp shuffles), valid or not.
         ss = group_sum<L>(ss);
         if (valid) {
-          const int row = it * GW + g;
+          const int row = cc.it * GW + g;
           const float inv = rsqrtf(ss * a.inv_d + a.eps);
           const float* w = wsm + (row < a.hq ? 0 : D) + l * N;
           float oa[N], ob[N];
@@ -197,6 +202,7 @@ __global__ void __launch_bounds__(kQkThreads) qk_norm_rope_kernel(const QkArgs a
           st_stream(dst + l, Vec<T>::pack(oa));
           st_stream(dst + L + l, Vec<T>::pack(ob));
         }
+        advance(cc);
       }
     }
   }

@@ -19,7 +19,9 @@ namespace nr {
 namespace {
 
 // One block per row; thread t owns vectors t, t + blockDim, ..., (VPT of them).
-template <typename T, int VPT, bool RES>
+// PW: load the weight together with the row (saves a dependent round trip when
+// there are few rows, e.g. decode; costs registers when there are many).
+template <typename T, int VPT, bool RES, bool PW>
 __global__ void __launch_bounds__(kRowMaxThreads) rmsnorm_row_kernel(T* __restrict__ out,
                                                            const T* __restrict__ x,
                                                            const T* __restrict__ w,
@@ -36,12 +38,14 @@ __global__ void __launch_bounds__(kRowMaxThreads) rmsnorm_row_kernel(T* __restri
 
   uint4 xv[VPT];
   uint4 rv[VPT];
+  uint4 wpre[PW ? VPT : 1];
 #pragma unroll
   for (int k = 0; k < VPT; k++) {
     const int vi = threadIdx.x + k * blockDim.x;
     if (vi < nvec) {
       xv[k] = ld_stream(xr + vi);
       if (RES) rv[k] = ld_stream(rr + vi);
+      if (PW) wpre[PW ? k : 0] = ld_param(wv + vi);
     }
   }
 
@@ -78,7 +82,7 @@ __global__ void __launch_bounds__(kRowMaxThreads) rmsnorm_row_kernel(T* __restri
     if (vi < nvec) {
       float v[N], wf[N];
       Vec<T>::unpack(xv[k], v);
-      Vec<T>::unpack(ld_param(wv + vi), wf);
+      Vec<T>::unpack(PW ? wpre[PW ? k : 0] : ld_param(wv + vi), wf);
 #pragma unroll
       for (int e = 0; e < N; e++) v[e] = v[e] * inv * (wf[e] + w_add);
       st_stream(orow + vi, Vec<T>::pack(v));
@@ -133,21 +137,33 @@ __global__ void __launch_bounds__(1024) rmsnorm_long_row_kernel(T* __restrict__ 
   }
 }
 
+template <typename T, int VPT, bool PW>
+cudaError_t launch_rows_pw(const RowLaunch& g, void* out, const void* x, const void* w, void* res,
+                           int64_t rows, int nvec, float hidden_f, float eps, float w_add,
+                           cudaStream_t s) {
+  const dim3 grid(static_cast<unsigned>(rows));
+  const dim3 block(g.threads);
+  if (res != nullptr)
+    rmsnorm_row_kernel<T, VPT, true, PW><<<grid, block, 0, s>>>(
+        static_cast<T*>(out), static_cast<const T*>(x), static_cast<const T*>(w),
+        static_cast<T*>(res), nvec, hidden_f, eps, w_add);
+  else
+    rmsnorm_row_kernel<T, VPT, false, PW><<<grid, block, 0, s>>>(
+        static_cast<T*>(out), static_cast<const T*>(x), static_cast<const T*>(w), nullptr, nvec,
+        hidden_f, eps, w_add);
+  return cudaGetLastError();
+}
+
+// Rows per launch up to which the weight is fetched together with the row.
+constexpr int64_t kPrefetchWeightRows = 1024;
+
 template <typename T, int VPT>
 cudaError_t launch_rows(const RowLaunch& g, void* out, const void* x, const void* w, void* res,
                         int64_t rows, int nvec, float hidden_f, float eps, float w_add,
                         cudaStream_t s) {
-  const dim3 grid(static_cast<unsigned>(rows));
-  const dim3 block(g.threads);
-  if (res != nullptr)
-    rmsnorm_row_kernel<T, VPT, true><<<grid, block, 0, s>>>(
-        static_cast<T*>(out), static_cast<const T*>(x), static_cast<const T*>(w),
-        static_cast<T*>(res), nvec, hidden_f, eps, w_add);
-  else
-    rmsnorm_row_kernel<T, VPT, false><<<grid, block, 0, s>>>(
-        static_cast<T*>(out), static_cast<const T*>(x), static_cast<const T*>(w), nullptr, nvec,
-        hidden_f, eps, w_add);
-  return cudaGetLastError();
+  if (rows <= kPrefetchWeightRows)
+    return launch_rows_pw<T, VPT, true>(g, out, x, w, res, rows, nvec, hidden_f, eps, w_add, s);
+  return launch_rows_pw<T, VPT, false>(g, out, x, w, res, rows, nvec, hidden_f, eps, w_add, s);
 }
 
 template <typename T>

@@ -3,7 +3,9 @@
 // Follows vllm.cpp src/vt/cuda/cuda_ops.cu, "silu_and_mul" (gate = first half
 // of the row, up = second half, f32 math).  Design: a 2-D grid (vector column
 // blocks x rows) so no thread divides a flat index; each thread moves UNROLL
-// 128-bit vectors of gate and of up, issuing every load before any math.
+// 128-bit vectors of gate and of up, issuing every load before any math.  The
+// exponential and division are the cheap hardware forms for bf16 outputs
+// (see silu<T> below), so the kernel stays memory-bound.
 #include "nr_common.cuh"
 #include "nr_internal.h"
 
@@ -11,6 +13,27 @@ namespace nr {
 namespace {
 
 constexpr int kSiluThreads = 128;
+
+// silu(a) = a * sigmoid(a).  For bf16 outputs (8 significant bits) the
+// hardware exponential and reciprocal (relative error ~1e-6) are exact to well
+// within half an output ulp.  They are used in an overflow-free form:
+// t = e^-|a| lies in (0, 1], sigmoid(|a|) = 1 / (1 + t) and
+// sigmoid(-|a|) = t / (1 + t), so the divisor stays in [1, 2] and large
+// negative gates keep their tiny (possibly subnormal) result.  f32 outputs use
+// the accurate expf and an IEEE division.
+template <typename T>
+__device__ __forceinline__ float silu(float a);
+template <>
+__device__ __forceinline__ float silu<__nv_bfloat16>(float a) {
+  const float t = exp2f(-fabsf(a) * 1.4426950408889634f);  // e^-|a|, subnormals kept
+  const float r = __fdividef(1.0f, 1.0f + t);
+  return a * (a >= 0.0f ? r : t * r);
+}
+template <>
+__device__ __forceinline__ float silu<float>(float a) {
+  return a / (1.0f + expf(-a));
+}
+
 constexpr unsigned kMaxGridY = 65535;
 
 template <typename T, int UNROLL>
@@ -40,7 +63,7 @@ __global__ void __launch_bounds__(kSiluThreads) silu_and_mul_kernel(T* __restric
         Vec<T>::unpack(gv[u], a);
         Vec<T>::unpack(uv[u], b);
 #pragma unroll
-        for (int e = 0; e < N; e++) a[e] = a[e] * __frcp_rn(1.0f + expf(-a[e])) * b[e];
+        for (int e = 0; e < N; e++) a[e] = silu<T>(a[e]) * b[e];
         st_stream(o + c, Vec<T>::pack(a));
       }
     }

@@ -103,7 +103,6 @@ __global__ void __launch_bounds__(ln_threads<WPR>()) ln_modulate_rows_kernel(
   }
   const float rstd = 1.0f / sqrtf(__fdiv_rn(row_group_sum<WPR>(dev, scratch_var), hidden_f) + eps);
   if (!active) return;
-  const float neg_mu_rstd = -mu * rstd;  // xhat = v * rstd - mu * rstd
 
 #pragma unroll
   for (int k = 0; k < VPT; k++) {
@@ -114,7 +113,7 @@ __global__ void __launch_bounds__(ln_threads<WPR>()) ln_modulate_rows_kernel(
       Vec<T>::unpack(ld_param(shv + vi), sh);
       Vec<T>::unpack(ld_param(scv + vi), sc);
 #pragma unroll
-      for (int e = 0; e < N; e++) v[e] = fmaf(fmaf(v[e], rstd, neg_mu_rstd), 1.0f + sc[e], sh[e]);
+      for (int e = 0; e < N; e++) v[e] = fmaf((v[e] - mu) * rstd, 1.0f + sc[e], sh[e]);
       st_stream(orow + vi, Vec<T>::pack(v));
     }
   }
@@ -154,7 +153,6 @@ __global__ void __launch_bounds__(1024) ln_modulate_long_row_kernel(
     }
   }
   const float rstd = 1.0f / sqrtf(__fdiv_rn(block_sum(dev, scratch_var), hidden_f) + eps);
-  const float neg_mu_rstd = -mu * rstd;
   // out may alias x: each thread overwrites only vectors it has finished reading.
   for (int64_t vi = threadIdx.x; vi < nvec; vi += blockDim.x) {
     float v[N], sh[N], sc[N];
@@ -162,7 +160,7 @@ __global__ void __launch_bounds__(1024) ln_modulate_long_row_kernel(
     Vec<T>::unpack(ld_param(shv + vi), sh);
     Vec<T>::unpack(ld_param(scv + vi), sc);
 #pragma unroll
-    for (int e = 0; e < N; e++) v[e] = fmaf(fmaf(v[e], rstd, neg_mu_rstd), 1.0f + sc[e], sh[e]);
+    for (int e = 0; e < N; e++) v[e] = fmaf((v[e] - mu) * rstd, 1.0f + sc[e], sh[e]);
     st_stream(orow + vi, Vec<T>::pack(v));
   }
 }

@@ -65,6 +65,41 @@ __device__ __forceinline__ void st_plain(void* p, uint4 v) {
 }
 
 // ---------------------------------------------------------------------------
+// Asynchronous global -> shared copies (cp.async).  Each thread copies its own
+// vectors and waits for its own copy groups; the data is then visible to that
+// thread (no other thread reads it), so no barrier is involved.  The wait is
+// a hardware wait on the thread's outstanding groups, not a spin loop.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ unsigned smem_addr(const void* p) {
+  return static_cast<unsigned>(__cvta_generic_to_shared(p));
+}
+
+// 16 bytes, L1 bypassed, ask L2 for the whole 256-byte sector group.
+__device__ __forceinline__ void cp_async16(unsigned dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global.L2::256B [%0], [%1], 16;" ::"r"(dst), "l"(src)
+               : "memory");
+}
+
+// 4 bytes (through L1: small, shared by many threads).
+__device__ __forceinline__ void cp_async4(unsigned dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+// Wait until at most `pending` of this thread's committed groups are still in flight.
+template <int pending>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(pending) : "memory");
+}
+
+__device__ __forceinline__ uint4 lds128(const void* p) {
+  return *reinterpret_cast<const uint4*>(p);
+}
+
+// ---------------------------------------------------------------------------
 // Element types: a 128-bit vector holds VEC values of T.
 // ---------------------------------------------------------------------------
 template <typename T>

@@ -65,18 +65,42 @@ struct QkArgs {
 
 // T: storage dtype of q/k; WT: weight dtype; L: lanes per head row
 // (head_dim = 2 * L * N with N = 128-bit vector width in elements);
-// R: iterations kept in flight per warp.
-template <typename T, typename WT, int L, int R>
+// RING: iterations kept in flight per warp (shared-memory ring slots).
+template <typename T, int L>
+struct QkSmem {
+  static constexpr int N = Vec<T>::N;
+  static constexpr int HALF = L * N;
+  static constexpr int D = 2 * HALF;
+  // per warp: RING slots x 32 lanes x (a, b) vectors, positions, one angle table
+  static constexpr size_t per_warp(int ring) {
+    return static_cast<size_t>(ring) * kWarp * (2 * sizeof(uint4) + sizeof(int)) +
+           HALF * sizeof(float2);
+  }
+  static constexpr size_t bytes(int ring) {
+    return kQkWarps * per_warp(ring) + 2 * D * sizeof(float) +
+           HALF * sizeof(unsigned long long);
+  }
+};
+
+template <typename T, typename WT, int L, int RING>
 __global__ void __launch_bounds__(kQkThreads) qk_norm_rope_kernel(const QkArgs a,
                                                                   const RopeTurns turns) {
-  constexpr int N = Vec<T>::N;
-  constexpr int HALF = L * N;
-  constexpr int D = 2 * HALF;
+  using S = QkSmem<T, L>;
+  constexpr int N = S::N;
+  constexpr int HALF = S::HALF;
+  constexpr int D = S::D;
   constexpr int GW = kWarp / L;  // head rows per warp iteration
 
-  __shared__ __align__(16) float wsm[2 * D];              // q weights, k weights (+ gemma 1)
-  __shared__ __align__(16) float2 trig[kQkWarps][HALF];   // per-warp (cos, sin) of one token
-  __shared__ unsigned long long turn_sm[HALF];              // the rotary turn constants
+  extern __shared__ __align__(16) unsigned char smem[];
+  const int warp = threadIdx.x / kWarp;
+  const int lane32 = threadIdx.x % kWarp;
+  unsigned char* wbase = smem + warp * S::per_warp(RING);
+  uint4* ring_a = reinterpret_cast<uint4*>(wbase);                  // [RING][32]
+  uint4* ring_b = ring_a + RING * kWarp;                            // [RING][32]
+  int* ring_pos = reinterpret_cast<int*>(ring_b + RING * kWarp);    // [RING][32]
+  float2* trig = reinterpret_cast<float2*>(ring_pos + RING * kWarp);  // [HALF]
+  float* wsm = reinterpret_cast<float*>(smem + kQkWarps * S::per_warp(RING));  // [2D]
+  unsigned long long* turn_sm = reinterpret_cast<unsigned long long*>(wsm + 2 * D);
 
   const WT* wq = static_cast<const WT*>(a.wq);
   const WT* wk = static_cast<const WT*>(a.wk);
@@ -91,8 +115,6 @@ __global__ void __launch_bounds__(kQkThreads) qk_norm_rope_kernel(const QkArgs a
   for (int i = threadIdx.x; i < HALF; i += kQkThreads) turn_sm[i] = turns.turn[i];
   __syncthreads();  // the only block-level barrier
 
-  const int warp = threadIdx.x / kWarp;
-  const int lane32 = threadIdx.x % kWarp;
   const int g = lane32 / L;  // head row within the iteration
   const int l = lane32 % L;  // vector slot within each half of the row
   const int64_t gw = static_cast<int64_t>(blockIdx.x) * kQkWarps + warp;
@@ -102,8 +124,8 @@ __global__ void __launch_bounds__(kQkThreads) qk_norm_rope_kernel(const QkArgs a
   const int IT = (H + GW - 1) / GW;  // iterations per token
 
   // A cursor walks this warp's iterations: token gw, gw + W, ... and, within
-  // a token, iterations 0 .. IT-1 (rows it*GW .. it*GW + GW-1).  The load
-  // cursor runs R iterations ahead of the compute cursor.
+  // a token, iterations 0 .. IT-1 (rows it*GW .. it*GW + GW-1).  The copy
+  // cursor runs RING iterations ahead of the compute cursor.
   struct Cursor {
     int64_t tok;
     int it;
@@ -114,109 +136,109 @@ __global__ void __launch_bounds__(kQkThreads) qk_norm_rope_kernel(const QkArgs a
       c.tok += W;
     }
   };
-  // Where this lane's row of the cursor's iteration lives (false: no row).
-  auto locate = [&](const Cursor& c, const uint4*& src, uint4*& dst) -> bool {
+  // Element offset of this lane's row of the cursor's iteration, and whether
+  // it is a Q row; false when the iteration has no row for this lane.
+  auto locate = [&](const Cursor& c, int64_t& off, bool& is_q) -> bool {
     const int row = c.it * GW + g;
     if (row >= H) return false;
-    if (row < a.hq) {
-      const int64_t off = c.tok * a.q_stride + static_cast<int64_t>(row) * D;
-      src = reinterpret_cast<const uint4*>(static_cast<const T*>(a.q) + off);
-      dst = reinterpret_cast<uint4*>(static_cast<T*>(a.q_out) + off);
-    } else {
-      const int64_t off = c.tok * a.k_stride + static_cast<int64_t>(row - a.hq) * D;
-      src = reinterpret_cast<const uint4*>(static_cast<const T*>(a.k) + off);
-      dst = reinterpret_cast<uint4*>(static_cast<T*>(a.k_out) + off);
-    }
+    is_q = row < a.hq;
+    off = is_q ? c.tok * a.q_stride + static_cast<int64_t>(row) * D
+               : c.tok * a.k_stride + static_cast<int64_t>(row - a.hq) * D;
     return true;
   };
 
-  uint4 va[R], vb[R];
-  int pos_at[R];  // position of the slot's token (loaded with its first iteration)
-  Cursor ld{gw, 0}, cc{gw, 0};
+  Cursor cp{gw, 0}, cc{gw, 0};
+  // Start the copies of the copy cursor's iteration into `slot`, one group.
   auto issue = [&](int slot) {
-    const uint4* src;
-    uint4* dst;
-    if (locate(ld, src, dst)) {
-      va[slot] = ld_stream(src + l);
-      vb[slot] = ld_stream(src + L + l);
+    if (cp.tok < a.tokens) {
+      int64_t off;
+      bool is_q;
+      if (locate(cp, off, is_q)) {
+        const T* src = static_cast<const T*>(is_q ? a.q : a.k) + off;
+        const uint4* v = reinterpret_cast<const uint4*>(src);
+        cp_async16(smem_addr(ring_a + slot * kWarp + lane32), v + l);
+        cp_async16(smem_addr(ring_b + slot * kWarp + lane32), v + L + l);
+      }
+      if (cp.it == 0) cp_async4(smem_addr(ring_pos + slot * kWarp + lane32), a.pos + cp.tok);
+      advance(cp);
     }
-    if (ld.it == 0) pos_at[slot] = __ldg(a.pos + ld.tok);
-    advance(ld);
+    cp_async_commit();  // possibly empty: keeps one group per iteration
   };
 
-#pragma unroll
-  for (int s = 0; s < R; s++)
-    if (ld.tok < a.tokens) issue(s);
+  for (int s = 0; s < RING; s++) issue(s);
 
   float2 cs[N];  // (cos, sin) of this lane's pairs for the current token
+  int slot = 0;
   while (cc.tok < a.tokens) {
+    cp_async_wait<RING - 1>();  // this iteration's group has landed
+    int64_t off;
+    bool is_q;
+    const bool valid = locate(cc, off, is_q);
+    if (cc.it == 0) {
+      // New token: its angles, once per warp, then this lane's N pairs.
+      const unsigned long long p = static_cast<unsigned long long>(
+          static_cast<long long>(ring_pos[slot * kWarp + lane32]));
+      __syncwarp();
+      for (int i = lane32; i < HALF; i += kWarp) {
+        const unsigned long long prod = p * turn_sm[i];  // angle, in turns, mod 1
+        const int hi = static_cast<int>(prod >> 32);      // signed turn fraction * 2^32
+        float sn, cn;
+        sincospif(static_cast<float>(hi) * 0x1p-31f, &sn, &cn);  // angle = pi * hi / 2^31
+        trig[i] = make_float2(cn, sn);
+      }
+      __syncwarp();
 #pragma unroll
-    for (int s = 0; s < R; s++) {
-      if (cc.tok < a.tokens) {
-        const uint4* src;
-        uint4* dst;
-        const bool valid = locate(cc, src, dst);
-        if (cc.it == 0) {
-          // New token: its angles, once per warp, then this lane's N pairs.
-          const unsigned long long p = static_cast<unsigned long long>(
-              static_cast<long long>(pos_at[s]));
-          __syncwarp();
-          for (int i = lane32; i < HALF; i += kWarp) {
-            const unsigned long long prod = p * turn_sm[i];  // angle, in turns, mod 1
-            const int hi = static_cast<int>(prod >> 32);      // signed turn fraction * 2^32
-            float sn, cn;
-            sincospif(static_cast<float>(hi) * 0x1p-31f, &sn, &cn);  // angle = pi * hi / 2^31
-            trig[warp][i] = make_float2(cn, sn);
-          }
-          __syncwarp();
+      for (int e = 0; e < N; e++) cs[e] = trig[l * N + e];
+    }
+    float xa[N], xb[N];
+    float ss = 0.0f;
+    if (valid) {
+      Vec<T>::unpack(lds128(ring_a + slot * kWarp + lane32), xa);
+      Vec<T>::unpack(lds128(ring_b + slot * kWarp + lane32), xb);
 #pragma unroll
-          for (int e = 0; e < N; e++) cs[e] = trig[warp][l * N + e];
-        }
-        float xa[N], xb[N];
-        float ss = 0.0f;
-        if (valid) {
-          Vec<T>::unpack(va[s], xa);
-          Vec<T>::unpack(vb[s], xb);
-#pragma unroll
-          for (int e = 0; e < N; e++) {
-            ss = fmaf(xa[e], xa[e], ss);
-            ss = fmaf(xb[e], xb[e], ss);
-          }
-        }
-        // The slot is free again: start the load R iterations ahead.
-        if (ld.tok < a.tokens) issue(s);
-        // Every lane joins the butterfly (full-warp shuffles), valid or not.
-        ss = group_sum<L>(ss);
-        if (valid) {
-          const int row = cc.it * GW + g;
-          const float inv = rsqrtf(ss * a.inv_d + a.eps);
-          const float* w = wsm + (row < a.hq ? 0 : D) + l * N;
-          float oa[N], ob[N];
-#pragma unroll
-          for (int e = 0; e < N; e++) {
-            const float na = xa[e] * inv * w[e];
-            const float nb = xb[e] * inv * w[HALF + e];
-            oa[e] = fmaf(na, cs[e].x, -nb * cs[e].y);
-            ob[e] = fmaf(na, cs[e].y, nb * cs[e].x);
-          }
-          st_stream(dst + l, Vec<T>::pack(oa));
-          st_stream(dst + L + l, Vec<T>::pack(ob));
-        }
-        advance(cc);
+      for (int e = 0; e < N; e++) {
+        ss = fmaf(xa[e], xa[e], ss);
+        ss = fmaf(xb[e], xb[e], ss);
       }
     }
+    // The slot's data is in registers: refill it RING iterations ahead.
+    issue(slot);
+    // Every lane joins the butterfly (full-warp shuffles), valid or not.
+    ss = group_sum<L>(ss);
+    if (valid) {
+      const float inv = rsqrtf(ss * a.inv_d + a.eps);
+      const float* w = wsm + (is_q ? 0 : D) + l * N;
+      float oa[N], ob[N];
+#pragma unroll
+      for (int e = 0; e < N; e++) {
+        const float na = xa[e] * inv * w[e];
+        const float nb = xb[e] * inv * w[HALF + e];
+        oa[e] = fmaf(na, cs[e].x, -nb * cs[e].y);
+        ob[e] = fmaf(na, cs[e].y, nb * cs[e].x);
+      }
+      uint4* dst = reinterpret_cast<uint4*>(static_cast<T*>(is_q ? a.q_out : a.k_out) + off);
+      st_stream(dst + l, Vec<T>::pack(oa));
+      st_stream(dst + L + l, Vec<T>::pack(ob));
+    }
+    advance(cc);
+    slot = slot + 1 == RING ? 0 : slot + 1;
   }
+  cp_async_wait<0>();  // nothing may land after the block's shared memory is released
 }
 
-// Resident blocks per SM of one kernel instantiation, cached per device.
-template <typename T, typename WT, int L, int R>
+// Resident blocks per SM of one kernel instantiation (with its dynamic shared
+// memory), cached per device; also raises the kernel's shared-memory limit.
+template <typename T, typename WT, int L, int RING>
 int blocks_per_sm(int device) {
   static int cached[64] = {0};
   if (device < 0 || device >= 64) return 1;
   if (cached[device] == 0) {
+    const size_t smem = QkSmem<T, L>::bytes(RING);
+    cudaFuncSetAttribute(qk_norm_rope_kernel<T, WT, L, RING>,
+                         cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, qk_norm_rope_kernel<T, WT, L, R>,
-                                                      kQkThreads, 0) != cudaSuccess ||
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, qk_norm_rope_kernel<T, WT, L, RING>,
+                                                      kQkThreads, smem) != cudaSuccess ||
         n < 1)
       n = 1;
     cached[device] = n;
@@ -238,16 +260,16 @@ int sm_count(int device) {
 
 template <typename T, typename WT, int L>
 cudaError_t launch_l(const QkArgs& a, const RopeTurns& turns, cudaStream_t s) {
-  constexpr int R = (L >= 16) ? 4 : 6;
+  constexpr int RING = 8;
   int device = 0;
   cudaError_t e = cudaGetDevice(&device);
   if (e != cudaSuccess) return e;
   const int64_t resident =
-      static_cast<int64_t>(sm_count(device)) * blocks_per_sm<T, WT, L, R>(device);
+      static_cast<int64_t>(sm_count(device)) * blocks_per_sm<T, WT, L, RING>(device);
   const int64_t needed = (a.tokens + kQkWarps - 1) / kQkWarps;  // one warp per token at most
   const int64_t blocks = needed < resident ? needed : resident;
-  qk_norm_rope_kernel<T, WT, L, R><<<dim3(static_cast<unsigned>(blocks)), kQkThreads, 0, s>>>(
-      a, turns);
+  qk_norm_rope_kernel<T, WT, L, RING>
+      <<<dim3(static_cast<unsigned>(blocks)), kQkThreads, QkSmem<T, L>::bytes(RING), s>>>(a, turns);
   return cudaGetLastError();
 }
 

@@ -31,6 +31,11 @@
 namespace nr {
 namespace {
 
+// Iterations in flight per warp (shared-memory ring slots); a build-time knob.
+#ifndef NR_QK_RING
+#define NR_QK_RING 8
+#endif
+
 constexpr int kQkThreads = 128;
 constexpr int kQkWarps = kQkThreads / kWarp;
 
@@ -260,7 +265,7 @@ int sm_count(int device) {
 
 template <typename T, typename WT, int L>
 cudaError_t launch_l(const QkArgs& a, const RopeTurns& turns, cudaStream_t s) {
-  constexpr int RING = 8;
+  constexpr int RING = NR_QK_RING;
   int device = 0;
   cudaError_t e = cudaGetDevice(&device);
   if (e != cudaSuccess) return e;

@@ -7,16 +7,16 @@
 //   out = round((x - mu) / sqrt(var + eps) * (1 + scale) + shift)
 // with shift/scale taken from sample row r / rows_per_sample.
 //
-// Design.  Rows of up to 512 vectors (hidden 4096 bf16; the benchmark's 3072
-// is 384 vectors = 12 per lane) belong to one warp, persistently: warp w of W
-// takes rows w, w + W, ... and streams them through a per-warp shared-memory
-// ring with cp.async, so the next RING rows are in flight while one is
-// computed.  The row is read once (into the ring, then registers), the mean
-// and the centred variance are warp-shuffle reductions over the registers,
-// and the output is written once.  Longer rows belong to a group of 2, 4 or 8
-// warps (one shared-memory step in each reduction); rows beyond 16 vectors
-// per thread at 8 warps use a three-pass kernel that re-reads the
-// (L2-resident) row.
+// Design.  A row belongs to a group of WPR warps: one warp for rows of up to
+// 512 vectors (hidden 4096 bf16; the benchmark's 3072 is 384 vectors = 12 per
+// lane), else 2, 4 or 8 warps; a block of 128 threads holds 4 / WPR groups (a
+// row of 8 warps is its own block).  The row is loaded once into registers,
+// the mean and the centred variance are two reductions over the
+// register-resident values (warp shuffles; one shared-memory step only when
+// WPR > 1), and the output is written once.  Rows beyond 16 vectors per
+// thread at 8 warps use a three-pass kernel that re-reads the (L2-resident)
+// row.  (A persistent variant streaming rows through a cp.async ring was
+// measured slower here: it trades resident warps for ring depth.)
 #include "nr_common.cuh"
 #include "nr_internal.h"
 
@@ -122,105 +122,94 @@ __global__ void __launch_bounds__(ln_threads<WPR>()) ln_modulate_rows_kernel(
   }
 }
 
-// Rows in flight per warp for rows of more than 4 vectors per lane; a
-// build-time knob.
-#ifndef NR_LN_RING
-#define NR_LN_RING 2
+// One modulation sample for all rows, rows of one warp: each block first
+// stages (1 + scale) and shift for the whole row as f32 in shared memory, so
+// the output step is two shared loads and one fma per element instead of two
+// unpacks, an add and an fma.  x is already in flight while the block stages.
+#ifndef NR_LN_STAGED
+#define NR_LN_STAGED 1
 #endif
+constexpr int kLnStagedThreads = 128;
 
-constexpr int kLnRingThreads = 128;
-constexpr int kLnRingWarps = kLnRingThreads / kWarp;
-
-// Shared memory of the ring kernel: per warp RING rows of VPT x 32 vectors.
-template <int VPT, int RING>
-constexpr size_t ln_ring_smem() {
-  return static_cast<size_t>(kLnRingWarps) * RING * VPT * kWarp * sizeof(uint4);
-}
-
-template <typename T, int VPT, int RING>
-__global__ void __launch_bounds__(kLnRingThreads) ln_modulate_ring_kernel(
+template <typename T, int VPT>
+__global__ void __launch_bounds__(kLnStagedThreads, VPT <= 12 ? 6 : 4) ln_modulate_staged_kernel(
     T* __restrict__ out, const T* __restrict__ x, const T* __restrict__ shift,
-    const T* __restrict__ scale, int64_t rows, int nvec, int64_t rows_per_sample, float hidden_f,
-    float eps) {
+    const T* __restrict__ scale, int64_t rows, int nvec, float hidden_f, float eps) {
   constexpr int N = Vec<T>::N;
-  extern __shared__ __align__(16) unsigned char smem[];
-  const int warp = threadIdx.x / kWarp;
+  extern __shared__ __align__(16) float params[];  // [nvec * N] (1 + scale), then [nvec * N] shift
+  float* gain = params;
+  float* bias = params + nvec * N;
   const int lane = threadIdx.x % kWarp;
-  uint4* ring = reinterpret_cast<uint4*>(smem) + warp * RING * VPT * kWarp;  // [RING][VPT][32]
-  const int64_t W = static_cast<int64_t>(gridDim.x) * kLnRingWarps;
-  const int64_t first = static_cast<int64_t>(blockIdx.x) * kLnRingWarps + warp;
-  if (first >= rows) return;
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * (kLnStagedThreads / kWarp) +
+                      threadIdx.x / kWarp;
+  const bool active = row < rows;
+  const uint4* xr = reinterpret_cast<const uint4*>(x) + (active ? row : 0) * nvec;
 
-  int64_t next = first;  // next row to copy
-  auto issue = [&](int slot) {
-    if (next < rows) {
-      const uint4* xr = reinterpret_cast<const uint4*>(x) + next * nvec;
+  uint4 xv[VPT];
 #pragma unroll
-      for (int k = 0; k < VPT; k++) {
-        const int vi = lane + k * kWarp;
-        if (vi < nvec) cp_async16(smem_addr(ring + (slot * VPT + k) * kWarp + lane), xr + vi);
-      }
-      next += W;
-    }
-    cp_async_commit();  // possibly empty: one group per ring slot use
-  };
-  for (int s = 0; s < RING; s++) issue(s);
-
-  int slot = 0;
-  for (int64_t row = first; row < rows; row += W) {
-    cp_async_wait<RING - 1>();  // this row's copies have landed
-    uint4 xv[VPT];
-#pragma unroll
-    for (int k = 0; k < VPT; k++)
-      if (lane + k * kWarp < nvec) xv[k] = lds128(ring + (slot * VPT + k) * kWarp + lane);
-    issue(slot);  // the slot is in registers: refill it RING rows ahead
-
-    float sum = 0.0f;
-#pragma unroll
-    for (int k = 0; k < VPT; k++) {
-      if (lane + k * kWarp < nvec) {
-        float v[N];
-        Vec<T>::unpack(xv[k], v);
-#pragma unroll
-        for (int e = 0; e < N; e++) sum += v[e];
-      }
-    }
-    const float mu = __fdiv_rn(group_sum<kWarp>(sum), hidden_f);
-    float dev = 0.0f;
-#pragma unroll
-    for (int k = 0; k < VPT; k++) {
-      if (lane + k * kWarp < nvec) {
-        float v[N];
-        Vec<T>::unpack(xv[k], v);
-#pragma unroll
-        for (int e = 0; e < N; e++) {
-          const float d = v[e] - mu;
-          dev = fmaf(d, d, dev);
-        }
-      }
-    }
-    const float rstd = 1.0f / sqrtf(__fdiv_rn(group_sum<kWarp>(dev), hidden_f) + eps);
-
-    const int64_t sample_off = (row / rows_per_sample) * nvec;
-    const uint4* shv = reinterpret_cast<const uint4*>(shift) + sample_off;
-    const uint4* scv = reinterpret_cast<const uint4*>(scale) + sample_off;
-    uint4* orow = reinterpret_cast<uint4*>(out) + row * nvec;
-#pragma unroll
-    for (int k = 0; k < VPT; k++) {
-      const int vi = lane + k * kWarp;
-      if (vi < nvec) {
-        float v[N], sh[N], sc[N];
-        Vec<T>::unpack(xv[k], v);
-        Vec<T>::unpack(ld_param(shv + vi), sh);
-        Vec<T>::unpack(ld_param(scv + vi), sc);
-#pragma unroll
-        for (int e = 0; e < N; e++) v[e] = fmaf((v[e] - mu) * rstd, 1.0f + sc[e], sh[e]);
-        st_stream(orow + vi, Vec<T>::pack(v));
-      }
-    }
-    slot = slot + 1 == RING ? 0 : slot + 1;
+  for (int k = 0; k < VPT; k++) {
+    const int vi = lane + k * kWarp;
+    if (active && vi < nvec) xv[k] = ld_stream(xr + vi);
   }
-  cp_async_wait<0>();
+  for (int vi = threadIdx.x; vi < nvec; vi += kLnStagedThreads) {
+    float sc[N], sh[N];
+    Vec<T>::unpack(ld_param(reinterpret_cast<const uint4*>(scale) + vi), sc);
+    Vec<T>::unpack(ld_param(reinterpret_cast<const uint4*>(shift) + vi), sh);
+#pragma unroll
+    for (int e = 0; e < N; e += 4) {
+      *reinterpret_cast<float4*>(gain + vi * N + e) =
+          make_float4(1.0f + sc[e], 1.0f + sc[e + 1], 1.0f + sc[e + 2], 1.0f + sc[e + 3]);
+      *reinterpret_cast<float4*>(bias + vi * N + e) =
+          make_float4(sh[e], sh[e + 1], sh[e + 2], sh[e + 3]);
+    }
+  }
+  __syncthreads();
+  if (!active) return;
+
+  float sum = 0.0f;
+#pragma unroll
+  for (int k = 0; k < VPT; k++) {
+    if (lane + k * kWarp < nvec) {
+      float v[N];
+      Vec<T>::unpack(xv[k], v);
+#pragma unroll
+      for (int e = 0; e < N; e++) sum += v[e];
+    }
+  }
+  const float mu = __fdiv_rn(group_sum<kWarp>(sum), hidden_f);
+  float dev = 0.0f;
+#pragma unroll
+  for (int k = 0; k < VPT; k++) {
+    if (lane + k * kWarp < nvec) {
+      float v[N];
+      Vec<T>::unpack(xv[k], v);
+#pragma unroll
+      for (int e = 0; e < N; e++) {
+        const float d = v[e] - mu;
+        dev = fmaf(d, d, dev);
+      }
+    }
+  }
+  const float rstd = 1.0f / sqrtf(__fdiv_rn(group_sum<kWarp>(dev), hidden_f) + eps);
+  uint4* orow = reinterpret_cast<uint4*>(out) + row * nvec;
+#pragma unroll
+  for (int k = 0; k < VPT; k++) {
+    const int vi = lane + k * kWarp;
+    if (vi < nvec) {
+      float v[N];
+      Vec<T>::unpack(xv[k], v);
+#pragma unroll
+      for (int e = 0; e < N; e += 4) {
+        const float4 gq = *reinterpret_cast<const float4*>(gain + vi * N + e);
+        const float4 bq = *reinterpret_cast<const float4*>(bias + vi * N + e);
+        v[e] = fmaf((v[e] - mu) * rstd, gq.x, bq.x);
+        v[e + 1] = fmaf((v[e + 1] - mu) * rstd, gq.y, bq.y);
+        v[e + 2] = fmaf((v[e + 2] - mu) * rstd, gq.z, bq.z);
+        v[e + 3] = fmaf((v[e + 3] - mu) * rstd, gq.w, bq.w);
+      }
+      st_stream(orow + vi, Vec<T>::pack(v));
+    }
+  }
 }
 
 template <typename T>
@@ -281,56 +270,31 @@ struct LnArgs {
   float eps;
 };
 
+template <typename T, int VPT>
+cudaError_t launch_staged(const LnArgs& a, cudaStream_t s) {
+  constexpr int RPB = kLnStagedThreads / kWarp;
+  const int64_t blocks = (a.rows + RPB - 1) / RPB;
+  const size_t smem = 2 * static_cast<size_t>(a.nvec) * Vec<T>::N * sizeof(float);
+  ln_modulate_staged_kernel<T, VPT><<<dim3(static_cast<unsigned>(blocks)), kLnStagedThreads,
+                                      smem, s>>>(
+      static_cast<T*>(a.out), static_cast<const T*>(a.x), static_cast<const T*>(a.shift),
+      static_cast<const T*>(a.scale), a.rows, a.nvec, a.hidden_f, a.eps);
+  return cudaGetLastError();
+}
+
 template <typename T, int VPT, int WPR>
 cudaError_t launch_rows(const LnArgs& a, cudaStream_t s) {
+  if constexpr (WPR == 1 && NR_LN_STAGED) {
+    // One sample for every row and the staged parameters fit the default
+    // 48 KB of shared memory (always true for one-warp rows).
+    if (a.rps >= a.rows && 2 * static_cast<size_t>(a.nvec) * Vec<T>::N * sizeof(float) <= 48 * 1024)
+      return launch_staged<T, VPT>(a, s);
+  }
   constexpr int THREADS = ln_threads<WPR>();
   constexpr int RPB = THREADS / (kWarp * WPR);
   static_assert(RPB >= 1, "row groups must fit the block");
   const int64_t blocks = (a.rows + RPB - 1) / RPB;
   ln_modulate_rows_kernel<T, VPT, WPR><<<dim3(static_cast<unsigned>(blocks)), THREADS, 0, s>>>(
-      static_cast<T*>(a.out), static_cast<const T*>(a.x), static_cast<const T*>(a.shift),
-      static_cast<const T*>(a.scale), a.rows, a.nvec, a.rps, a.hidden_f, a.eps);
-  return cudaGetLastError();
-}
-
-int ln_sm_count(int device) {
-  static int cached[64] = {0};
-  if (device < 0 || device >= 64) return 1;
-  if (cached[device] == 0) {
-    int n = 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, device) != cudaSuccess || n < 1)
-      n = 1;
-    cached[device] = n;
-  }
-  return cached[device];
-}
-
-// Persistent grid for the ring kernel: as many blocks as fit on the GPU (or
-// one warp per row when there are fewer rows).
-template <typename T, int VPT>
-cudaError_t launch_ring(const LnArgs& a, cudaStream_t s) {
-  constexpr int RING = VPT <= 4 ? 4 : NR_LN_RING;
-  constexpr size_t smem = ln_ring_smem<VPT, RING>();
-  static int resident_per_sm[64] = {0};
-  int device = 0;
-  cudaError_t e = cudaGetDevice(&device);
-  if (e != cudaSuccess) return e;
-  if (device < 0 || device >= 64) device = 0;
-  if (resident_per_sm[device] == 0) {
-    cudaFuncSetAttribute(ln_modulate_ring_kernel<T, VPT, RING>,
-                         cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, ln_modulate_ring_kernel<T, VPT, RING>,
-                                                      kLnRingThreads, smem) != cudaSuccess ||
-        n < 1)
-      n = 1;
-    resident_per_sm[device] = n;
-  }
-  const int64_t resident = static_cast<int64_t>(ln_sm_count(device)) * resident_per_sm[device];
-  const int64_t needed = (a.rows + kLnRingWarps - 1) / kLnRingWarps;
-  const int64_t blocks = needed < resident ? needed : resident;
-  ln_modulate_ring_kernel<T, VPT, RING><<<dim3(static_cast<unsigned>(blocks)), kLnRingThreads,
-                                          smem, s>>>(
       static_cast<T*>(a.out), static_cast<const T*>(a.x), static_cast<const T*>(a.shift),
       static_cast<const T*>(a.scale), a.rows, a.nvec, a.rps, a.hidden_f, a.eps);
   return cudaGetLastError();
@@ -356,15 +320,15 @@ cudaError_t launch_typed(const LnArgs& a, cudaStream_t s) {
         if (vpt == 0 && v >= need) vpt = v;
     }
     switch (wpr * 100 + vpt) {
-      case 101: return launch_ring<T, 1>(a, s);
-      case 102: return launch_ring<T, 2>(a, s);
-      case 103: return launch_ring<T, 3>(a, s);
-      case 104: return launch_ring<T, 4>(a, s);
-      case 106: return launch_ring<T, 6>(a, s);
-      case 108: return launch_ring<T, 8>(a, s);
-      case 110: return launch_ring<T, 10>(a, s);
-      case 112: return launch_ring<T, 12>(a, s);
-      case 116: return launch_ring<T, 16>(a, s);
+      case 101: return launch_rows<T, 1, 1>(a, s);
+      case 102: return launch_rows<T, 2, 1>(a, s);
+      case 103: return launch_rows<T, 3, 1>(a, s);
+      case 104: return launch_rows<T, 4, 1>(a, s);
+      case 106: return launch_rows<T, 6, 1>(a, s);
+      case 108: return launch_rows<T, 8, 1>(a, s);
+      case 110: return launch_rows<T, 10, 1>(a, s);
+      case 112: return launch_rows<T, 12, 1>(a, s);
+      case 116: return launch_rows<T, 16, 1>(a, s);
       case 208: return launch_rows<T, 8, 2>(a, s);
       case 212: return launch_rows<T, 12, 2>(a, s);
       case 216: return launch_rows<T, 16, 2>(a, s);

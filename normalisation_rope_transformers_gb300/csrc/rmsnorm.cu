@@ -90,119 +90,6 @@ __global__ void __launch_bounds__(kRowMaxThreads) rmsnorm_row_kernel(T* __restri
   }
 }
 
-// Rows in flight per block for the persistent ring kernel; a build-time knob.
-#ifndef NR_RMS_RING
-#define NR_RMS_RING 2
-#endif
-
-// Persistent variant for many rows: block b takes rows b, b + G, ...  Each
-// thread streams its own vectors of x (and of the residual) through a
-// RING-deep shared-memory ring with cp.async, so the next rows are in flight
-// while one is reduced; the weight stays in registers for all rows.  One
-// barrier per row: the cross-warp partial sums alternate between two buffers.
-template <typename T, int VPT, bool RES, int RING>
-__global__ void __launch_bounds__(kRowMaxThreads) rmsnorm_ring_kernel(
-    T* __restrict__ out, const T* __restrict__ x, const T* __restrict__ w, T* __restrict__ res,
-    int64_t rows, int nvec, float hidden_f, float eps, float w_add) {
-  constexpr int N = Vec<T>::N;
-  constexpr int NBUF = RES ? 2 : 1;
-  extern __shared__ __align__(16) unsigned char smem[];
-  uint4* ring = reinterpret_cast<uint4*>(smem);  // [RING][NBUF][VPT][blockDim]
-  __shared__ float partial[2][kRowMaxThreads / kWarp];
-  const int tid = threadIdx.x;
-  const int nthreads = blockDim.x;
-  const int nwarps = (nthreads + kWarp - 1) / kWarp;
-  const int64_t G = gridDim.x;
-  auto slot_ptr = [&](int slot, int buf, int k) {
-    return ring + ((slot * NBUF + buf) * VPT + k) * nthreads + tid;
-  };
-
-  uint4 wpk[VPT];  // the weight, packed, for all of this block's rows
-#pragma unroll
-  for (int k = 0; k < VPT; k++) {
-    const int vi = tid + k * nthreads;
-    if (vi < nvec) wpk[k] = ld_param(reinterpret_cast<const uint4*>(w) + vi);
-  }
-
-  int64_t next = blockIdx.x;
-  auto issue = [&](int slot) {
-    if (next < rows) {
-      const uint4* xr = reinterpret_cast<const uint4*>(x) + next * nvec;
-      const uint4* rr = RES ? reinterpret_cast<const uint4*>(res) + next * nvec : nullptr;
-#pragma unroll
-      for (int k = 0; k < VPT; k++) {
-        const int vi = tid + k * nthreads;
-        if (vi < nvec) {
-          cp_async16(smem_addr(slot_ptr(slot, 0, k)), xr + vi);
-          if (RES) cp_async16(smem_addr(slot_ptr(slot, NBUF - 1, k)), rr + vi);
-        }
-      }
-      next += G;
-    }
-    cp_async_commit();
-  };
-  for (int s = 0; s < RING; s++) issue(s);
-
-  int slot = 0, parity = 0;
-  for (int64_t row = blockIdx.x; row < rows; row += G) {
-    cp_async_wait<RING - 1>();
-    uint4 xv[VPT], rv[VPT];
-#pragma unroll
-    for (int k = 0; k < VPT; k++) {
-      if (tid + k * nthreads < nvec) {
-        xv[k] = lds128(slot_ptr(slot, 0, k));
-        if (RES) rv[k] = lds128(slot_ptr(slot, NBUF - 1, k));
-      }
-    }
-    issue(slot);  // the slot is in registers: refill it RING rows ahead
-
-    uint4* rrow = RES ? reinterpret_cast<uint4*>(res) + row * nvec : nullptr;
-    float sum_sq = 0.0f;
-#pragma unroll
-    for (int k = 0; k < VPT; k++) {
-      const int vi = tid + k * nthreads;
-      if (vi < nvec) {
-        float v[N];
-        Vec<T>::unpack(xv[k], v);
-        if (RES) {
-          float r[N];
-          Vec<T>::unpack(rv[k], r);
-#pragma unroll
-          for (int e = 0; e < N; e++) v[e] += r[e];
-          xv[k] = Vec<T>::pack(v);  // rounded once to the residual's dtype
-          st_stream(rrow + vi, xv[k]);
-          Vec<T>::unpack(xv[k], v);
-        }
-#pragma unroll
-        for (int e = 0; e < N; e++) sum_sq = fmaf(v[e], v[e], sum_sq);
-      }
-    }
-    sum_sq = group_sum<kWarp>(sum_sq);
-    if (tid % kWarp == 0) partial[parity][tid / kWarp] = sum_sq;
-    __syncthreads();
-    float total = 0.0f;
-    for (int i = 0; i < nwarps; i++) total += partial[parity][i];
-    const float inv = 1.0f / sqrtf(__fdiv_rn(total, hidden_f) + eps);
-
-    uint4* orow = reinterpret_cast<uint4*>(out) + row * nvec;
-#pragma unroll
-    for (int k = 0; k < VPT; k++) {
-      const int vi = tid + k * nthreads;
-      if (vi < nvec) {
-        float v[N], wf[N];
-        Vec<T>::unpack(xv[k], v);
-        Vec<T>::unpack(wpk[k], wf);
-#pragma unroll
-        for (int e = 0; e < N; e++) v[e] = v[e] * inv * (wf[e] + w_add);
-        st_stream(orow + vi, Vec<T>::pack(v));
-      }
-    }
-    slot = slot + 1 == RING ? 0 : slot + 1;
-    parity ^= 1;
-  }
-  cp_async_wait<0>();
-}
-
 // Rows too long for registers: pass 1 adds, writes the residual and reduces;
 // pass 2 re-reads the stored values (L2-resident) and normalises.
 template <typename T, bool RES>
@@ -267,55 +154,8 @@ cudaError_t launch_rows_pw(const RowLaunch& g, void* out, const void* x, const v
   return cudaGetLastError();
 }
 
-int rms_sm_count(int device) {
-  static int cached[64] = {0};
-  if (device < 0 || device >= 64) return 1;
-  if (cached[device] == 0) {
-    int n = 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, device) != cudaSuccess || n < 1)
-      n = 1;
-    cached[device] = n;
-  }
-  return cached[device];
-}
-
-template <typename T, int VPT, bool RES>
-cudaError_t launch_ring(const RowLaunch& g, void* out, const void* x, const void* w, void* res,
-                        int64_t rows, int nvec, float hidden_f, float eps, float w_add,
-                        cudaStream_t s) {
-  constexpr int RING = NR_RMS_RING;
-  const size_t smem = static_cast<size_t>(RING) * (RES ? 2 : 1) * VPT * g.threads * sizeof(uint4);
-  int device = 0;
-  cudaError_t e = cudaGetDevice(&device);
-  if (e != cudaSuccess) return e;
-  if (device < 0 || device >= 64) device = 0;
-  // Occupancy depends on the block size, so it is cached per (device, threads/32).
-  static int resident_per_sm[64][kRowMaxThreads / kWarp + 1] = {{0}};
-  int& cached = resident_per_sm[device][g.threads / kWarp];
-  if (cached == 0) {
-    cudaFuncSetAttribute(rmsnorm_ring_kernel<T, VPT, RES, RING>,
-                         cudaFuncAttributeMaxDynamicSharedMemorySize, 96 * 1024);
-    int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, rmsnorm_ring_kernel<T, VPT, RES, RING>,
-                                                      g.threads, smem) != cudaSuccess ||
-        n < 1)
-      n = 1;
-    cached = n;
-  }
-  const int64_t resident = static_cast<int64_t>(rms_sm_count(device)) * cached;
-  const int64_t blocks = rows < resident ? rows : resident;
-  rmsnorm_ring_kernel<T, VPT, RES, RING><<<dim3(static_cast<unsigned>(blocks)), g.threads, smem,
-                                           s>>>(
-      static_cast<T*>(out), static_cast<const T*>(x), static_cast<const T*>(w),
-      static_cast<T*>(res), rows, nvec, hidden_f, eps, w_add);
-  return cudaGetLastError();
-}
-
-// Rows per launch up to which the weight is fetched together with the row;
-// beyond this the persistent ring kernel runs.
+// Rows per launch up to which the weight is fetched together with the row.
 constexpr int64_t kPrefetchWeightRows = 1024;
-// Ring slots above this many bytes per block fall back to the row kernel.
-constexpr size_t kRingMaxSmem = 96 * 1024;
 
 template <typename T, int VPT>
 cudaError_t launch_rows(const RowLaunch& g, void* out, const void* x, const void* w, void* res,
@@ -323,15 +163,6 @@ cudaError_t launch_rows(const RowLaunch& g, void* out, const void* x, const void
                         cudaStream_t s) {
   if (rows <= kPrefetchWeightRows)
     return launch_rows_pw<T, VPT, true>(g, out, x, w, res, rows, nvec, hidden_f, eps, w_add, s);
-  if constexpr (VPT <= 8) {
-    const size_t ring_smem =
-        static_cast<size_t>(NR_RMS_RING) * (res ? 2 : 1) * VPT * g.threads * sizeof(uint4);
-    if (ring_smem <= kRingMaxSmem) {
-      if (res != nullptr)
-        return launch_ring<T, VPT, true>(g, out, x, w, res, rows, nvec, hidden_f, eps, w_add, s);
-      return launch_ring<T, VPT, false>(g, out, x, w, res, rows, nvec, hidden_f, eps, w_add, s);
-    }
-  }
   return launch_rows_pw<T, VPT, false>(g, out, x, w, res, rows, nvec, hidden_f, eps, w_add, s);
 }
 

@@ -67,6 +67,34 @@ def parse_args():
 
 
 # ---------------------------------------------------------------------------
+# Sharding across ranks (one process per GPU).  Every row and every token is
+# independent, so ranks need no data exchange: a rank takes its own rows, and
+# RoPE takes global positions, so a token shard passes its own slice of them.
+# ---------------------------------------------------------------------------
+def shard_range(total, world, rank):
+    """Contiguous, balanced [lo, hi) of `total` units for `rank` of `world`."""
+    base, extra = divmod(total, world)
+    lo = rank * base + min(rank, extra)
+    return lo, lo + base + (1 if rank < extra else 0)
+
+
+def weak_positions_start(tokens_per_rank, rank):
+    """First global position of `rank`'s tokens when every rank holds the same
+    number of tokens of one longer sequence (weak scaling)."""
+    return rank * tokens_per_rank
+
+
+def max_over_ranks(value, dist, device=None):
+    """The maximum of a float over all ranks (the job's time is its slowest rank)."""
+    import torch
+
+    t = torch.tensor([float(value)], dtype=torch.float64,
+                     device=device if device is not None else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.item()
+
+
+# ---------------------------------------------------------------------------
 # Workload
 # ---------------------------------------------------------------------------
 class Call:
@@ -116,7 +144,8 @@ def build_step(nr, synth, torch, device, rank, only=None):
     c = synth.QK_NORM_ROPE
     if want("qk_norm_rope_bf16_26598x24x128"):
         q, k, wq, wk, pos = synth.qk_inputs(c["tokens"], c["hq"], c["hk"], c["head_dim"],
-                                            c["seed"], bf16, f32, pos_start=rank * c["tokens"])
+                                            c["seed"], bf16, f32,
+                                            pos_start=weak_positions_start(c["tokens"], rank))
         q, k, wq, wk, pos = (t.to(device) for t in (q, k, wq, wk, pos))
         qo, ko = torch.empty_like(q), torch.empty_like(k)
         calls.append(Call("qk_norm_rope_bf16_26598x24x128", "qk_norm_rope",
@@ -330,9 +359,7 @@ def run_ours(args):
     per_call_ms = [statistics.fmean(ev[i][j][0].elapsed_time(ev[i][j][1]) for i in range(K))
                    for j in range(len(calls))]
     if world > 1:
-        t = torch.tensor([elapsed_ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = t.item()
+        elapsed_ms = max_over_ranks(elapsed_ms, dist, device)
 
     ms_per_step = elapsed_ms / K
     value = world * step_bytes * K / (elapsed_ms * 1e-3) / 1e9
@@ -440,9 +467,7 @@ def run_e2e(args, torch, calls, device, world, barrier, step_bytes):
     if world > 1:
         import torch.distributed as dist
 
-        t = torch.tensor([ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = t.item()
+        ms = max_over_ranks(ms, dist, device)
     return {"value": round(world * step_bytes * n / (ms * 1e-3) / 1e9, 1), "unit": "GB/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n,
             "ms_per_step": round(ms / n, 3),

@@ -15,8 +15,10 @@
 // register-resident values (warp shuffles; one shared-memory step only when
 // WPR > 1), and the output is written once.  Rows beyond 16 vectors per
 // thread at 8 warps use a three-pass kernel that re-reads the (L2-resident)
-// row.  (A persistent variant streaming rows through a cp.async ring was
-// measured slower here: it trades resident warps for ring depth.)
+// row.  (Measured slower here and not used: a persistent variant streaming
+// rows through a cp.async ring, which trades resident warps for ring depth;
+// and staging (1 + scale) and shift per block in shared memory, which re-reads
+// them from L2 for every block instead of hitting L1.)
 #include "nr_common.cuh"
 #include "nr_internal.h"
 
@@ -122,96 +124,6 @@ __global__ void __launch_bounds__(ln_threads<WPR>()) ln_modulate_rows_kernel(
   }
 }
 
-// One modulation sample for all rows, rows of one warp: each block first
-// stages (1 + scale) and shift for the whole row as f32 in shared memory, so
-// the output step is two shared loads and one fma per element instead of two
-// unpacks, an add and an fma.  x is already in flight while the block stages.
-#ifndef NR_LN_STAGED
-#define NR_LN_STAGED 1
-#endif
-constexpr int kLnStagedThreads = 128;
-
-template <typename T, int VPT>
-__global__ void __launch_bounds__(kLnStagedThreads, VPT <= 12 ? 6 : 4) ln_modulate_staged_kernel(
-    T* __restrict__ out, const T* __restrict__ x, const T* __restrict__ shift,
-    const T* __restrict__ scale, int64_t rows, int nvec, float hidden_f, float eps) {
-  constexpr int N = Vec<T>::N;
-  extern __shared__ __align__(16) float params[];  // [nvec * N] (1 + scale), then [nvec * N] shift
-  float* gain = params;
-  float* bias = params + nvec * N;
-  const int lane = threadIdx.x % kWarp;
-  const int64_t row = static_cast<int64_t>(blockIdx.x) * (kLnStagedThreads / kWarp) +
-                      threadIdx.x / kWarp;
-  const bool active = row < rows;
-  const uint4* xr = reinterpret_cast<const uint4*>(x) + (active ? row : 0) * nvec;
-
-  uint4 xv[VPT];
-#pragma unroll
-  for (int k = 0; k < VPT; k++) {
-    const int vi = lane + k * kWarp;
-    if (active && vi < nvec) xv[k] = ld_stream(xr + vi);
-  }
-  for (int vi = threadIdx.x; vi < nvec; vi += kLnStagedThreads) {
-    float sc[N], sh[N];
-    Vec<T>::unpack(ld_param(reinterpret_cast<const uint4*>(scale) + vi), sc);
-    Vec<T>::unpack(ld_param(reinterpret_cast<const uint4*>(shift) + vi), sh);
-#pragma unroll
-    for (int e = 0; e < N; e += 4) {
-      *reinterpret_cast<float4*>(gain + vi * N + e) =
-          make_float4(1.0f + sc[e], 1.0f + sc[e + 1], 1.0f + sc[e + 2], 1.0f + sc[e + 3]);
-      *reinterpret_cast<float4*>(bias + vi * N + e) =
-          make_float4(sh[e], sh[e + 1], sh[e + 2], sh[e + 3]);
-    }
-  }
-  __syncthreads();
-  if (!active) return;
-
-  float sum = 0.0f;
-#pragma unroll
-  for (int k = 0; k < VPT; k++) {
-    if (lane + k * kWarp < nvec) {
-      float v[N];
-      Vec<T>::unpack(xv[k], v);
-#pragma unroll
-      for (int e = 0; e < N; e++) sum += v[e];
-    }
-  }
-  const float mu = __fdiv_rn(group_sum<kWarp>(sum), hidden_f);
-  float dev = 0.0f;
-#pragma unroll
-  for (int k = 0; k < VPT; k++) {
-    if (lane + k * kWarp < nvec) {
-      float v[N];
-      Vec<T>::unpack(xv[k], v);
-#pragma unroll
-      for (int e = 0; e < N; e++) {
-        const float d = v[e] - mu;
-        dev = fmaf(d, d, dev);
-      }
-    }
-  }
-  const float rstd = 1.0f / sqrtf(__fdiv_rn(group_sum<kWarp>(dev), hidden_f) + eps);
-  uint4* orow = reinterpret_cast<uint4*>(out) + row * nvec;
-#pragma unroll
-  for (int k = 0; k < VPT; k++) {
-    const int vi = lane + k * kWarp;
-    if (vi < nvec) {
-      float v[N];
-      Vec<T>::unpack(xv[k], v);
-#pragma unroll
-      for (int e = 0; e < N; e += 4) {
-        const float4 gq = *reinterpret_cast<const float4*>(gain + vi * N + e);
-        const float4 bq = *reinterpret_cast<const float4*>(bias + vi * N + e);
-        v[e] = fmaf((v[e] - mu) * rstd, gq.x, bq.x);
-        v[e + 1] = fmaf((v[e + 1] - mu) * rstd, gq.y, bq.y);
-        v[e + 2] = fmaf((v[e + 2] - mu) * rstd, gq.z, bq.z);
-        v[e + 3] = fmaf((v[e + 3] - mu) * rstd, gq.w, bq.w);
-      }
-      st_stream(orow + vi, Vec<T>::pack(v));
-    }
-  }
-}
-
 template <typename T>
 __global__ void __launch_bounds__(1024) ln_modulate_long_row_kernel(
     T* __restrict__ out, const T* __restrict__ x, const T* __restrict__ shift,
@@ -270,26 +182,8 @@ struct LnArgs {
   float eps;
 };
 
-template <typename T, int VPT>
-cudaError_t launch_staged(const LnArgs& a, cudaStream_t s) {
-  constexpr int RPB = kLnStagedThreads / kWarp;
-  const int64_t blocks = (a.rows + RPB - 1) / RPB;
-  const size_t smem = 2 * static_cast<size_t>(a.nvec) * Vec<T>::N * sizeof(float);
-  ln_modulate_staged_kernel<T, VPT><<<dim3(static_cast<unsigned>(blocks)), kLnStagedThreads,
-                                      smem, s>>>(
-      static_cast<T*>(a.out), static_cast<const T*>(a.x), static_cast<const T*>(a.shift),
-      static_cast<const T*>(a.scale), a.rows, a.nvec, a.hidden_f, a.eps);
-  return cudaGetLastError();
-}
-
 template <typename T, int VPT, int WPR>
 cudaError_t launch_rows(const LnArgs& a, cudaStream_t s) {
-  if constexpr (WPR == 1 && NR_LN_STAGED) {
-    // One sample for every row and the staged parameters fit the default
-    // 48 KB of shared memory (always true for one-warp rows).
-    if (a.rps >= a.rows && 2 * static_cast<size_t>(a.nvec) * Vec<T>::N * sizeof(float) <= 48 * 1024)
-      return launch_staged<T, VPT>(a, s);
-  }
   constexpr int THREADS = ln_threads<WPR>();
   constexpr int RPB = THREADS / (kWarp * WPR);
   static_assert(RPB >= 1, "row groups must fit the block");

@@ -33,7 +33,7 @@ namespace {
 
 // Iterations in flight per warp (shared-memory ring slots); a build-time knob.
 #ifndef NR_QK_RING
-#define NR_QK_RING 6
+#define NR_QK_RING 5
 #endif
 
 constexpr int kQkThreads = 128;

@@ -284,8 +284,9 @@ def source_hash(rel):
 
 def ncu_traffic(kernel, units):
     """DRAM bytes per launch of `kernel` from the committed ncu capture, scaled
-    to `units` if the capture ran a smaller case; None if the kernel's source
-    changed since the capture."""
+    by the units processed when the capture ran a smaller case (reads grow in
+    proportion; writes still dirty in L2 at the kernel's end are written back
+    after it and are not counted); None if the kernel's source changed since."""
     try:
         with open(TRAFFIC_FILE) as f:
             rec = json.load(f)[kernel]
@@ -293,7 +294,11 @@ def ncu_traffic(kernel, units):
         return None
     if rec.get("source_hash") != source_hash(KERNEL_SOURCES[kernel]):
         return None
-    return rec["dram_bytes_per_launch"] * units / rec["units"]
+    f = units / rec["units"]
+    return {"traffic": int(rec["dram_bytes_per_launch"] * f),
+            "traffic_read": int(rec["dram_bytes_read"] * f),
+            "traffic_write": int(rec["dram_bytes_write"] * f),
+            "traffic_source": "ncu capture of %s, scaled by %s" % (rec["case"], rec["unit"])}
 
 
 # ---------------------------------------------------------------------------
@@ -392,11 +397,12 @@ def run_ours(args):
                    "l2": "no flush: step footprint %.2f GB >> 129 MB L2; each large call's "
                          "operands exceed L2" % (step_bytes / 1e9),
                    "parallelism": "dp%d (independent row/token shards, no collective)" % world},
-        "roofline": {"bound": "hbm", "kernel": dc.name, "achieved": round(achieved, 1),
-                     "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4),
-                     "traffic": None if traffic is None else int(traffic),
-                     "algorithmic_bytes": dc.nbytes},
+        "roofline": dict({"bound": "hbm", "kernel": dc.name, "achieved": round(achieved, 1),
+                          "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                          "frac": round(achieved / peak, 4),
+                          "frac_of_nominal_8TBs": round(achieved / NOMINAL_HBM_GBS, 4),
+                          "traffic": None, "algorithmic_bytes": dc.nbytes},
+                         **(traffic or {})),
         "kernels": kernels,
         "rows_per_s": round(world * sum(c.rows for c in calls) / (ms_per_step * 1e-3), 1),
         "e2e": e2e,

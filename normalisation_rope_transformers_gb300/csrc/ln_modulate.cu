@@ -25,6 +25,12 @@
 namespace nr {
 namespace {
 
+// Minimum resident blocks per SM asked of the register allocator for
+// one-warp rows (0: none); a build-time knob.
+#ifndef NR_LN_MINB
+#define NR_LN_MINB 0
+#endif
+
 // Block size of a WPR-warp row group kernel: 128 threads, or one row group
 // when a row needs more than 4 warps.
 template <int WPR>
@@ -50,7 +56,8 @@ __device__ __forceinline__ float row_group_sum(float v, float* scratch) {
 }
 
 template <typename T, int VPT, int WPR>
-__global__ void __launch_bounds__(ln_threads<WPR>()) ln_modulate_rows_kernel(
+__global__ void __launch_bounds__(ln_threads<WPR>(), WPR == 1 ? NR_LN_MINB : 0)
+    ln_modulate_rows_kernel(
     T* __restrict__ out, const T* __restrict__ x, const T* __restrict__ shift,
     const T* __restrict__ scale, int64_t rows, int nvec, int64_t rows_per_sample, float hidden_f,
     float eps) {

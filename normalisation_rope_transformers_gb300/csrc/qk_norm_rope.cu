@@ -36,6 +36,12 @@ namespace {
 #define NR_QK_RING 5
 #endif
 
+// Minimum resident blocks per SM asked of the register allocator (0: none); a
+// build-time knob.
+#ifndef NR_QK_MINB
+#define NR_QK_MINB 0
+#endif
+
 constexpr int kQkThreads = 128;
 constexpr int kQkWarps = kQkThreads / kWarp;
 
@@ -88,7 +94,7 @@ struct QkSmem {
 };
 
 template <typename T, typename WT, int L, int RING>
-__global__ void __launch_bounds__(kQkThreads) qk_norm_rope_kernel(const QkArgs a,
+__global__ void __launch_bounds__(kQkThreads, NR_QK_MINB) qk_norm_rope_kernel(const QkArgs a,
                                                                   const RopeTurns turns) {
   using S = QkSmem<T, L>;
   constexpr int N = S::N;

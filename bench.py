@@ -59,6 +59,7 @@ def parse_args():
     p.add_argument("--e2e-steps", type=int, default=10)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-decode-sweep", action="store_true")
+    p.add_argument("--no-next-rows", action="store_true")
     p.add_argument("--profile", default=None,
                    help="run only the named call of the step (e.g. qk_norm_rope) --steps times, "
                         "for ncu; --rows overrides its row/token count; prints no JSON")
@@ -411,6 +412,8 @@ def run_ours(args):
     }
     if rank == 0 and not args.no_decode_sweep:
         result["decode_sweep"] = decode_sweep(nr, synth, torch, device)
+    if rank == 0 and not args.no_next_rows:
+        result["next_rows"] = next_rows(nr, synth, torch, device, peak)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(fraction=0.5)
     if world > 1:
@@ -478,6 +481,42 @@ def run_e2e(args, torch, calls, device, world, barrier, step_bytes):
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n,
             "ms_per_step": round(ms / n, 3),
             "note": "pinned host buffers; H2D, kernels and D2H on three streams ordered per call"}
+
+
+def next_rows(nr, synth, torch, device, peak):
+    """The ops beyond the seven-call step, each timed alone on its own workload
+    (mean of CUDA-event times over back-to-back calls, operands larger than L2)."""
+    out = {}
+
+    def timed(name, fn, nb, rows, iters=50):
+        for _ in range(5):
+            fn()
+        torch.cuda.synchronize()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        for _ in range(iters):
+            fn()
+        e.record()
+        torch.cuda.synchronize()
+        us = s.elapsed_time(e) * 1e3 / iters
+        gbs = nb / (us * 1e-6) / 1e9
+        out[name] = {"us": round(us, 2), "bytes": nb, "GB_s": round(gbs, 1),
+                     "frac_of_measured": round(gbs / peak, 4),
+                     "frac_of_nominal_8TBs": round(gbs / NOMINAL_HBM_GBS, 4),
+                     "rows_per_s": round(rows / (us * 1e-6), 1)}
+
+    # gated residual + LayerNorm + modulation at the DiT shape, one sample
+    rows, hidden = synth.LN_MODULATE["rows"], synth.LN_MODULATE["hidden"]
+    res = synth.tensor(5, 20, (rows, hidden), torch.bfloat16).to(device)
+    y = synth.tensor(5, 21, (rows, hidden), torch.bfloat16).to(device)
+    gate, sh, sc = (synth.tensor(5, i, (1, hidden), torch.bfloat16, std=0.1).to(device)
+                    for i in (22, 23, 24))
+    o = torch.empty_like(res)
+    timed("gated_residual_ln_modulate_bf16_26598x3072",
+          lambda: nr.gated_residual_ln_modulate(res, y, gate, sh, sc, out=o),
+          nbytes(res, y, gate, sh, sc) + nbytes(res, o), rows)
+    del res, y, o
+    return out
 
 
 def decode_sweep(nr, synth, torch, device):

@@ -142,6 +142,32 @@ nr_status nr_ln_modulate(void* out, const void* x, const void* shift, const void
                          nr_dtype dtype, cudaStream_t stream);
 
 /*
+ * Gated residual add fused with LayerNorm + adaLN modulation -- the DiT step
+ * around the fusion that nr_ln_modulate covers:
+ *     residual_j <- round(residual_j + gate_j * y_j)    (in place; the exact value
+ *                                                         rounded once)
+ *     out_j = round((v_j - mu) / sqrt(var + eps) * (1 + scale_j) + shift_j)
+ * with mu, var the mean and biased variance of the updated residual row v
+ * (f32 statistics).  The pages name the LayerNorm + modulation fusion
+ * (FastVideo compare view feat/pan2-inference-optimizations, PAN2 docs,
+ * "Performance switches", dit_fused_kernels) but not the gate; this is the
+ * plain DiT reading of the residual update next to it.
+ *
+ * out                    [rows, hidden], dtype `dtype`.
+ * residual               [rows, hidden], read and written in place.
+ * y                      [rows, hidden] (the branch output the gate scales).
+ * gate, shift, scale     [samples, hidden]; row r uses sample r / rows_per_sample.
+ * No operand may overlap out or residual.
+ * hidden > 0, a multiple of 8 (bf16) or 4 (f32), at most 8192 (bf16) / 4096 (f32);
+ * eps finite >= 0; rows_per_sample >= 1.
+ * Errors: as nr_rmsnorm.
+ */
+nr_status nr_gated_residual_ln_modulate(void* out, void* residual, const void* y,
+                                        const void* gate, const void* shift, const void* scale,
+                                        int64_t rows, int64_t hidden, int64_t rows_per_sample,
+                                        float eps, nr_dtype dtype, cudaStream_t stream);
+
+/*
  * silu_and_mul: out[r, j] = silu(x[r, j]) * x[r, inter + j],  silu(a) = a / (1 + e^-a).
  *
  * Follows vllm.cpp src/vt/cuda/cuda_ops.cu, "silu_and_mul" (gate is the first

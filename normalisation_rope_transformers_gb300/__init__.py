@@ -13,6 +13,8 @@ or ``__graft_entry__.build()``).
                  q_out=None, k_out=None)
     ln_modulate(x, shift, scale, eps=1e-6, rows_per_sample=None, out=None)
     silu_and_mul(x, out=None)
+    gated_residual_ln_modulate(residual, y, gate, shift, scale, eps=1e-6,
+                               rows_per_sample=None, out=None)
 """
 from __future__ import annotations
 
@@ -39,6 +41,9 @@ lib.nr_qk_norm_rope.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _int, _vp, _i64, _
 lib.nr_qk_norm_rope.restype = _int
 lib.nr_ln_modulate.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _f32, _int, _vp]
 lib.nr_ln_modulate.restype = _int
+lib.nr_gated_residual_ln_modulate.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64,
+                                              _f32, _int, _vp]
+lib.nr_gated_residual_ln_modulate.restype = _int
 lib.nr_silu_and_mul.argtypes = [_vp, _vp, _i64, _i64, _int, _vp]
 lib.nr_silu_and_mul.restype = _int
 lib.nr_status_string.argtypes = [_int]
@@ -51,6 +56,7 @@ lib.nr_version.restype = _int
 NR_F32 = 0
 NR_BF16 = 1
 ENTRY_POINTS = ("nr_rmsnorm", "nr_qk_norm_rope", "nr_ln_modulate", "nr_silu_and_mul",
+                "nr_gated_residual_ln_modulate",
                 "nr_status_string", "nr_last_error_message", "nr_version")
 
 
@@ -145,6 +151,26 @@ def ln_modulate(x, shift, scale, eps=1e-6, rows_per_sample=None, out=None):
     return out
 
 
+def gated_residual_ln_modulate(residual, y, gate, shift, scale, eps=1e-6, rows_per_sample=None,
+                               out=None):
+    """residual <- round(residual + gate * y) in place, then LayerNorm (no affine)
+    of it * (1 + scale) + shift.  gate/shift/scale are [samples, hidden]; row r
+    uses sample r // rows_per_sample.  Returns out."""
+    _cuda(residual, y, gate, shift, scale, out)
+    for t in (residual, y):
+        if t.dim() != 2 or not t.is_contiguous():
+            raise ValueError("residual and y must be contiguous [rows, hidden] tensors")
+    if rows_per_sample is None:
+        rows_per_sample = max(residual.shape[0], 1)
+    if out is None:
+        out = torch.empty_like(residual)
+    _check(lib.nr_gated_residual_ln_modulate(
+        _ptr(out), _ptr(residual), _ptr(y), _ptr(gate), _ptr(shift), _ptr(scale),
+        residual.shape[0], residual.shape[1], int(rows_per_sample), float(eps),
+        _dtype_code(residual), _stream(residual)))
+    return out
+
+
 def silu_and_mul(x, out=None):
     """silu(x[:, :I]) * x[:, I:] for x [rows, 2I].  Returns out [rows, I]."""
     _cuda(x, out)
@@ -157,5 +183,6 @@ def silu_and_mul(x, out=None):
     return out
 
 
-__all__ = ["rmsnorm", "qk_norm_rope", "ln_modulate", "silu_and_mul", "NrError", "lib",
+__all__ = ["rmsnorm", "qk_norm_rope", "ln_modulate", "silu_and_mul",
+           "gated_residual_ln_modulate", "NrError", "lib",
            "LIB_PATH", "ENTRY_POINTS", "NR_F32", "NR_BF16"]

@@ -131,6 +131,128 @@ __global__ void __launch_bounds__(ln_threads<WPR>(), WPR == 1 ? NR_LN_MINB : 0)
   }
 }
 
+// ---------------------------------------------------------------------------
+// Gated residual + LayerNorm + modulation: residual <- round(residual + gate*y)
+// (one rounding of the exact value), then out = LN(residual)*(1+scale)+shift.
+// ---------------------------------------------------------------------------
+template <typename T>
+struct GatedAdd;
+
+template <>
+struct GatedAdd<float> {
+  // fmaf rounds the exact r + g*y once.
+  __device__ __forceinline__ static uint4 apply(const uint4& r, const uint4& g, const uint4& y) {
+    float rv[4], gv[4], yv[4];
+    Vec<float>::unpack(r, rv);
+    Vec<float>::unpack(g, gv);
+    Vec<float>::unpack(y, yv);
+#pragma unroll
+    for (int e = 0; e < 4; e++) rv[e] = fmaf(gv[e], yv[e], rv[e]);
+    return Vec<float>::pack(rv);
+  }
+};
+
+template <>
+struct GatedAdd<__nv_bfloat16> {
+  // g*y of two bf16 values is exact in f32; TwoSum gives the exact error of
+  // adding r, and round_sum_bf16 rounds the exact sum once.
+  __device__ __forceinline__ static uint4 apply(const uint4& r, const uint4& g, const uint4& y) {
+    float rv[8], gv[8], yv[8];
+    Vec<__nv_bfloat16>::unpack(r, rv);
+    Vec<__nv_bfloat16>::unpack(g, gv);
+    Vec<__nv_bfloat16>::unpack(y, yv);
+    uint32_t bits[8];
+#pragma unroll
+    for (int e = 0; e < 8; e++) {
+      const float p = gv[e] * yv[e];
+      const float sum = p + rv[e];
+      const float bb = sum - p;
+      const float err = (p - (sum - bb)) + (rv[e] - bb);
+      bits[e] = round_sum_bf16(sum, err);
+    }
+    return make_uint4(bits[0] | (bits[1] << 16), bits[2] | (bits[3] << 16),
+                      bits[4] | (bits[5] << 16), bits[6] | (bits[7] << 16));
+  }
+};
+
+template <typename T, int VPT, int WPR>
+__global__ void __launch_bounds__(ln_threads<WPR>(), 4) gated_ln_modulate_kernel(
+    T* __restrict__ out, T* __restrict__ residual, const T* __restrict__ y,
+    const T* __restrict__ gate, const T* __restrict__ shift, const T* __restrict__ scale,
+    int64_t rows, int nvec, int64_t rows_per_sample, float hidden_f, float eps) {
+  constexpr int N = Vec<T>::N;
+  constexpr int THREADS = ln_threads<WPR>();
+  constexpr int TPR = kWarp * WPR;
+  constexpr int RPB = THREADS / TPR;
+  static_assert(RPB >= 1 && RPB * TPR == THREADS, "row groups must tile the block");
+  __shared__ float scratch_mean[THREADS / kWarp];
+  __shared__ float scratch_var[THREADS / kWarp];
+  const int t = threadIdx.x % TPR;
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * RPB + threadIdx.x / TPR;
+  const bool active = row < rows;
+  const int64_t r = active ? row : 0;
+  uint4* rr = reinterpret_cast<uint4*>(residual) + r * nvec;
+  const uint4* yr = reinterpret_cast<const uint4*>(y) + r * nvec;
+  uint4* orow = reinterpret_cast<uint4*>(out) + r * nvec;
+  const int64_t sample_off = (r / rows_per_sample) * nvec;
+  const uint4* gv = reinterpret_cast<const uint4*>(gate) + sample_off;
+  const uint4* shv = reinterpret_cast<const uint4*>(shift) + sample_off;
+  const uint4* scv = reinterpret_cast<const uint4*>(scale) + sample_off;
+
+  uint4 xv[VPT], yv[VPT];
+#pragma unroll
+  for (int k = 0; k < VPT; k++) {
+    const int vi = t + k * TPR;
+    if (active && vi < nvec) {
+      xv[k] = ld_stream(rr + vi);
+      yv[k] = ld_stream(yr + vi);
+    }
+  }
+  float sum = 0.0f;
+#pragma unroll
+  for (int k = 0; k < VPT; k++) {
+    const int vi = t + k * TPR;
+    if (active && vi < nvec) {
+      xv[k] = GatedAdd<T>::apply(xv[k], ld_param(gv + vi), yv[k]);
+      st_stream(rr + vi, xv[k]);
+      float v[N];
+      Vec<T>::unpack(xv[k], v);
+#pragma unroll
+      for (int e = 0; e < N; e++) sum += v[e];
+    }
+  }
+  const float mu = __fdiv_rn(row_group_sum<WPR>(sum, scratch_mean), hidden_f);
+  float dev = 0.0f;
+#pragma unroll
+  for (int k = 0; k < VPT; k++) {
+    const int vi = t + k * TPR;
+    if (active && vi < nvec) {
+      float v[N];
+      Vec<T>::unpack(xv[k], v);
+#pragma unroll
+      for (int e = 0; e < N; e++) {
+        const float d = v[e] - mu;
+        dev = fmaf(d, d, dev);
+      }
+    }
+  }
+  const float rstd = 1.0f / sqrtf(__fdiv_rn(row_group_sum<WPR>(dev, scratch_var), hidden_f) + eps);
+  if (!active) return;
+#pragma unroll
+  for (int k = 0; k < VPT; k++) {
+    const int vi = t + k * TPR;
+    if (vi < nvec) {
+      float v[N], sh[N], sc[N];
+      Vec<T>::unpack(xv[k], v);
+      Vec<T>::unpack(ld_param(shv + vi), sh);
+      Vec<T>::unpack(ld_param(scv + vi), sc);
+#pragma unroll
+      for (int e = 0; e < N; e++) v[e] = fmaf((v[e] - mu) * rstd, 1.0f + sc[e], sh[e]);
+      st_stream(orow + vi, Vec<T>::pack(v));
+    }
+  }
+}
+
 template <typename T>
 __global__ void __launch_bounds__(1024) ln_modulate_long_row_kernel(
     T* __restrict__ out, const T* __restrict__ x, const T* __restrict__ shift,
@@ -248,7 +370,73 @@ cudaError_t launch_typed(const LnArgs& a, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+struct GatedArgs {
+  void* out;
+  void* residual;
+  const void* y;
+  const void* gate;
+  const void* shift;
+  const void* scale;
+  int64_t rows;
+  int nvec;
+  int64_t rps;
+  float hidden_f;
+  float eps;
+};
+
+template <typename T, int VPT, int WPR>
+cudaError_t launch_gated_rows(const GatedArgs& a, cudaStream_t s) {
+  constexpr int THREADS = ln_threads<WPR>();
+  constexpr int RPB = THREADS / (kWarp * WPR);
+  const int64_t blocks = (a.rows + RPB - 1) / RPB;
+  gated_ln_modulate_kernel<T, VPT, WPR><<<dim3(static_cast<unsigned>(blocks)), THREADS, 0, s>>>(
+      static_cast<T*>(a.out), static_cast<T*>(a.residual), static_cast<const T*>(a.y),
+      static_cast<const T*>(a.gate), static_cast<const T*>(a.shift),
+      static_cast<const T*>(a.scale), a.rows, a.nvec, a.rps, a.hidden_f, a.eps);
+  return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_gated_typed(const GatedArgs& a, cudaStream_t s) {
+  for (int wpr : {1, 2, 4}) {
+    const int64_t need = (a.nvec + kWarp * wpr - 1) / (kWarp * wpr);
+    const int vpt = need <= 2 ? 2 : need <= 4 ? 4 : need <= 6 ? 6 : need <= 8 ? 8 : 0;
+    switch (wpr * 100 + vpt) {
+      case 102: return launch_gated_rows<T, 2, 1>(a, s);
+      case 104: return launch_gated_rows<T, 4, 1>(a, s);
+      case 106: return launch_gated_rows<T, 6, 1>(a, s);
+      case 108: return launch_gated_rows<T, 8, 1>(a, s);
+      case 206: return launch_gated_rows<T, 6, 2>(a, s);
+      case 208: return launch_gated_rows<T, 8, 2>(a, s);
+      case 406: return launch_gated_rows<T, 6, 4>(a, s);
+      case 408: return launch_gated_rows<T, 8, 4>(a, s);
+      default: break;
+    }
+  }
+  return cudaErrorNotSupported;  // rows beyond kGatedMaxVectors (rejected by the ABI first)
+}
+
 }  // namespace
+
+cudaError_t launch_gated_ln_modulate(void* out, void* residual, const void* y, const void* gate,
+                                     const void* shift, const void* scale, int64_t rows,
+                                     int64_t hidden, int64_t rows_per_sample, int is_bf16,
+                                     float eps, cudaStream_t stream) {
+  GatedArgs a;
+  a.out = out;
+  a.residual = residual;
+  a.y = y;
+  a.gate = gate;
+  a.shift = shift;
+  a.scale = scale;
+  a.rows = rows;
+  a.nvec = static_cast<int>(hidden / (is_bf16 ? 8 : 4));
+  a.rps = rows_per_sample;
+  a.hidden_f = static_cast<float>(hidden);
+  a.eps = eps;
+  if (is_bf16) return launch_gated_typed<__nv_bfloat16>(a, stream);
+  return launch_gated_typed<float>(a, stream);
+}
 
 cudaError_t launch_ln_modulate(void* out, const void* x, const void* shift, const void* scale,
                                int64_t rows, int64_t hidden, int64_t rows_per_sample,

@@ -231,6 +231,43 @@ nr_status nr_ln_modulate(void* out, const void* x, const void* shift, const void
                    "nr_ln_modulate launch");
 }
 
+nr_status nr_gated_residual_ln_modulate(void* out, void* residual, const void* y,
+                                        const void* gate, const void* shift, const void* scale,
+                                        int64_t rows, int64_t hidden, int64_t rows_per_sample,
+                                        float eps, nr_dtype dtype, cudaStream_t stream) {
+  const char* fn = "nr_gated_residual_ln_modulate";
+  if (!valid_dtype(dtype)) return fail(NR_ERR_DTYPE, "%s: unknown dtype %d", fn, (int)dtype);
+  if (rows < 0 || hidden <= 0 || rows_per_sample < 1)
+    return fail(NR_ERR_SHAPE, "%s: need rows >= 0, hidden > 0, rows_per_sample >= 1", fn);
+  if (!eps_ok(eps)) return fail(NR_ERR_VALUE, "%s: eps must be finite and >= 0", fn);
+  if (rows == 0) return ok();
+  if (!out || !residual || !y || !gate || !shift || !scale)
+    return fail(NR_ERR_NULL, "%s: every pointer must be non-NULL", fn);
+  const int vec = vec_elems(dtype);
+  if (hidden % vec != 0)
+    return fail(NR_ERR_UNSUPPORTED, "%s: hidden = %lld is not a multiple of %d", fn,
+                (long long)hidden, vec);
+  if (hidden / vec > nr::kGatedMaxVectors)
+    return fail(NR_ERR_UNSUPPORTED, "%s: hidden = %lld is above %lld for this dtype", fn,
+                (long long)hidden, (long long)(nr::kGatedMaxVectors * vec));
+  if (rows > INT32_MAX) return fail(NR_ERR_SHAPE, "%s: rows too large", fn);
+  if (!aligned16(out) || !aligned16(residual) || !aligned16(y) || !aligned16(gate) ||
+      !aligned16(shift) || !aligned16(scale))
+    return fail(NR_ERR_ALIGN, "%s: pointers must be 16-byte aligned", fn);
+  const int64_t row_bytes = hidden * elem_size(dtype);
+  const int64_t samples = (rows + rows_per_sample - 1) / rows_per_sample;
+  const Region ro = dense(out, rows * row_bytes), rr = dense(residual, rows * row_bytes);
+  const Region ins[] = {dense(y, rows * row_bytes), dense(gate, samples * row_bytes),
+                        dense(shift, samples * row_bytes), dense(scale, samples * row_bytes)};
+  if (overlap(ro, rr)) return fail(NR_ERR_ALIAS, "%s: out overlaps residual", fn);
+  for (const Region& in : ins)
+    if (overlap(ro, in) || overlap(rr, in))
+      return fail(NR_ERR_ALIAS, "%s: out or residual overlaps an input", fn);
+  return from_cuda(nr::launch_gated_ln_modulate(out, residual, y, gate, shift, scale, rows, hidden,
+                                                rows_per_sample, dtype == NR_BF16, eps, stream),
+                   "nr_gated_residual_ln_modulate launch");
+}
+
 nr_status nr_silu_and_mul(void* out, const void* x, int64_t rows, int64_t inter, nr_dtype dtype,
                           cudaStream_t stream) {
   if (!valid_dtype(dtype)) return fail(NR_ERR_DTYPE, "nr_silu_and_mul: unknown dtype %d", (int)dtype);

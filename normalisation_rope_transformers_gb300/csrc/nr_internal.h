@@ -45,6 +45,15 @@ cudaError_t launch_ln_modulate(void* out, const void* x, const void* shift, cons
                                int64_t rows, int64_t hidden, int64_t rows_per_sample,
                                int is_bf16, float eps, cudaStream_t stream);
 
+// Rows of the gated kernel hold at most this many 128-bit vectors
+// (4 warps x 32 lanes x 8 vectors).
+constexpr int64_t kGatedMaxVectors = 4 * 32 * 8;
+
+cudaError_t launch_gated_ln_modulate(void* out, void* residual, const void* y, const void* gate,
+                                     const void* shift, const void* scale, int64_t rows,
+                                     int64_t hidden, int64_t rows_per_sample, int is_bf16,
+                                     float eps, cudaStream_t stream);
+
 cudaError_t launch_silu_and_mul(void* out, const void* x, int64_t rows, int64_t inter,
                                 int is_bf16, cudaStream_t stream);
 

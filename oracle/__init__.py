@@ -59,6 +59,9 @@ def configure(lib):
     lib.nro_qk_norm_rope.restype = cint
     lib.nro_ln_modulate.argtypes = [cint, i64, i64, i64, vp, vp, vp, dbl, vp, vp, vp]
     lib.nro_ln_modulate.restype = None
+    lib.nro_gated_ln_modulate.argtypes = [cint, i64, i64, i64, vp, vp, vp, vp, vp, dbl, vp, vp,
+                                          vp, vp]
+    lib.nro_gated_ln_modulate.restype = None
     lib.nro_silu_and_mul.argtypes = [cint, i64, i64, vp, vp, vp]
     lib.nro_silu_and_mul.restype = None
     lib.nro_rounding_mode_is_nearest.argtypes = []
@@ -196,6 +199,30 @@ def ln_modulate(x, shift, scale, eps=1e-6, rows_per_sample=None, want_y=False):
     lib.nro_ln_modulate(dt, rows, hidden, int(rows_per_sample), _ptr(x), _ptr(shift), _ptr(scale),
                         float(eps), _ptr(out), _ptr(y), _ptr(mag))
     return out, y, mag
+
+
+def gated_ln_modulate(residual, y, gate, shift, scale, eps=1e-6, rows_per_sample=None,
+                      want_y=False):
+    """residual <- round(residual + gate * y) (one rounding of the exact value),
+    then LayerNorm + modulation of it.  gate/shift/scale are [samples, hidden].
+    Returns (out, residual_out, y or None, mag or None)."""
+    lib = _load()
+    residual, y = _c(residual), _c(y)
+    dt = _dtype_code(residual)
+    gate, shift, scale = (_c(np.atleast_2d(a)) for a in (gate, shift, scale))
+    for a in (y, gate, shift, scale):
+        if a.dtype != residual.dtype:
+            raise TypeError("all operands share one dtype")
+    rows, hidden = residual.shape
+    if rows_per_sample is None:
+        rows_per_sample = max(rows, 1)
+    out, res_out = np.empty_like(residual), np.empty_like(residual)
+    yv = np.empty(residual.shape, np.float64) if want_y else None
+    mag = np.empty(residual.shape, np.float64) if want_y else None
+    lib.nro_gated_ln_modulate(dt, rows, hidden, int(rows_per_sample), _ptr(residual), _ptr(y),
+                              _ptr(gate), _ptr(shift), _ptr(scale), float(eps), _ptr(res_out),
+                              _ptr(out), _ptr(yv), _ptr(mag))
+    return out, res_out, yv, mag
 
 
 def silu_and_mul(x, want_y=False):

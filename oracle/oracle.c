@@ -260,6 +260,33 @@ void nro_ln_modulate(int dtype, int64_t rows, int64_t hidden, int64_t rows_per_s
 }
 
 /* ------------------------------------------------------------------------ */
+/* Gated residual add + LayerNorm + adaLN modulation: the DiT step around the */
+/* fused LayerNorm + modulation ([PAN2], as read above):                      */
+/*   v_j = round_dtype(residual_j + gate_j * y_j)   (the exact value, rounded */
+/*         once; written back to the residual)                                */
+/*   out = LN(v) * (1 + scale) + shift              (nro_ln_modulate on v)    */
+/* gate, shift and scale hold one row per sample (row r: r / rows_per_sample). */
+/* ------------------------------------------------------------------------ */
+void nro_gated_ln_modulate(int dtype, int64_t rows, int64_t hidden, int64_t rows_per_sample,
+                           const void* residual, const void* y, const void* gate,
+                           const void* shift, const void* scale, double eps, void* res_out,
+                           void* out, double* y_out, double* mag) {
+  for (int64_t r = 0; r < rows; r++) {
+    const int64_t sample = (r / rows_per_sample) * hidden;
+    for (int64_t j = 0; j < hidden; j++) {
+      /* gate*y is exact in double (at most 48 significant bits); the sum is
+       * rounded once to double and then to the storage dtype, which equals
+       * rounding the exact sum once (53 >= 2p + 2 for p = 8 and p = 24). */
+      const double v = load(dtype, residual, r * hidden + j) +
+                       load(dtype, gate, sample + j) * load(dtype, y, r * hidden + j);
+      store(dtype, res_out, r * hidden + j, v);
+    }
+  }
+  nro_ln_modulate(dtype, rows, hidden, rows_per_sample, res_out, shift, scale, eps, out, y_out,
+                  mag);
+}
+
+/* ------------------------------------------------------------------------ */
 /* silu_and_mul ([VT] "silu_and_mul").  x is [rows, 2*inter]:                 */
 /*   a = x[r, j] (gate, first half), b = x[r, inter + j] (up, second half)    */
 /*   y = a / (1 + exp(-a)) * b;  out[r, j] = round_dtype(y)                   */

@@ -28,6 +28,8 @@ def lib(lib_path):
                                   f32, f64, cint, cint, vp]
     L.nr_ln_modulate.argtypes = [vp, vp, vp, vp, i64, i64, i64, f32, cint, vp]
     L.nr_silu_and_mul.argtypes = [vp, vp, i64, i64, cint, vp]
+    L.nr_gated_residual_ln_modulate.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, f32, cint,
+                                                vp]
     L.nr_status_string.argtypes = [cint]
     L.nr_status_string.restype = ctypes.c_char_p
     L.nr_last_error_message.restype = ctypes.c_char_p
@@ -149,3 +151,24 @@ def test_silu_and_mul_validation(lib):
     assert lib.nr_silu_and_mul(A, A + MB, 4, 60, BF16, None) == UNSUP
     assert lib.nr_silu_and_mul(A + 4, A + MB, 4, 64, F32, None) == ALIGN
     assert lib.nr_silu_and_mul(A, A + 256, 4, 64, BF16, None) == ALIAS  # out inside x
+
+
+def gated(lib, out=A, res=A + 64 * MB, y=A + 128 * MB, gate=A + 192 * MB, shift=A + 193 * MB,
+          scale=A + 194 * MB, rows=4, hidden=64, rps=4, eps=1e-6, dtype=BF16):
+    return lib.nr_gated_residual_ln_modulate(out, res, y, gate, shift, scale, rows, hidden, rps,
+                                             eps, dtype, None)
+
+
+def test_gated_residual_ln_modulate_validation(lib):
+    assert gated(lib, rows=0, out=None, res=None, y=None, gate=None, shift=None, scale=None) == OK
+    assert gated(lib, dtype=4) == DTYPE
+    assert gated(lib, rps=0) == SHAPE
+    assert gated(lib, gate=None) == NULL
+    assert gated(lib, hidden=20) == UNSUP
+    assert gated(lib, hidden=8200) == UNSUP  # above 8192 for bf16
+    assert gated(lib, hidden=4100, dtype=F32) == UNSUP  # above 4096 for f32
+    assert gated(lib, y=A + 128 * MB + 8) == ALIGN
+    assert gated(lib, eps=-0.5) == VALUE
+    assert gated(lib, out=A + 64 * MB) == ALIAS  # out is the residual
+    assert gated(lib, y=A + 64 * MB) == ALIAS  # y is the residual
+    assert gated(lib, shift=A + 16) == ALIAS  # shift inside out

@@ -53,6 +53,12 @@ MUTANTS = [
     ("ln shift sign", "const double yj = xhat * g + sh;", "const double yj = xhat * g - sh;"),
     ("ln sample index", "(r / rows_per_sample) * hidden", "(r % rows_per_sample) * hidden"),
     ("ln eps outside the sqrt", "1.0 / sqrt(var + eps)", "1.0 / (sqrt(var) + eps)"),
+    ("gated: gate ignored", "load(dtype, gate, sample + j) * load(dtype, y, r * hidden + j)",
+     "load(dtype, y, r * hidden + j)"),
+    ("gated: gate on the residual", "const double v = load(dtype, residual, r * hidden + j) +\n                       load(dtype, gate, sample + j) * load(dtype, y, r * hidden + j);",
+     "const double v = load(dtype, residual, r * hidden + j) * load(dtype, gate, sample + j) +\n                       load(dtype, y, r * hidden + j);"),
+    ("gated: sample index", "const int64_t sample = (r / rows_per_sample) * hidden;\n    for (int64_t j = 0; j < hidden; j++) {\n      /* gate",
+     "const int64_t sample = (r % rows_per_sample) * hidden;\n    for (int64_t j = 0; j < hidden; j++) {\n      /* gate"),
     ("silu exponent sign", "a / (1.0 + exp(-a)) * b", "a / (1.0 + exp(a)) * b"),
     ("silu gate and up swapped", "const double a = load(dtype, x, r * 2 * inter + j);\n      const double b = load(dtype, x, r * 2 * inter + inter + j);",
      "const double b = load(dtype, x, r * 2 * inter + j);\n      const double a = load(dtype, x, r * 2 * inter + inter + j);"),

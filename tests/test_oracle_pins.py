@@ -453,6 +453,85 @@ def test_ln_modulation_uses_one_plus_scale():
 
 
 # --------------------------------------------------------------------------
+# gated residual + LayerNorm + modulation
+# --------------------------------------------------------------------------
+def _gated_inputs(rows, hidden, seed, samples=1, dtype=torch.bfloat16):
+    res = synth.tensor(seed, 20, (rows, hidden), dtype)
+    y = synth.tensor(seed, 21, (rows, hidden), dtype)
+    gate = synth.tensor(seed, 22, (samples, hidden), dtype, std=0.5)
+    shift = synth.tensor(seed, 23, (samples, hidden), dtype, std=0.1)
+    scale = synth.tensor(seed, 24, (samples, hidden), dtype, std=0.1)
+    return [synth.to_oracle(t) for t in (res, y, gate, shift, scale)]
+
+
+def test_gated_zero_gate_is_plain_ln_modulate():
+    res, y, gate, shift, scale = _gated_inputs(6, 64, 81)
+    zero = np.zeros_like(gate)
+    out, res_out, yv, _ = oracle.gated_ln_modulate(res, y, zero, shift, scale, want_y=True)
+    assert np.array_equal(res_out, res)
+    o2, y2, _ = oracle.ln_modulate(res, shift, scale, want_y=True)
+    assert np.array_equal(out, o2) and np.array_equal(yv, y2)
+
+
+def test_gated_unit_gate_is_the_residual_add():
+    """gate = 1: the residual update is the plain residual add (pinned above)."""
+    res, y, gate, shift, scale = _gated_inputs(6, 64, 82)
+    one = bf16([[1.0] * 64])
+    _, res_out, _, _ = oracle.gated_ln_modulate(res, y, one, shift, scale)
+    _, r2, _ = oracle.rmsnorm(y, bf16([1.0] * 64), residual=res)
+    assert np.array_equal(res_out, r2)
+
+
+def test_gated_residual_is_one_exact_rounding():
+    """round(r + g*y) against exact rational arithmetic, over wide exponent gaps."""
+    rng = np.random.default_rng(83)
+    n = 16 * 64
+
+    def spread(seed_shift):
+        a = rng.standard_normal(n) * np.exp2(rng.integers(-20, 20, n))
+        return torch.from_numpy(a).to(torch.bfloat16)
+
+    r, g, yy = spread(0), spread(1), spread(2)
+    ro, go, yo = (synth.to_oracle(t) for t in (r, g, yy))
+    zero = np.zeros((1, 64), np.uint16)
+    for i in range(16):
+        sl = slice(i * 64, (i + 1) * 64)
+        _, res_out, _, _ = oracle.gated_ln_modulate(ro[sl].reshape(1, 64), yo[sl].reshape(1, 64),
+                                                    go[sl].reshape(1, 64), zero, zero)
+        rv, gv, yv = (bf16_to_f64(a[sl]) for a in (ro, go, yo))
+        for j in range(0, 64, 3):
+            exact = Fraction(rv[j]) + Fraction(gv[j]) * Fraction(yv[j])
+            assert res_out[0, j] == _nearest_bf16_exact(float(exact)) or \
+                bf16_to_f64(np.array([res_out[0, j]], np.uint16))[0] == float(exact)
+
+
+def test_gated_residual_rounds_exactly_at_f32_midpoints():
+    """g*y an exact bf16 midpoint (1.75 * 37/64 = 1 + 3*2^-8) plus a tiny r:
+    the exact sum is just off the midpoint, so the single rounding goes the
+    way r points (an f32 sum would land on the midpoint and tie to even)."""
+    g, yv = bf16([[1.75, 1.75]]), bf16([[37 / 64, 37 / 64]])
+    r = bf16([[2.0 ** -25, -(2.0 ** -25)]])
+    zero = bf16([[0.0, 0.0]])
+    _, res_out, _, _ = oracle.gated_ln_modulate(r, yv, g, zero, zero)
+    mid = 1 + 3 * 2.0 ** -8
+    for j in range(2):
+        exact = Fraction(mid) + Fraction(bf16_to_f64(r)[0, j])
+        assert res_out[0, j] == _nearest_bf16_exact(float(exact))
+    assert list(res_out[0]) == [0x3F82, 0x3F81]
+
+
+def test_gated_per_sample_gate_rows():
+    """Row r uses gate row r // rows_per_sample: with y = 1 and residual = 0
+    the updated residual is the gate row itself."""
+    res = np.zeros((4, 8), np.uint16)
+    y = bf16([[1.0] * 8] * 4)
+    gate = bf16([[0.5] * 8, [-2.0] * 8])
+    zero = np.zeros((2, 8), np.uint16)
+    _, res_out, _, _ = oracle.gated_ln_modulate(res, y, gate, zero, zero, rows_per_sample=2)
+    assert np.array_equal(res_out, gate[[0, 0, 1, 1]])
+
+
+# --------------------------------------------------------------------------
 # silu_and_mul
 # --------------------------------------------------------------------------
 def test_silu_closed_forms_and_operand_order():

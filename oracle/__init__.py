@@ -57,6 +57,10 @@ def configure(lib):
     lib.nro_qk_norm_rope.argtypes = [cint, cint, i64, i64, i64, i64, vp, i64, vp, i64, vp, vp,
                                      vp, dbl, dbl, cint, vp, vp, vp, vp, vp, vp]
     lib.nro_qk_norm_rope.restype = cint
+    lib.nro_qk_norm_rope_ex.argtypes = [cint, cint, i64, i64, i64, i64, vp, i64, vp, i64, vp, vp,
+                                        vp, dbl, cint, i64, cint, dbl, dbl, dbl, dbl, dbl, vp,
+                                        cint, vp, vp, vp, vp, vp, vp]
+    lib.nro_qk_norm_rope_ex.restype = cint
     lib.nro_ln_modulate.argtypes = [cint, i64, i64, i64, vp, vp, vp, dbl, vp, vp, vp]
     lib.nro_ln_modulate.restype = None
     lib.nro_gated_ln_modulate.argtypes = [cint, i64, i64, i64, vp, vp, vp, vp, vp, dbl, vp, vp,
@@ -176,6 +180,40 @@ def qk_norm_rope(q, k, wq, wk, positions, eps=1e-6, theta=10000.0, gemma=False, 
     if rc != 0:
         raise ValueError("oracle qk_norm_rope: head_dim must be even and <= 1024")
     return q_out, k_out, q_y, k_y, q_mag, k_mag
+
+
+def qk_norm_rope_ex(q, k, wq, wk, positions, eps=1e-6, gemma=False, rotary_dim=None,
+                    interleaved=False, theta=10000.0, llama3=None, mrope_sections=None,
+                    mrope_interleaved=False, want_y=False):
+    """The RoPE variants on top of the per-head RMSNorm: rotary_dim (default
+    head_dim), GPT-J interleaved pairing, Llama-3 frequency rescale
+    (llama3 = (factor, low_freq_factor, high_freq_factor, original_max_position)),
+    M-RoPE (positions [3, tokens], mrope_sections = (t, h, w), contiguous or
+    interleaved).  Returns (q_out, k_out, q_y, k_y, q_mag, k_mag), dense."""
+    lib = _load()
+    dt = _dtype_code(q)
+    wq, wk = _c(wq), _c(wk)
+    wdt = _dtype_code(wq)
+    tokens, hq, D = q.shape
+    _, hk, _ = k.shape
+    rot = D if rotary_dim is None else int(rotary_dim)
+    q_d, k_d = np.ascontiguousarray(q), np.ascontiguousarray(k)
+    pos = np.ascontiguousarray(positions, dtype=np.int32)
+    want_shape = (3, tokens) if mrope_sections is not None else (tokens,)
+    if pos.shape != want_shape:
+        raise ValueError("positions must be %s" % (want_shape,))
+    l3 = (0.0, 1.0, 4.0, 8192.0) if llama3 is None else tuple(float(v) for v in llama3)
+    sec = None if mrope_sections is None else np.ascontiguousarray(mrope_sections, dtype=np.int32)
+    q_out, k_out = np.empty_like(q_d), np.empty_like(k_d)
+    arrs = [np.empty(a.shape, np.float64) if want_y else None for a in (q_d, k_d, q_d, k_d)]
+    rc = lib.nro_qk_norm_rope_ex(dt, wdt, tokens, hq, hk, D, _ptr(q_d), hq * D, _ptr(k_d), hk * D,
+                                 _ptr(wq), _ptr(wk), _ptr(pos), float(eps), int(gemma), rot,
+                                 int(bool(interleaved)), float(theta), *l3, _ptr(sec),
+                                 int(bool(mrope_interleaved)), _ptr(q_out), _ptr(k_out),
+                                 *(_ptr(a) for a in arrs))
+    if rc != 0:
+        raise ValueError("oracle qk_norm_rope_ex: unsupported shape")
+    return (q_out, k_out, *arrs)
 
 
 def ln_modulate(x, shift, scale, eps=1e-6, rows_per_sample=None, want_y=False):

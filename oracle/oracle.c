@@ -215,6 +215,109 @@ int nro_qk_norm_rope(int dtype, int w_dtype, int64_t tokens, int64_t hq, int64_t
 }
 
 /* ------------------------------------------------------------------------ */
+/* RoPE variants on top of the per-head RMSNorm ([VT] "rope_neox",            */
+/* "Supplied-cache RoPE", "attn_qk_norm_rope_gate"):                           */
+/*  - rotary dim rot <= D: pairs i < rot/2 rotate; elements [rot, D) keep the */
+/*    normed value;  f_i = theta^(-2i/rot)                                     */
+/*  - pairing: rotate-half (i, i + rot/2) or interleaved GPT-J (2i, 2i + 1)    */
+/*  - Llama-3 frequency rescale (factor > 0): with wavelength L = 2pi / f,     */
+/*    L < orig/high keeps f, L > orig/low gives f / factor, and in between    */
+/*    f is interpolated with weight s = (orig/L - low) / (high - low) on the  */
+/*    unscaled frequency: (1 - s) f / factor + s f                            */
+/*  - M-RoPE: positions are [3, tokens] (axis t, h, w); pair i takes the       */
+/*    position of axis(i): contiguous sections (t: i < sec_t, h: next sec_h,  */
+/*    w: the rest) or interleaved (i % 3 == 1 within the first sec_h such     */
+/*    pairs: h; i % 3 == 2 within the first sec_w: w; otherwise t).           */
+/* ------------------------------------------------------------------------ */
+static double llama3_frequency(double f, double factor, double low, double high, double orig) {
+  if (!(factor > 0.0)) return f;
+  const double two_pi = 6.283185307179586476925286766559;
+  const double wavelength = two_pi / f;
+  if (wavelength < orig / high) return f;
+  if (wavelength > orig / low) return f / factor;
+  const double s = (low != high) ? (orig / wavelength - low) / (high - low) : 0.0;
+  return (1.0 - s) * f / factor + s * f;
+}
+
+static int mrope_axis(int64_t i, const int* sections, int interleaved) {
+  if (sections == NULL) return 0;
+  if (interleaved) {
+    if (i % 3 == 1 && i / 3 < sections[1]) return 1;
+    if (i % 3 == 2 && i / 3 < sections[2]) return 2;
+    return 0;
+  }
+  if (i < sections[0]) return 0;
+  if (i < sections[0] + sections[1]) return 1;
+  return 2;
+}
+
+static void norm_rope_ex_one(int dtype, int w_dtype, int64_t tokens, int64_t heads, int64_t D,
+                             const void* src, int64_t tok_stride, const void* w,
+                             const int32_t* pos, double eps, int gemma, int64_t rot,
+                             int interleaved, double theta, double l3_factor, double l3_low,
+                             double l3_high, double l3_orig, const int* sections,
+                             int mrope_interleaved, void* dst, double* y, double* mag) {
+  double n[1024];
+  for (int64_t t = 0; t < tokens; t++) {
+    for (int64_t h = 0; h < heads; h++) {
+      const int64_t row0 = t * tok_stride + h * D;
+      double sum_sq = 0.0;
+      for (int64_t j = 0; j < D; j++) {
+        const double v = load(dtype, src, row0 + j);
+        sum_sq += v * v;
+      }
+      const double inv = 1.0 / sqrt(sum_sq / (double)D + eps);
+      for (int64_t j = 0; j < D; j++) {
+        double wj = load(w_dtype, w, j);
+        if (gemma) wj += 1.0;
+        n[j] = load(dtype, src, row0 + j) * inv * wj;
+      }
+      for (int64_t j = rot; j < D; j++) { /* not rotated: the normed value */
+        store(dtype, dst, row0 + j, n[j]);
+        if (y != NULL) y[row0 + j] = n[j];
+        if (mag != NULL) mag[row0 + j] = fabs(n[j]);
+      }
+      for (int64_t i = 0; i < rot / 2; i++) {
+        const double f = llama3_frequency(pow(theta, -2.0 * (double)i / (double)rot), l3_factor,
+                                          l3_low, l3_high, l3_orig);
+        const int axis = mrope_axis(i, sections, mrope_interleaved);
+        const double angle = (double)pos[axis * tokens + t] * f;
+        const double c = cos(angle), s = sin(angle);
+        const int64_t a = interleaved ? 2 * i : i;
+        const int64_t b = interleaved ? 2 * i + 1 : i + rot / 2;
+        const double ya = n[a] * c - n[b] * s;
+        const double yb = n[a] * s + n[b] * c;
+        store(dtype, dst, row0 + a, ya);
+        store(dtype, dst, row0 + b, yb);
+        if (y != NULL) {
+          y[row0 + a] = ya;
+          y[row0 + b] = yb;
+        }
+        if (mag != NULL) mag[row0 + a] = mag[row0 + b] = fabs(n[a]) + fabs(n[b]);
+      }
+    }
+  }
+}
+
+/* Returns 0, or -1 for a shape the definition does not cover. */
+int nro_qk_norm_rope_ex(int dtype, int w_dtype, int64_t tokens, int64_t hq, int64_t hk,
+                        int64_t head_dim, const void* q, int64_t q_tok_stride, const void* k,
+                        int64_t k_tok_stride, const void* wq, const void* wk, const int32_t* pos,
+                        double eps, int gemma, int64_t rot, int interleaved, double theta,
+                        double l3_factor, double l3_low, double l3_high, double l3_orig,
+                        const int* sections, int mrope_interleaved, void* q_out, void* k_out,
+                        double* q_y, double* k_y, double* q_mag, double* k_mag) {
+  if (head_dim <= 0 || head_dim > 1024 || rot <= 0 || rot > head_dim || rot % 2 != 0) return -1;
+  norm_rope_ex_one(dtype, w_dtype, tokens, hq, head_dim, q, q_tok_stride, wq, pos, eps, gemma,
+                   rot, interleaved, theta, l3_factor, l3_low, l3_high, l3_orig, sections,
+                   mrope_interleaved, q_out, q_y, q_mag);
+  norm_rope_ex_one(dtype, w_dtype, tokens, hk, head_dim, k, k_tok_stride, wk, pos, eps, gemma,
+                   rot, interleaved, theta, l3_factor, l3_low, l3_high, l3_orig, sections,
+                   mrope_interleaved, k_out, k_y, k_mag);
+  return 0;
+}
+
+/* ------------------------------------------------------------------------ */
 /* LayerNorm (no affine) + adaLN modulation ([PAN2]; formula as read above).   */
 /*                                                                            */
 /*   mu = mean_j x_j;  var = mean_j (x_j - mu)^2   (two passes, biased)       */

@@ -59,6 +59,18 @@ MUTANTS = [
      "const double v = load(dtype, residual, r * hidden + j) * load(dtype, gate, sample + j) +\n                       load(dtype, y, r * hidden + j);"),
     ("gated: sample index", "const int64_t sample = (r / rows_per_sample) * hidden;\n    for (int64_t j = 0; j < hidden; j++) {\n      /* gate",
      "const int64_t sample = (r % rows_per_sample) * hidden;\n    for (int64_t j = 0; j < hidden; j++) {\n      /* gate"),
+    ("rope-ex: head stride", "const int64_t row0 = t * tok_stride + h * D;",
+     "const int64_t row0 = t * tok_stride + h * (D - 2);"),
+    ("rope-ex: frequency over D, not rot", "pow(theta, -2.0 * (double)i / (double)rot)",
+     "pow(theta, -2.0 * (double)i / (double)D)"),
+    ("rope-ex: interleaved pairs (i, i+1)", "const int64_t a = interleaved ? 2 * i : i;",
+     "const int64_t a = interleaved ? i : i;"),
+    ("rope-ex: llama3 regions swapped", "if (wavelength > orig / low) return f / factor;",
+     "if (wavelength > orig / low) return f;"),
+    ("rope-ex: mrope interleaved off by one", "if (i % 3 == 1 && i / 3 < sections[1]) return 1;",
+     "if (i % 3 == 1 && i / 3 <= sections[1]) return 1;"),
+    ("rope-ex: mrope contiguous sections", "if (i < sections[0] + sections[1]) return 1;",
+     "if (i < sections[1]) return 1;"),
     ("silu exponent sign", "a / (1.0 + exp(-a)) * b", "a / (1.0 + exp(a)) * b"),
     ("silu gate and up swapped", "const double a = load(dtype, x, r * 2 * inter + j);\n      const double b = load(dtype, x, r * 2 * inter + inter + j);",
      "const double b = load(dtype, x, r * 2 * inter + j);\n      const double a = load(dtype, x, r * 2 * inter + inter + j);"),
@@ -103,7 +115,7 @@ def test_real_oracle_passes_all_pins():
 def test_mutant_is_caught(name, old, new, tmp_path):
     src = open(SRC).read()
     assert src.count(old) >= 1, "mutation anchor not found: %r" % old
-    mutated = src.replace(old, new)
+    mutated = src.replace(old, new, 1)  # the first occurrence only
     path = tmp_path / "mutant.c"
     path.write_text(mutated)
     lib_path = oracle.compile_source(str(path), str(tmp_path / "libmutant.so"))

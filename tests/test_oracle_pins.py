@@ -393,6 +393,100 @@ def test_rope_brute_force_4_tokens():
 
 
 # --------------------------------------------------------------------------
+# RoPE variants
+# --------------------------------------------------------------------------
+def test_rope_ex_defaults_equal_the_plain_rope():
+    q, k, wq, wk, _ = _qk_small(tokens=4, hq=2, hk=2, D=64, seed=91)
+    pos = np.array([0, 5, 300, 26000], np.int32)
+    a = oracle.qk_norm_rope(q, k, wq, wk, pos, want_y=True)
+    b = oracle.qk_norm_rope_ex(q, k, wq, wk, pos, want_y=True)
+    for x, y in zip(a, b):
+        assert np.array_equal(x, y)
+
+
+def _onehot_ex(idx, p, D=128, **kw):
+    q = np.zeros((1, 1, D), np.float32)
+    q[0, 0, idx] = 1.0
+    q = synth.to_oracle(torch.from_numpy(q).to(torch.bfloat16))
+    w = (1.0 + np.arange(D) / 256.0).astype(np.float32)
+    pos = kw.pop("pos", np.array([p], np.int32))
+    _, _, qy, _, _, _ = oracle.qk_norm_rope_ex(q, q.copy(), w, w, pos, eps=0.0, want_y=True, **kw)
+    return qy[0, 0], math.sqrt(D) * float(w[idx])
+
+
+def test_rope_partial_rotary_pairs_and_unrotated_tail():
+    """rot = 64 of D = 128: pair (i, i + 32) with freq theta^(-2i/64); elements
+    64..127 keep their normed value whatever the position."""
+    y, n = _onehot_ex(0, 1, rotary_dim=64)
+    assert abs(y[0] - n * math.cos(1.0)) < 1e-12 and abs(y[32] - n * math.sin(1.0)) < 1e-12
+    assert y[64] == 0.0
+    y, n = _onehot_ex(16, 100, rotary_dim=64)  # 10000^(-32/64) = 1/100
+    assert abs(y[16] - n * math.cos(1.0)) < 1e-12 and abs(y[48] - n * math.sin(1.0)) < 1e-12
+    y, n = _onehot_ex(100, 12345, rotary_dim=64)
+    assert abs(y[100] - n) < 1e-12 and np.count_nonzero(y) == 1
+    q, k, wq, wk, _ = _qk_small(tokens=3, hq=2, hk=1, D=64, seed=92)
+    wb = synth.to_oracle(torch.from_numpy(wq).to(torch.bfloat16))
+    out = oracle.qk_norm_rope_ex(q, k, wb, wb, np.array([7, 70, 700], np.int32), rotary_dim=32,
+                                 want_y=True)
+    _, _, ry = oracle.rmsnorm(q.reshape(-1, 64), wb, want_y=True)
+    assert np.array_equal(out[2].reshape(-1, 64)[:, 32:], ry[:, 32:])
+
+
+def test_rope_interleaved_pairs():
+    """GPT-J pairing: (2i, 2i + 1), freq theta^(-2i/rot)."""
+    y, n = _onehot_ex(0, 1, interleaved=True)
+    assert abs(y[0] - n * math.cos(1.0)) < 1e-12 and abs(y[1] - n * math.sin(1.0)) < 1e-12
+    y, n = _onehot_ex(65, 100, interleaved=True)  # pair 32 (odd member): freq 1/100
+    assert abs(y[64] + n * math.sin(1.0)) < 1e-12 and abs(y[65] - n * math.cos(1.0)) < 1e-12
+
+
+def test_rope_llama3_rescale_regions():
+    """orig 8192, low 1, high 4, factor 8: wavelengths below 2048 keep f, above
+    8192 divide f by 8, in between interpolate with s = (8192/L - 1)/3."""
+    D, theta = 128, 500000.0
+    f = [theta ** (-2 * i / D) for i in range(D // 2)]
+    L = [2 * math.pi / x for x in f]
+    i_hi = max(i for i in range(64) if L[i] < 2048)
+    i_lo = min(i for i in range(64) if L[i] > 8192)
+    i_mid = next(i for i in range(64) if 2048 <= L[i] <= 8192)
+    for i, expect in ((i_hi, f[i_hi]), (i_lo, f[i_lo] / 8),
+                      (i_mid, (1 - (8192 / L[i_mid] - 1) / 3) * f[i_mid] / 8
+                       + (8192 / L[i_mid] - 1) / 3 * f[i_mid])):
+        p = 3
+        y, n = _onehot_ex(i, p, theta=theta, llama3=(8.0, 1.0, 4.0, 8192.0))
+        assert abs(y[i] - n * math.cos(p * expect)) < 1e-12
+        assert abs(y[i + 64] - n * math.sin(p * expect)) < 1e-12
+    y1, _ = _onehot_ex(5, 77, theta=theta, llama3=(1.0, 1.0, 4.0, 8192.0))  # factor 1: no change
+    y0, _ = _onehot_ex(5, 77, theta=theta)
+    assert np.allclose(y1, y0, rtol=0, atol=1e-15)
+
+
+@pytest.mark.parametrize("interleaved", [False, True])
+def test_mrope_axis_selection(interleaved):
+    """Three equal position rows reproduce plain RoPE; changing only the h row
+    changes exactly the pairs of axis h."""
+    D, T = 32, 3  # 16 pairs
+    sec = (8, 3, 5)
+    q, k, wq, wk, _ = _qk_small(tokens=T, hq=1, hk=1, D=D, seed=93)
+    base = np.array([11, 222, 3333], np.int32)
+    same = np.stack([base, base, base])
+    a = oracle.qk_norm_rope(q, k, wq, wk, base, want_y=True)
+    b = oracle.qk_norm_rope_ex(q, k, wq, wk, same, mrope_sections=sec,
+                               mrope_interleaved=interleaved, want_y=True)
+    assert np.array_equal(a[2], b[2])
+    moved = same.copy()
+    moved[1] += 1000
+    c = oracle.qk_norm_rope_ex(q, k, wq, wk, moved, mrope_sections=sec,
+                               mrope_interleaved=interleaved, want_y=True)
+    if interleaved:
+        h_pairs = [i for i in range(16) if i % 3 == 1 and i // 3 < sec[1]]
+    else:
+        h_pairs = list(range(sec[0], sec[0] + sec[1]))
+    changed = [i for i in range(16) if not np.allclose(c[2][..., i], b[2][..., i], atol=1e-14)]
+    assert changed == h_pairs
+
+
+# --------------------------------------------------------------------------
 # LayerNorm + adaLN modulation
 # --------------------------------------------------------------------------
 def test_ln_row_1_to_8_closed_form():

@@ -121,6 +121,55 @@ nr_status nr_qk_norm_rope(void* q_out, void* k_out, const void* q, const void* k
                           int gemma, nr_dtype dtype, cudaStream_t stream);
 
 /*
+ * RoPE variants for nr_qk_norm_rope_ex.  Zero-initialise, then set theta.
+ *   rotary_dim           0 or head_dim: rotate the whole head; else the first
+ *                        rotary_dim elements rotate and the rest keep their
+ *                        normed value (vllm.cpp cuda_ops.cu,
+ *                        "attn_qk_norm_rope_gate"); freq_i = theta^(-2i/rotary_dim).
+ *   interleaved          0: rotate-half pairs (i, i + rotary_dim/2) (NeoX);
+ *                        1: GPT-J pairs (2i, 2i + 1) ("Supplied-cache RoPE").
+ *   llama3_factor > 0    Llama-3 frequency rescale ("rope_neox", Llama-3
+ *                        rescale): with wavelength L = 2pi / freq, L below
+ *                        original_max_position / high_freq_factor keeps freq,
+ *                        L above original_max_position / low_freq_factor
+ *                        divides it by llama3_factor, and in between it is
+ *                        interpolated.
+ *   mrope_section        all zero: positions are [tokens]; else M-RoPE with
+ *                        positions [3, tokens] (rows t, h, w) and sections
+ *                        (t, h, w) summing to rotary_dim / 2: contiguous, or
+ *                        with mrope_interleaved = 1 the t/h/w rows cycle over
+ *                        pairs i % 3 = 0/1/2 while each of h and w has pairs
+ *                        left ("Supplied-cache RoPE", M-RoPE axis selection).
+ */
+typedef struct nr_rope_config {
+  int64_t rotary_dim;
+  int32_t interleaved;
+  int32_t mrope_interleaved;
+  double theta;
+  double llama3_factor;
+  double llama3_low_freq_factor;
+  double llama3_high_freq_factor;
+  double llama3_original_max_position;
+  int32_t mrope_section[3];
+} nr_rope_config;
+
+/*
+ * nr_qk_norm_rope with the RoPE variants of nr_rope_config.  Arguments as for
+ * nr_qk_norm_rope (theta comes from the config); `positions` is [3, tokens]
+ * when M-RoPE is on.  Additional requirements: 0 < rotary_dim <= head_dim,
+ * rotary_dim a multiple of 16 (bf16) or 8 (f32) for rotate-half pairs and of 8
+ * (bf16) or 4 (f32) for interleaved pairs; Llama-3 factors positive with
+ * high_freq_factor >= low_freq_factor; M-RoPE sections >= 0.
+ * Errors: as nr_qk_norm_rope; a NULL config is NR_ERR_NULL.
+ */
+nr_status nr_qk_norm_rope_ex(void* q_out, void* k_out, const void* q, const void* k,
+                             const void* wq, const void* wk, nr_dtype w_dtype,
+                             const int32_t* positions, int64_t tokens, int64_t hq, int64_t hk,
+                             int64_t head_dim, int64_t q_tok_stride, int64_t k_tok_stride,
+                             float eps, int gemma, const nr_rope_config* rope, nr_dtype dtype,
+                             cudaStream_t stream);
+
+/*
  * LayerNorm (no affine) fused with adaLN modulation.
  *
  * The pages name this fusion (FastVideo compare view

@@ -11,6 +11,8 @@ or ``__graft_entry__.build()``).
     rmsnorm(x, w, residual=None, eps=1e-6, gemma=False, out=None)
     qk_norm_rope(q, k, wq, wk, positions, eps=1e-6, theta=10000.0, gemma=False,
                  q_out=None, k_out=None)
+    qk_norm_rope_ex(q, k, wq, wk, positions, ..., rotary_dim=None, interleaved=False,
+                    llama3=None, mrope_sections=None, mrope_interleaved=False)
     ln_modulate(x, shift, scale, eps=1e-6, rows_per_sample=None, out=None)
     silu_and_mul(x, out=None)
     gated_residual_ln_modulate(residual, y, gate, shift, scale, eps=1e-6,
@@ -39,6 +41,20 @@ lib.nr_rmsnorm.restype = _int
 lib.nr_qk_norm_rope.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _int, _vp, _i64, _i64, _i64, _i64,
                                 _i64, _i64, _f32, _f64, _int, _int, _vp]
 lib.nr_qk_norm_rope.restype = _int
+class RopeConfig(ctypes.Structure):
+    """Mirror of nr_rope_config (include/nr.h)."""
+    _fields_ = [("rotary_dim", ctypes.c_int64), ("interleaved", ctypes.c_int32),
+                ("mrope_interleaved", ctypes.c_int32), ("theta", ctypes.c_double),
+                ("llama3_factor", ctypes.c_double), ("llama3_low_freq_factor", ctypes.c_double),
+                ("llama3_high_freq_factor", ctypes.c_double),
+                ("llama3_original_max_position", ctypes.c_double),
+                ("mrope_section", ctypes.c_int32 * 3)]
+
+
+lib.nr_qk_norm_rope_ex.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _int, _vp, _i64, _i64, _i64,
+                                   _i64, _i64, _i64, _f32, _int, ctypes.POINTER(RopeConfig), _int,
+                                   _vp]
+lib.nr_qk_norm_rope_ex.restype = _int
 lib.nr_ln_modulate.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _f32, _int, _vp]
 lib.nr_ln_modulate.restype = _int
 lib.nr_gated_residual_ln_modulate.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64,
@@ -55,8 +71,8 @@ lib.nr_version.restype = _int
 
 NR_F32 = 0
 NR_BF16 = 1
-ENTRY_POINTS = ("nr_rmsnorm", "nr_qk_norm_rope", "nr_ln_modulate", "nr_silu_and_mul",
-                "nr_gated_residual_ln_modulate",
+ENTRY_POINTS = ("nr_rmsnorm", "nr_qk_norm_rope", "nr_qk_norm_rope_ex", "nr_ln_modulate",
+                "nr_silu_and_mul", "nr_gated_residual_ln_modulate",
                 "nr_status_string", "nr_last_error_message", "nr_version")
 
 
@@ -134,6 +150,44 @@ def qk_norm_rope(q, k, wq, wk, positions, eps=1e-6, theta=10000.0, gemma=False, 
     return q_out, k_out
 
 
+def qk_norm_rope_ex(q, k, wq, wk, positions, eps=1e-6, gemma=False, rotary_dim=None,
+                    interleaved=False, theta=10000.0, llama3=None, mrope_sections=None,
+                    mrope_interleaved=False, q_out=None, k_out=None):
+    """qk_norm_rope with the RoPE variants: rotary_dim (default head_dim), GPT-J
+    interleaved pairs, Llama-3 rescale (llama3 = (factor, low_freq_factor,
+    high_freq_factor, original_max_position)) and M-RoPE (positions [3, tokens],
+    mrope_sections = (t, h, w)).  Returns (q_out, k_out)."""
+    _cuda(q, k, wq, wk, positions, q_out, k_out)
+    for t in (q, k):
+        if t.dim() != 3 or t.stride(2) != 1 or t.stride(1) != t.shape[2]:
+            raise ValueError("q/k must be [tokens, heads, head_dim] with contiguous heads")
+    want = 2 if mrope_sections is not None else 1
+    if positions.dtype != torch.int32 or positions.dim() != want or not positions.is_contiguous():
+        raise TypeError("positions must be a contiguous int32 tensor of %d dims" % want)
+    if q_out is None:
+        q_out = torch.empty_strided(q.shape, q.stride(), dtype=q.dtype, device=q.device)
+    if k_out is None:
+        k_out = torch.empty_strided(k.shape, k.stride(), dtype=k.dtype, device=k.device)
+    if q_out.stride() != q.stride() or k_out.stride() != k.stride():
+        raise ValueError("q_out/k_out must have the strides of q/k")
+    cfg = RopeConfig()
+    cfg.rotary_dim = 0 if rotary_dim is None else int(rotary_dim)
+    cfg.interleaved = int(bool(interleaved))
+    cfg.mrope_interleaved = int(bool(mrope_interleaved))
+    cfg.theta = float(theta)
+    if llama3 is not None:
+        (cfg.llama3_factor, cfg.llama3_low_freq_factor, cfg.llama3_high_freq_factor,
+         cfg.llama3_original_max_position) = (float(v) for v in llama3)
+    if mrope_sections is not None:
+        for i, v in enumerate(mrope_sections):
+            cfg.mrope_section[i] = int(v)
+    _check(lib.nr_qk_norm_rope_ex(_ptr(q_out), _ptr(k_out), _ptr(q), _ptr(k), _ptr(wq), _ptr(wk),
+                                  _dtype_code(wq), _ptr(positions), q.shape[0], q.shape[1],
+                                  k.shape[1], q.shape[2], q.stride(0), k.stride(0), float(eps),
+                                  int(bool(gemma)), ctypes.byref(cfg), _dtype_code(q), _stream(q)))
+    return q_out, k_out
+
+
 def ln_modulate(x, shift, scale, eps=1e-6, rows_per_sample=None, out=None):
     """LayerNorm (no affine) of x [rows, hidden] then * (1 + scale) + shift,
     with shift/scale [samples, hidden] (row r uses sample r // rows_per_sample).
@@ -183,6 +237,7 @@ def silu_and_mul(x, out=None):
     return out
 
 
-__all__ = ["rmsnorm", "qk_norm_rope", "ln_modulate", "silu_and_mul",
+__all__ = ["rmsnorm", "qk_norm_rope", "qk_norm_rope_ex", "RopeConfig", "ln_modulate",
+           "silu_and_mul",
            "gated_residual_ln_modulate", "NrError", "lib",
            "LIB_PATH", "ENTRY_POINTS", "NR_F32", "NR_BF16"]

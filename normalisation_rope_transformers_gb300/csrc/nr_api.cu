@@ -124,45 +124,101 @@ nr_status nr_rmsnorm(void* out, const void* x, const void* w, void* residual, in
                    "nr_rmsnorm launch");
 }
 
-nr_status nr_qk_norm_rope(void* q_out, void* k_out, const void* q, const void* k, const void* wq,
-                          const void* wk, nr_dtype w_dtype, const int32_t* positions,
-                          int64_t tokens, int64_t hq, int64_t hk, int64_t head_dim,
-                          int64_t q_tok_stride, int64_t k_tok_stride, float eps, double theta,
-                          int gemma, nr_dtype dtype, cudaStream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// Llama-3 rescale of one rotary frequency: keep short wavelengths, divide long
+// ones by `factor`, and blend linearly (in 1/wavelength) between the two bands.
+double llama3_rescale(double freq, const nr_rope_config& c) {
+  if (!(c.llama3_factor > 0.0)) return freq;
+  const double wavelength = 2.0 * M_PI / freq;
+  const double short_band = c.llama3_original_max_position / c.llama3_high_freq_factor;
+  const double long_band = c.llama3_original_max_position / c.llama3_low_freq_factor;
+  if (wavelength < short_band) return freq;
+  if (wavelength > long_band) return freq / c.llama3_factor;
+  const double blend =
+      c.llama3_high_freq_factor == c.llama3_low_freq_factor
+          ? 0.0
+          : (c.llama3_original_max_position / wavelength - c.llama3_low_freq_factor) /
+                (c.llama3_high_freq_factor - c.llama3_low_freq_factor);
+  return blend * freq + (1.0 - blend) * freq / c.llama3_factor;
+}
+
+// M-RoPE position row (0 = t, 1 = h, 2 = w) of rotary pair i.
+unsigned char mrope_row(int64_t i, const nr_rope_config& c) {
+  const int32_t* sec = c.mrope_section;
+  if (c.mrope_interleaved) {
+    const int64_t cycle = i / 3;
+    if (i % 3 == 1 && cycle < sec[1]) return 1;
+    if (i % 3 == 2 && cycle < sec[2]) return 2;
+    return 0;
+  }
+  if (i < sec[0]) return 0;
+  return i < sec[0] + sec[1] ? 1 : 2;
+}
+
+nr_status qk_norm_rope_impl(const char* fn, void* q_out, void* k_out, const void* q, const void* k,
+                            const void* wq, const void* wk, nr_dtype w_dtype,
+                            const int32_t* positions, int64_t tokens, int64_t hq, int64_t hk,
+                            int64_t head_dim, int64_t q_tok_stride, int64_t k_tok_stride,
+                            float eps, int gemma, const nr_rope_config& rope, nr_dtype dtype,
+                            cudaStream_t stream) {
   if (!valid_dtype(dtype) || !valid_dtype(w_dtype))
-    return fail(NR_ERR_DTYPE, "nr_qk_norm_rope: unknown dtype (%d, weights %d)", (int)dtype,
-                (int)w_dtype);
+    return fail(NR_ERR_DTYPE, "%s: unknown dtype (%d, weights %d)", fn, (int)dtype, (int)w_dtype);
   if (tokens < 0 || hq < 1 || hk < 0 || head_dim <= 0)
-    return fail(NR_ERR_SHAPE, "nr_qk_norm_rope: need tokens >= 0, hq >= 1, hk >= 0, head_dim > 0");
-  if (head_dim % 2 != 0) return fail(NR_ERR_SHAPE, "nr_qk_norm_rope: head_dim must be even");
+    return fail(NR_ERR_SHAPE, "%s: need tokens >= 0, hq >= 1, hk >= 0, head_dim > 0", fn);
+  if (head_dim % 2 != 0) return fail(NR_ERR_SHAPE, "%s: head_dim must be even", fn);
   const int vec = vec_elems(dtype);
   const int64_t lanes = head_dim / (2 * vec);
   if (head_dim % (2 * vec) != 0 || lanes > 32 || (lanes & (lanes - 1)) != 0)
     return fail(NR_ERR_UNSUPPORTED,
-                "nr_qk_norm_rope: head_dim %lld not supported for this dtype (bf16: 16..512, "
-                "f32: 8..256, powers of two)",
-                (long long)head_dim);
-  if (!eps_ok(eps)) return fail(NR_ERR_VALUE, "nr_qk_norm_rope: eps must be finite and >= 0");
-  if (!(isfinite(theta) && theta > 0.0))
-    return fail(NR_ERR_VALUE, "nr_qk_norm_rope: theta must be finite and > 0");
-  if (gemma != 0 && gemma != 1) return fail(NR_ERR_VALUE, "nr_qk_norm_rope: gemma must be 0 or 1");
+                "%s: head_dim %lld not supported for this dtype (bf16: 16..512, f32: 8..256, "
+                "powers of two)",
+                fn, (long long)head_dim);
+  const int64_t rot = rope.rotary_dim == 0 ? head_dim : rope.rotary_dim;
+  if (rot <= 0 || rot > head_dim || rot % 2 != 0)
+    return fail(NR_ERR_SHAPE, "%s: rotary_dim %lld must be even and in (0, head_dim]", fn,
+                (long long)rot);
+  if ((rope.interleaved != 0 && rope.interleaved != 1) ||
+      (rope.mrope_interleaved != 0 && rope.mrope_interleaved != 1))
+    return fail(NR_ERR_VALUE, "%s: interleaved flags must be 0 or 1", fn);
+  if (rot % (rope.interleaved ? vec : 2 * vec) != 0)
+    return fail(NR_ERR_UNSUPPORTED, "%s: rotary_dim %lld must be a multiple of %d", fn,
+                (long long)rot, rope.interleaved ? vec : 2 * vec);
+  if (!eps_ok(eps)) return fail(NR_ERR_VALUE, "%s: eps must be finite and >= 0", fn);
+  if (!(isfinite(rope.theta) && rope.theta > 0.0))
+    return fail(NR_ERR_VALUE, "%s: theta must be finite and > 0", fn);
+  if (!isfinite(rope.llama3_factor) ||
+      (rope.llama3_factor > 0.0 &&
+       !(rope.llama3_low_freq_factor > 0.0 &&
+         rope.llama3_high_freq_factor >= rope.llama3_low_freq_factor &&
+         rope.llama3_original_max_position > 0.0 && isfinite(rope.llama3_high_freq_factor) &&
+         isfinite(rope.llama3_original_max_position))))
+    return fail(NR_ERR_VALUE, "%s: Llama-3 factors must be positive and finite, high >= low", fn);
+  const int32_t* sec = rope.mrope_section;
+  const bool mrope = sec[0] != 0 || sec[1] != 0 || sec[2] != 0;
+  if (sec[0] < 0 || sec[1] < 0 || sec[2] < 0 ||
+      (mrope && static_cast<int64_t>(sec[0]) + sec[1] + sec[2] != rot / 2))
+    return fail(NR_ERR_SHAPE, "%s: M-RoPE sections must be >= 0 and sum to rotary_dim / 2", fn);
+  if (gemma != 0 && gemma != 1) return fail(NR_ERR_VALUE, "%s: gemma must be 0 or 1", fn);
   if (q_tok_stride < hq * head_dim || (hk > 0 && k_tok_stride < hk * head_dim))
-    return fail(NR_ERR_SHAPE, "nr_qk_norm_rope: token stride smaller than heads * head_dim");
+    return fail(NR_ERR_SHAPE, "%s: token stride smaller than heads * head_dim", fn);
   if (tokens > INT32_MAX || hq + hk > 65536)
-    return fail(NR_ERR_SHAPE, "nr_qk_norm_rope: tokens or head count too large");
+    return fail(NR_ERR_SHAPE, "%s: tokens or head count too large", fn);
   if (tokens == 0) return ok();
   if (!q_out || !q || !wq || !positions)
-    return fail(NR_ERR_NULL, "nr_qk_norm_rope: q_out, q, wq and positions must be non-NULL");
+    return fail(NR_ERR_NULL, "%s: q_out, q, wq and positions must be non-NULL", fn);
   if (hk > 0 && (!k_out || !k || !wk))
-    return fail(NR_ERR_NULL, "nr_qk_norm_rope: k_out, k and wk must be non-NULL when hk > 0");
+    return fail(NR_ERR_NULL, "%s: k_out, k and wk must be non-NULL when hk > 0", fn);
   const int es = elem_size(dtype);
   if ((q_tok_stride * es) % 16 != 0 || (hk > 0 && (k_tok_stride * es) % 16 != 0))
-    return fail(NR_ERR_ALIGN, "nr_qk_norm_rope: token strides must be multiples of 16 bytes");
+    return fail(NR_ERR_ALIGN, "%s: token strides must be multiples of 16 bytes", fn);
   if (!aligned16(q_out) || !aligned16(q) || !aligned16(wq) ||
       (hk > 0 && (!aligned16(k_out) || !aligned16(k) || !aligned16(wk))) ||
       (reinterpret_cast<uintptr_t>(positions) & 3u))
     return fail(NR_ERR_ALIGN,
-                "nr_qk_norm_rope: q/k/weights must be 16-byte aligned, positions 4-byte aligned");
+                "%s: q/k/weights must be 16-byte aligned, positions 4-byte aligned", fn);
 
   const Region rq{reinterpret_cast<uintptr_t>(q), q_tok_stride * es, hq * head_dim * es, tokens};
   const Region rqo{reinterpret_cast<uintptr_t>(q_out), q_tok_stride * es, hq * head_dim * es,
@@ -174,31 +230,65 @@ nr_status nr_qk_norm_rope(void* q_out, void* k_out, const void* q, const void* k
   const int ws = elem_size(w_dtype);
   const Region rwq = dense(wq, head_dim * ws);
   const Region rwk = dense(wk, hk > 0 ? head_dim * ws : 0);
-  const Region rpos = dense(positions, tokens * 4);
+  const Region rpos = dense(positions, (mrope ? 3 : 1) * tokens * 4);
   if ((q_out != q && overlap(rqo, rq)) || overlap(rqo, rk) || overlap(rqo, rwq) ||
       overlap(rqo, rwk) || overlap(rqo, rpos) || overlap(rqo, rko))
-    return fail(NR_ERR_ALIAS, "nr_qk_norm_rope: q_out overlaps an input or k_out");
+    return fail(NR_ERR_ALIAS, "%s: q_out overlaps an input or k_out", fn);
   if ((k_out != k && overlap(rko, rk)) || overlap(rko, rq) || overlap(rko, rwq) ||
       overlap(rko, rwk) || overlap(rko, rpos))
-    return fail(NR_ERR_ALIAS, "nr_qk_norm_rope: k_out overlaps an input");
+    return fail(NR_ERR_ALIAS, "%s: k_out overlaps an input", fn);
 
-  // turn_i = frac(freq_i / 2pi) * 2^64 with freq_i = theta^(-2i/D) in double.
-  // Positions are integers, so pos * freq_i mod 2pi = pos * frac-part mod 2pi.
+  // turn_i = frac(freq_i / 2pi) * 2^64, freq_i = theta^(-2i/rot) (Llama-3
+  // rescaled when asked), in double.  Positions are integers, so
+  // pos * freq_i mod 2pi = pos * (freq_i mod 2pi) mod 2pi.
   nr::RopeTurns turns;
-  const int64_t half = head_dim / 2;
-  for (int64_t i = 0; i < nr::kMaxHalfDim; i++) turns.turn[i] = 0;
-  for (int64_t i = 0; i < half; i++) {
-    const double freq = pow(theta, -2.0 * static_cast<double>(i) / static_cast<double>(head_dim));
+  for (int64_t i = 0; i < nr::kMaxHalfDim; i++) {
+    turns.turn[i] = 0;
+    turns.axis[i] = 0;
+  }
+  for (int64_t i = 0; i < rot / 2; i++) {
+    const double freq = llama3_rescale(
+        pow(rope.theta, -2.0 * static_cast<double>(i) / static_cast<double>(rot)), rope);
     const double turns_per_step = freq / (2.0 * M_PI);
     const double frac = turns_per_step - floor(turns_per_step);
     const double scaled = ldexp(frac, 64);
-    turns.turn[i] = scaled >= 18446744073709551616.0 ? 0ull : static_cast<unsigned long long>(scaled);
+    turns.turn[i] =
+        scaled >= 18446744073709551616.0 ? 0ull : static_cast<unsigned long long>(scaled);
+    turns.axis[i] = mrope ? mrope_row(i, rope) : 0;
   }
   return from_cuda(nr::launch_qk_norm_rope(q_out, k_out, q, k, wq, wk, w_dtype == NR_BF16,
                                            positions, tokens, hq, hk, head_dim, q_tok_stride,
-                                           k_tok_stride, eps, turns, gemma, dtype == NR_BF16,
-                                           stream),
-                   "nr_qk_norm_rope launch");
+                                           k_tok_stride, eps, turns, gemma, rot, rope.interleaved,
+                                           mrope ? 1 : 0, dtype == NR_BF16, stream),
+                   fn);
+}
+
+}  // namespace
+
+extern "C" {
+
+nr_status nr_qk_norm_rope(void* q_out, void* k_out, const void* q, const void* k, const void* wq,
+                          const void* wk, nr_dtype w_dtype, const int32_t* positions,
+                          int64_t tokens, int64_t hq, int64_t hk, int64_t head_dim,
+                          int64_t q_tok_stride, int64_t k_tok_stride, float eps, double theta,
+                          int gemma, nr_dtype dtype, cudaStream_t stream) {
+  nr_rope_config rope = {};
+  rope.theta = theta;
+  return qk_norm_rope_impl("nr_qk_norm_rope", q_out, k_out, q, k, wq, wk, w_dtype, positions,
+                           tokens, hq, hk, head_dim, q_tok_stride, k_tok_stride, eps, gemma, rope,
+                           dtype, stream);
+}
+
+nr_status nr_qk_norm_rope_ex(void* q_out, void* k_out, const void* q, const void* k,
+                             const void* wq, const void* wk, nr_dtype w_dtype,
+                             const int32_t* positions, int64_t tokens, int64_t hq, int64_t hk,
+                             int64_t head_dim, int64_t q_tok_stride, int64_t k_tok_stride,
+                             float eps, int gemma, const nr_rope_config* rope, nr_dtype dtype,
+                             cudaStream_t stream) {
+  if (rope == nullptr) return fail(NR_ERR_NULL, "nr_qk_norm_rope_ex: rope config is NULL");
+  return qk_norm_rope_impl("nr_qk_norm_rope_ex", q_out, k_out, q, k, wq, wk, w_dtype, positions,
+                           tokens, hq, hk, head_dim, q_tok_stride, k_tok_stride, eps, gemma, *rope,
+                           dtype, stream);
 }
 
 nr_status nr_ln_modulate(void* out, const void* x, const void* shift, const void* scale,

@@ -57,19 +57,21 @@ cudaError_t launch_gated_ln_modulate(void* out, void* residual, const void* y, c
 cudaError_t launch_silu_and_mul(void* out, const void* x, int64_t rows, int64_t inter,
                                 int is_bf16, cudaStream_t stream);
 
-// Per-call rotary constants: turn[i] = frac(freq_i / (2*pi)) * 2^64, freq_i =
-// theta^(-2i/head_dim), so that (pos * turn[i]) mod 2^64 is the angle pos*freq_i
-// as a fraction of a full turn.
+// Per-call rotary constants: turn[i] = frac(freq_i / (2*pi)) * 2^64 for pair i
+// (freq_i = theta^(-2i/rotary_dim), Llama-3 rescaled when asked), so that
+// (pos * turn[i]) mod 2^64 is the angle pos*freq_i as a fraction of a full
+// turn; axis[i] is the M-RoPE position row of pair i (0 without M-RoPE).
 constexpr int kMaxHalfDim = 256;
 struct RopeTurns {
   unsigned long long turn[kMaxHalfDim];
+  unsigned char axis[kMaxHalfDim];
 };
 
 cudaError_t launch_qk_norm_rope(void* q_out, void* k_out, const void* q, const void* k,
                                 const void* wq, const void* wk, int w_is_bf16,
                                 const int32_t* positions, int64_t tokens, int64_t hq, int64_t hk,
                                 int64_t head_dim, int64_t q_tok_stride, int64_t k_tok_stride,
-                                float eps, const RopeTurns& turns, int gemma, int is_bf16,
-                                cudaStream_t stream);
+                                float eps, const RopeTurns& turns, int gemma, int64_t rotary_dim,
+                                int interleaved, int mrope, int is_bf16, cudaStream_t stream);
 
 }  // namespace nr

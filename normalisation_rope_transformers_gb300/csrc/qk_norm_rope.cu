@@ -72,6 +72,11 @@ struct QkArgs {
   float eps;
   float inv_d;
   float w_add;
+  // RoPE variants (the general kernel only)
+  int rot_vec;             // 128-bit vectors of the row that are rotated (rotary_dim / N)
+  int interleaved;         // 0: rotate-half pairs (i, i + rot/2); 1: GPT-J pairs (2i, 2i + 1)
+  int mrope;               // 1: three position rows, pair i uses row axis[i]
+  int64_t pos_row_stride;  // elements between the position rows (= tokens)
 };
 
 // T: storage dtype of q/k; WT: weight dtype; L: lanes per head row
@@ -82,36 +87,43 @@ struct QkSmem {
   static constexpr int N = Vec<T>::N;
   static constexpr int HALF = L * N;
   static constexpr int D = 2 * HALF;
-  // per warp: RING slots x 32 lanes x (a, b) vectors, positions, one angle table
-  static constexpr size_t per_warp(int ring) {
-    return static_cast<size_t>(ring) * kWarp * (2 * sizeof(uint4) + sizeof(int)) +
+  // per warp: RING slots x 32 lanes x ((a, b) vectors + npos positions), one angle table
+  static constexpr size_t per_warp(int ring, int npos) {
+    return static_cast<size_t>(ring) * kWarp * (2 * sizeof(uint4) + npos * sizeof(int)) +
            HALF * sizeof(float2);
   }
-  static constexpr size_t bytes(int ring) {
-    return kQkWarps * per_warp(ring) + 2 * D * sizeof(float) +
-           HALF * sizeof(unsigned long long);
+  static constexpr size_t bytes(int ring, int npos) {
+    return kQkWarps * per_warp(ring, npos) + 2 * D * sizeof(float) +
+           HALF * sizeof(unsigned long long) + HALF;
   }
 };
 
-template <typename T, typename WT, int L, int RING>
+// GEN = false: the rotary dimension is the whole head and pairs are
+// rotate-half (the benchmark path).  GEN = true adds, at run time: a rotary
+// dimension below head_dim (lanes past the rotated block carry two normed,
+// unrotated vectors), GPT-J interleaved pairs (both members inside one vector)
+// and M-RoPE (three position rows; pair i takes row axis[i]).
+template <typename T, typename WT, int L, int RING, bool GEN>
 __global__ void __launch_bounds__(kQkThreads, NR_QK_MINB) qk_norm_rope_kernel(const QkArgs a,
                                                                   const RopeTurns turns) {
   using S = QkSmem<T, L>;
-  constexpr int N = S::N;
+  constexpr int N = Vec<T>::N;
   constexpr int HALF = S::HALF;
   constexpr int D = S::D;
   constexpr int GW = kWarp / L;  // head rows per warp iteration
+  constexpr int NPOS = GEN ? 3 : 1;
 
   extern __shared__ __align__(16) unsigned char smem[];
   const int warp = threadIdx.x / kWarp;
   const int lane32 = threadIdx.x % kWarp;
-  unsigned char* wbase = smem + warp * S::per_warp(RING);
-  uint4* ring_a = reinterpret_cast<uint4*>(wbase);                  // [RING][32]
-  uint4* ring_b = ring_a + RING * kWarp;                            // [RING][32]
-  int* ring_pos = reinterpret_cast<int*>(ring_b + RING * kWarp);    // [RING][32]
-  float2* trig = reinterpret_cast<float2*>(ring_pos + RING * kWarp);  // [HALF]
-  float* wsm = reinterpret_cast<float*>(smem + kQkWarps * S::per_warp(RING));  // [2D]
-  unsigned long long* turn_sm = reinterpret_cast<unsigned long long*>(wsm + 2 * D);
+  unsigned char* wbase = smem + warp * S::per_warp(RING, NPOS);
+  uint4* ring_a = reinterpret_cast<uint4*>(wbase);                   // [RING][32]
+  uint4* ring_b = ring_a + RING * kWarp;                             // [RING][32]
+  int* ring_pos = reinterpret_cast<int*>(ring_b + RING * kWarp);     // [RING][32][NPOS]
+  float2* trig = reinterpret_cast<float2*>(ring_pos + RING * kWarp * NPOS);  // [HALF]
+  float* wsm = reinterpret_cast<float*>(smem + kQkWarps * S::per_warp(RING, NPOS));  // [2D]
+  unsigned long long* turn_sm = reinterpret_cast<unsigned long long*>(wsm + 2 * D);  // [HALF]
+  unsigned char* axis_sm = reinterpret_cast<unsigned char*>(turn_sm + HALF);         // [HALF]
 
   const WT* wq = static_cast<const WT*>(a.wq);
   const WT* wk = static_cast<const WT*>(a.wk);
@@ -123,16 +135,37 @@ __global__ void __launch_bounds__(kQkThreads, NR_QK_MINB) qk_norm_rope_kernel(co
       wv = load_w<WT>(wk, i - D);
     wsm[i] = wv + a.w_add;
   }
-  for (int i = threadIdx.x; i < HALF; i += kQkThreads) turn_sm[i] = turns.turn[i];
+  for (int i = threadIdx.x; i < HALF; i += kQkThreads) {
+    turn_sm[i] = turns.turn[i];
+    if (GEN) axis_sm[i] = turns.axis[i];
+  }
   __syncthreads();  // the only block-level barrier
 
   const int g = lane32 / L;  // head row within the iteration
-  const int l = lane32 % L;  // vector slot within each half of the row
+  const int l = lane32 % L;  // this lane's slot in the row
   const int64_t gw = static_cast<int64_t>(blockIdx.x) * kQkWarps + warp;
   const int64_t W = static_cast<int64_t>(gridDim.x) * kQkWarps;
   if (gw >= a.tokens) return;
   const int H = a.hq + a.hk;
   const int IT = (H + GW - 1) / GW;  // iterations per token
+
+  // The two vectors of the row this lane owns.  Rotate-half: vector l and its
+  // partner l + R/2 of the rotated block (R = 2L when the whole head rotates);
+  // lanes past the rotated block take two unrotated vectors.  Interleaved:
+  // vectors l and l + L (pairs never straddle vectors).
+  int va_vec = l, vb_vec = l + L;
+  bool rotates = true;  // rotate-half lane of the rotated block
+  const int half_rot = GEN ? a.rot_vec / 2 : L;
+  const int rot_pairs = GEN ? a.rot_vec * N / 2 : HALF;
+  if (GEN && !a.interleaved) {
+    if (l < half_rot) {
+      vb_vec = l + half_rot;
+    } else {
+      va_vec = a.rot_vec + 2 * (l - half_rot);
+      vb_vec = va_vec + 1;
+      rotates = false;
+    }
+  }
 
   // A cursor walks this warp's iterations: token gw, gw + W, ... and, within
   // a token, iterations 0 .. IT-1 (rows it*GW .. it*GW + GW-1).  The copy
@@ -167,10 +200,16 @@ __global__ void __launch_bounds__(kQkThreads, NR_QK_MINB) qk_norm_rope_kernel(co
       if (locate(cp, off, is_q)) {
         const T* src = static_cast<const T*>(is_q ? a.q : a.k) + off;
         const uint4* v = reinterpret_cast<const uint4*>(src);
-        cp_async16(smem_addr(ring_a + slot * kWarp + lane32), v + l);
-        cp_async16(smem_addr(ring_b + slot * kWarp + lane32), v + L + l);
+        cp_async16(smem_addr(ring_a + slot * kWarp + lane32), v + va_vec);
+        cp_async16(smem_addr(ring_b + slot * kWarp + lane32), v + vb_vec);
       }
-      if (cp.it == 0) cp_async4(smem_addr(ring_pos + slot * kWarp + lane32), a.pos + cp.tok);
+      if (cp.it == 0) {
+#pragma unroll
+        for (int ax = 0; ax < NPOS; ax++)
+          if (ax == 0 || (GEN && a.mrope))
+            cp_async4(smem_addr(ring_pos + (slot * kWarp + lane32) * NPOS + ax),
+                      a.pos + ax * a.pos_row_stride + cp.tok);
+      }
       advance(cp);
     }
     cp_async_commit();  // possibly empty: keeps one group per iteration
@@ -186,20 +225,36 @@ __global__ void __launch_bounds__(kQkThreads, NR_QK_MINB) qk_norm_rope_kernel(co
     bool is_q;
     const bool valid = locate(cc, off, is_q);
     if (cc.it == 0) {
-      // New token: its angles, once per warp, then this lane's N pairs.
-      const unsigned long long p = static_cast<unsigned long long>(
-          static_cast<long long>(ring_pos[slot * kWarp + lane32]));
+      // New token: its angles, once per warp, then this lane's pairs.
+      long long p[NPOS];
+#pragma unroll
+      for (int ax = 0; ax < NPOS; ax++)
+        p[ax] = (ax == 0 || (GEN && a.mrope)) ? ring_pos[(slot * kWarp + lane32) * NPOS + ax] : 0;
       __syncwarp();
-      for (int i = lane32; i < HALF; i += kWarp) {
-        const unsigned long long prod = p * turn_sm[i];  // angle, in turns, mod 1
-        const int hi = static_cast<int>(prod >> 32);      // signed turn fraction * 2^32
+      for (int i = lane32; i < rot_pairs; i += kWarp) {
+        const long long pi = (GEN && a.mrope) ? (axis_sm[i] == 0 ? p[0] : axis_sm[i] == 1
+                                                     ? p[NPOS > 1 ? 1 : 0] : p[NPOS > 2 ? 2 : 0])
+                                              : p[0];
+        // the angle in turns, mod 1: exact for any int32 position
+        const unsigned long long prod = static_cast<unsigned long long>(pi) * turn_sm[i];
+        const int hi = static_cast<int>(prod >> 32);  // signed turn fraction * 2^32
         float sn, cn;
         sincospif(static_cast<float>(hi) * 0x1p-31f, &sn, &cn);  // angle = pi * hi / 2^31
         trig[i] = make_float2(cn, sn);
       }
       __syncwarp();
+      if (!GEN || !a.interleaved) {
+        if (rotates) {
 #pragma unroll
-      for (int e = 0; e < N; e++) cs[e] = trig[l * N + e];
+          for (int e = 0; e < N; e++) cs[e] = trig[l * N + e];
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < N / 2; j++) {
+          if (va_vec < a.rot_vec) cs[j] = trig[va_vec * (N / 2) + j];
+          if (vb_vec < a.rot_vec) cs[N / 2 + j] = trig[vb_vec * (N / 2) + j];
+        }
+      }
     }
     float xa[N], xb[N];
     float ss = 0.0f;
@@ -218,18 +273,43 @@ __global__ void __launch_bounds__(kQkThreads, NR_QK_MINB) qk_norm_rope_kernel(co
     ss = group_sum<L>(ss);
     if (valid) {
       const float inv = rsqrtf(ss * a.inv_d + a.eps);
-      const float* w = wsm + (is_q ? 0 : D) + l * N;
+      const float* w = wsm + (is_q ? 0 : D);
+      const float* wa = w + va_vec * N;
+      const float* wb = w + vb_vec * N;
       float oa[N], ob[N];
+      if (!GEN || (!a.interleaved && rotates)) {
 #pragma unroll
-      for (int e = 0; e < N; e++) {
-        const float na = xa[e] * inv * w[e];
-        const float nb = xb[e] * inv * w[HALF + e];
-        oa[e] = fmaf(na, cs[e].x, -nb * cs[e].y);
-        ob[e] = fmaf(na, cs[e].y, nb * cs[e].x);
+        for (int e = 0; e < N; e++) {
+          const float na = xa[e] * inv * wa[e];
+          const float nb = xb[e] * inv * wb[e];
+          oa[e] = fmaf(na, cs[e].x, -nb * cs[e].y);
+          ob[e] = fmaf(na, cs[e].y, nb * cs[e].x);
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < N; e++) {
+          oa[e] = xa[e] * inv * wa[e];
+          ob[e] = xb[e] * inv * wb[e];
+        }
+        if (a.interleaved) {
+#pragma unroll
+          for (int j = 0; j < N / 2; j++) {
+            if (va_vec < a.rot_vec) {
+              const float x0 = oa[2 * j], x1 = oa[2 * j + 1];
+              oa[2 * j] = fmaf(x0, cs[j].x, -x1 * cs[j].y);
+              oa[2 * j + 1] = fmaf(x0, cs[j].y, x1 * cs[j].x);
+            }
+            if (vb_vec < a.rot_vec) {
+              const float x0 = ob[2 * j], x1 = ob[2 * j + 1];
+              ob[2 * j] = fmaf(x0, cs[N / 2 + j].x, -x1 * cs[N / 2 + j].y);
+              ob[2 * j + 1] = fmaf(x0, cs[N / 2 + j].y, x1 * cs[N / 2 + j].x);
+            }
+          }
+        }
       }
       uint4* dst = reinterpret_cast<uint4*>(static_cast<T*>(is_q ? a.q_out : a.k_out) + off);
-      st_stream(dst + l, Vec<T>::pack(oa));
-      st_stream(dst + L + l, Vec<T>::pack(ob));
+      st_stream(dst + va_vec, Vec<T>::pack(oa));
+      st_stream(dst + vb_vec, Vec<T>::pack(ob));
     }
     advance(cc);
     slot = slot + 1 == RING ? 0 : slot + 1;
@@ -239,16 +319,16 @@ __global__ void __launch_bounds__(kQkThreads, NR_QK_MINB) qk_norm_rope_kernel(co
 
 // Resident blocks per SM of one kernel instantiation (with its dynamic shared
 // memory), cached per device; also raises the kernel's shared-memory limit.
-template <typename T, typename WT, int L, int RING>
+template <typename T, typename WT, int L, int RING, bool GEN>
 int blocks_per_sm(int device) {
   static int cached[64] = {0};
   if (device < 0 || device >= 64) return 1;
   if (cached[device] == 0) {
-    const size_t smem = QkSmem<T, L>::bytes(RING);
-    cudaFuncSetAttribute(qk_norm_rope_kernel<T, WT, L, RING>,
+    const size_t smem = QkSmem<T, L>::bytes(RING, GEN ? 3 : 1);
+    cudaFuncSetAttribute(qk_norm_rope_kernel<T, WT, L, RING, GEN>,
                          cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, qk_norm_rope_kernel<T, WT, L, RING>,
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, qk_norm_rope_kernel<T, WT, L, RING, GEN>,
                                                       kQkThreads, smem) != cudaSuccess ||
         n < 1)
       n = 1;
@@ -269,19 +349,27 @@ int sm_count(int device) {
   return cached[device];
 }
 
-template <typename T, typename WT, int L>
-cudaError_t launch_l(const QkArgs& a, const RopeTurns& turns, cudaStream_t s) {
+template <typename T, typename WT, int L, bool GEN>
+cudaError_t launch_g(const QkArgs& a, const RopeTurns& turns, cudaStream_t s) {
   constexpr int RING = NR_QK_RING;
   int device = 0;
   cudaError_t e = cudaGetDevice(&device);
   if (e != cudaSuccess) return e;
   const int64_t resident =
-      static_cast<int64_t>(sm_count(device)) * blocks_per_sm<T, WT, L, RING>(device);
+      static_cast<int64_t>(sm_count(device)) * blocks_per_sm<T, WT, L, RING, GEN>(device);
   const int64_t needed = (a.tokens + kQkWarps - 1) / kQkWarps;  // one warp per token at most
   const int64_t blocks = needed < resident ? needed : resident;
-  qk_norm_rope_kernel<T, WT, L, RING>
-      <<<dim3(static_cast<unsigned>(blocks)), kQkThreads, QkSmem<T, L>::bytes(RING), s>>>(a, turns);
+  qk_norm_rope_kernel<T, WT, L, RING, GEN><<<dim3(static_cast<unsigned>(blocks)), kQkThreads,
+                                             QkSmem<T, L>::bytes(RING, GEN ? 3 : 1), s>>>(a,
+                                                                                       turns);
   return cudaGetLastError();
+}
+
+template <typename T, typename WT, int L>
+cudaError_t launch_l(const QkArgs& a, const RopeTurns& turns, cudaStream_t s) {
+  const bool general = a.rot_vec != 2 * L || a.interleaved || a.mrope;
+  if (general) return launch_g<T, WT, L, true>(a, turns, s);
+  return launch_g<T, WT, L, false>(a, turns, s);
 }
 
 template <typename T, typename WT>
@@ -303,8 +391,8 @@ cudaError_t launch_qk_norm_rope(void* q_out, void* k_out, const void* q, const v
                                 const void* wq, const void* wk, int w_is_bf16,
                                 const int32_t* positions, int64_t tokens, int64_t hq, int64_t hk,
                                 int64_t head_dim, int64_t q_tok_stride, int64_t k_tok_stride,
-                                float eps, const RopeTurns& turns, int gemma, int is_bf16,
-                                cudaStream_t stream) {
+                                float eps, const RopeTurns& turns, int gemma, int64_t rotary_dim,
+                                int interleaved, int mrope, int is_bf16, cudaStream_t stream) {
   const int n = is_bf16 ? 8 : 4;
   const int lanes = static_cast<int>(head_dim / (2 * n));
   QkArgs a;
@@ -323,6 +411,10 @@ cudaError_t launch_qk_norm_rope(void* q_out, void* k_out, const void* q, const v
   a.eps = eps;
   a.inv_d = 1.0f / static_cast<float>(head_dim);
   a.w_add = gemma ? 1.0f : 0.0f;
+  a.rot_vec = static_cast<int>(rotary_dim / n);
+  a.interleaved = interleaved;
+  a.mrope = mrope;
+  a.pos_row_stride = tokens;
 
   if (is_bf16) {
     if (w_is_bf16) return launch_w<__nv_bfloat16, __nv_bfloat16>(a, lanes, turns, stream);

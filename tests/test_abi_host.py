@@ -18,6 +18,15 @@ A = 0x7F0000000000  # fake, 16-byte aligned "device" addresses
 MB = 1 << 20
 
 
+class RopeConfig(ctypes.Structure):
+    _fields_ = [("rotary_dim", ctypes.c_int64), ("interleaved", ctypes.c_int32),
+                ("mrope_interleaved", ctypes.c_int32), ("theta", ctypes.c_double),
+                ("llama3_factor", ctypes.c_double), ("llama3_low_freq_factor", ctypes.c_double),
+                ("llama3_high_freq_factor", ctypes.c_double),
+                ("llama3_original_max_position", ctypes.c_double),
+                ("mrope_section", ctypes.c_int32 * 3)]
+
+
 @pytest.fixture(scope="module")
 def lib(lib_path):
     L = ctypes.CDLL(lib_path)
@@ -28,6 +37,8 @@ def lib(lib_path):
                                   f32, f64, cint, cint, vp]
     L.nr_ln_modulate.argtypes = [vp, vp, vp, vp, i64, i64, i64, f32, cint, vp]
     L.nr_silu_and_mul.argtypes = [vp, vp, i64, i64, cint, vp]
+    L.nr_qk_norm_rope_ex.argtypes = [vp, vp, vp, vp, vp, vp, cint, vp, i64, i64, i64, i64, i64,
+                                     i64, f32, cint, ctypes.POINTER(RopeConfig), cint, vp]
     L.nr_gated_residual_ln_modulate.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, f32, cint,
                                                 vp]
     L.nr_status_string.argtypes = [cint]
@@ -172,3 +183,34 @@ def test_gated_residual_ln_modulate_validation(lib):
     assert gated(lib, out=A + 64 * MB) == ALIAS  # out is the residual
     assert gated(lib, y=A + 64 * MB) == ALIAS  # y is the residual
     assert gated(lib, shift=A + 16) == ALIAS  # shift inside out
+
+
+def qk_ex(lib, cfg=None, D=128, dtype=BF16, tokens=8, **over):
+    if cfg is None:
+        cfg = RopeConfig()
+        cfg.theta = 1e4
+    for k_, v in over.items():
+        if k_ == "sections":
+            for i, x in enumerate(v):
+                cfg.mrope_section[i] = x
+        else:
+            setattr(cfg, k_, v)
+    return lib.nr_qk_norm_rope_ex(A, A + 64 * MB, A + 128 * MB, A + 192 * MB, A + 256 * MB,
+                                  A + 257 * MB, F32, A + 258 * MB, tokens, 4, 2, D, 4 * D, 2 * D,
+                                  1e-6, 0, ctypes.byref(cfg), dtype, None)
+
+
+def test_qk_norm_rope_ex_validation(lib):
+    assert lib.nr_qk_norm_rope_ex(A, A, A, A, A, A, F32, A, 8, 4, 2, 128, 512, 256, 1e-6, 0,
+                                  None, BF16, None) == NULL
+    assert qk_ex(lib, tokens=0) == OK
+    assert qk_ex(lib, rotary_dim=130) == SHAPE  # above head_dim
+    assert qk_ex(lib, rotary_dim=63) == SHAPE  # odd
+    assert qk_ex(lib, rotary_dim=40) == UNSUP  # rotate-half needs multiples of 16 (bf16)
+    assert qk_ex(lib, rotary_dim=40, interleaved=1, sections=(0, 0, 0), theta=0.0) == VALUE
+    assert qk_ex(lib, interleaved=2) == VALUE
+    assert qk_ex(lib, llama3_factor=8.0) == VALUE  # factors missing
+    assert qk_ex(lib, llama3_factor=8.0, llama3_low_freq_factor=4.0, llama3_high_freq_factor=1.0,
+                 llama3_original_max_position=8192.0) == VALUE  # high < low
+    assert qk_ex(lib, sections=(16, 24, 23)) == SHAPE  # sum != 64
+    assert qk_ex(lib, sections=(-1, 33, 32)) == SHAPE

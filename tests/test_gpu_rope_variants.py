@@ -1,0 +1,85 @@
+"""GPU parity: nr_qk_norm_rope_ex (RoPE variants) against the oracle.
+
+Same tolerance as test_gpu_qk_norm_rope.py (1 bf16 ulp, or the cancellation
+allowance with K = 32).  Sources: vllm.cpp src/vt/cuda/cuda_ops.cu, "rope_neox"
+(Llama-3 rescale), "Supplied-cache RoPE" (GPT-J pairs, M-RoPE axis selection),
+"attn_qk_norm_rope_gate" (partial rotary)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from tests.gpu_util import Guarded, dev, host_bits
+from tests.parity import check_bf16, check_f32
+
+pytestmark = pytest.mark.gpu
+K_ROPE = 32
+LLAMA3 = (8.0, 1.0, 4.0, 8192.0)
+
+
+def run_variant(nr, tokens, hq, hk, D, dtype=torch.bfloat16, seed=0, pos=None, **kw):
+    q, k, wq, wk, p = synth.qk_inputs(tokens, hq, hk, D, seed, dtype, torch.float32)
+    if pos is not None:
+        p = pos
+    qg, kg = Guarded(q.shape, dtype), Guarded(k.shape, dtype)
+    nr.qk_norm_rope_ex(dev(q), dev(k), dev(wq), dev(wk), dev(p), q_out=qg.t, k_out=kg.t, **kw)
+    torch.cuda.synchronize()
+    qg.check()
+    kg.check()
+    ref = oracle.qk_norm_rope_ex(host_bits(q), host_bits(k), host_bits(wq), host_bits(wk),
+                                 p.numpy(), want_y=True, **kw)
+    for got, o, y, m, name in ((qg.t, ref[0], ref[2], ref[4], "q"),
+                               (kg.t, ref[1], ref[3], ref[5], "k")):
+        g = host_bits(got)
+        if dtype == torch.bfloat16:
+            check_bf16(g, o, y, m, k_cancel=K_ROPE, what="rope-ex " + name)
+        else:
+            check_f32(g, y, rel=1e-5, mag=m, k_cancel=K_ROPE, what="rope-ex " + name)
+    return qg.t, kg.t
+
+
+def test_defaults_match_the_plain_entry_point(nr):
+    q, k, wq, wk, p = synth.qk_inputs(40, 8, 2, 128, 3, torch.bfloat16, torch.float32)
+    a = nr.qk_norm_rope(dev(q), dev(k), dev(wq), dev(wk), dev(p))
+    b = nr.qk_norm_rope_ex(dev(q), dev(k), dev(wq), dev(wk), dev(p))
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+@pytest.mark.parametrize("D,rot", [(128, 64), (128, 32), (128, 16), (256, 64), (64, 32)])
+def test_partial_rotary(nr, D, rot):
+    run_variant(nr, 37, 4, 2, D, seed=rot, rotary_dim=rot)
+
+
+@pytest.mark.parametrize("D,rot", [(128, 128), (128, 64), (128, 24), (64, 8), (256, 256)])
+def test_interleaved_pairs(nr, D, rot):
+    run_variant(nr, 29, 3, 3, D, seed=D + rot, rotary_dim=rot, interleaved=True)
+
+
+def test_llama3_rescale_long_positions(nr):
+    pos = torch.arange(0, 131072, 131072 // 64, dtype=torch.int32)
+    run_variant(nr, 64, 4, 2, 128, seed=5, pos=pos, theta=500000.0, llama3=LLAMA3)
+
+
+@pytest.mark.parametrize("interleaved", [False, True])
+def test_mrope_sections(nr, interleaved):
+    T = 33
+    rng = np.random.default_rng(7)
+    pos = torch.from_numpy(rng.integers(0, 8192, (3, T)).astype(np.int32))
+    run_variant(nr, T, 6, 2, 128, seed=8, pos=pos, mrope_sections=(16, 24, 24),
+                mrope_interleaved=interleaved, theta=1e6)
+
+
+@pytest.mark.parametrize("kw", [dict(rotary_dim=64), dict(interleaved=True),
+                                dict(rotary_dim=32, interleaved=True)])
+def test_f32_variants(nr, kw):
+    run_variant(nr, 21, 3, 1, 64, dtype=torch.float32, seed=11, **kw)
+
+
+def test_all_at_once(nr):
+    """Partial rotary, interleaved pairs, Llama-3 and interleaved M-RoPE together."""
+    T = 17
+    rng = np.random.default_rng(12)
+    pos = torch.from_numpy(rng.integers(-1000, 100000, (3, T)).astype(np.int32))
+    run_variant(nr, T, 5, 3, 256, seed=13, pos=pos, rotary_dim=128, interleaved=True,
+                llama3=LLAMA3, mrope_sections=(24, 20, 20), mrope_interleaved=True)

@@ -516,6 +516,15 @@ def next_rows(nr, synth, torch, device, peak):
           lambda: nr.gated_residual_ln_modulate(res, y, gate, sh, sc, out=o),
           nbytes(res, y, gate, sh, sc) + nbytes(res, o), rows)
     del res, y, o
+    # RMSNorm + e4m3 quantisation with the residual add, at the dense shape
+    c = synth.ADD_RMSNORM
+    x, res, w = synth.rmsnorm_inputs(c["rows"], c["hidden"], c["seed"], torch.bfloat16)
+    x, res, w = x.to(device), res.to(device), w.to(device)
+    codes = torch.empty(x.shape, dtype=torch.uint8, device=device)
+    timed("rmsnorm_quant_fp8_bf16_8192x5120",
+          lambda: nr.rmsnorm_quant_fp8(x, w, 0.02, residual=res, codes=codes),
+          nbytes(x, w, res) + nbytes(res, codes), c["rows"])
+    del x, res, w, codes
     return out
 
 

@@ -82,6 +82,29 @@ nr_status nr_rmsnorm(void* out, const void* x, const void* w, void* residual, in
                      int64_t hidden, nr_dtype dtype, float eps, int gemma, cudaStream_t stream);
 
 /*
+ * RMSNorm (optionally with the fused residual add) followed by static FP8
+ * quantisation of its output.
+ *
+ * Follows vllm.cpp src/vt/cuda/cuda_ops.cu, "rmsnorm + static fp8 quant": the
+ * normalised value n_j of nr_rmsnorm is rounded to bf16 (nb_j, whatever the
+ * input dtype), and
+ *     code_j = e4m3_satfinite(f32(nb_j) * inv_scale),   inv_scale = 1.0f / scale
+ * with the product in f32: FP8 E4M3 (bias 7, largest finite 448, no
+ * infinities), round to nearest even, finite values beyond +-448 saturating.
+ *
+ * codes     [rows, hidden] bytes (e4m3 codes).
+ * out_bf16  [rows, hidden] bf16 copy of nb, or NULL.
+ * x, w, residual, rows, hidden, dtype, eps, gemma: as nr_rmsnorm; hidden is at
+ *           most 32768 (bf16) / 16384 (f32) here.
+ * scale     finite, > 0, with 1/scale finite.
+ * No output may overlap an input or the other output.
+ * Errors: as nr_rmsnorm.
+ */
+nr_status nr_rmsnorm_quant_fp8(void* codes, void* out_bf16, const void* x, const void* w,
+                               void* residual, int64_t rows, int64_t hidden, nr_dtype dtype,
+                               float eps, int gemma, float scale, cudaStream_t stream);
+
+/*
  * Per-head RMSNorm of Q and K followed by NeoX rotary embedding, in one pass.
  *
  * Follows vllm.cpp src/vt/cuda/cuda_ops.cu, "attn_qk_norm_rope_gate" (RMSNorm

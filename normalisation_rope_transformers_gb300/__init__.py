@@ -9,6 +9,7 @@ has not been built (``python -m normalisation_rope_transformers_gb300.build``
 or ``__graft_entry__.build()``).
 
     rmsnorm(x, w, residual=None, eps=1e-6, gemma=False, out=None)
+    rmsnorm_quant_fp8(x, w, scale, residual=None, eps=1e-6, gemma=False, out_bf16=False)
     qk_norm_rope(q, k, wq, wk, positions, eps=1e-6, theta=10000.0, gemma=False,
                  q_out=None, k_out=None)
     qk_norm_rope_ex(q, k, wq, wk, positions, ..., rotary_dim=None, interleaved=False,
@@ -38,6 +39,9 @@ _vp, _i64, _f32, _f64, _int = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_float, 
                                 ctypes.c_int)
 lib.nr_rmsnorm.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _int, _f32, _int, _vp]
 lib.nr_rmsnorm.restype = _int
+lib.nr_rmsnorm_quant_fp8.argtypes = [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _int, _f32, _int, _f32,
+                                     _vp]
+lib.nr_rmsnorm_quant_fp8.restype = _int
 lib.nr_qk_norm_rope.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _int, _vp, _i64, _i64, _i64, _i64,
                                 _i64, _i64, _f32, _f64, _int, _int, _vp]
 lib.nr_qk_norm_rope.restype = _int
@@ -71,7 +75,7 @@ lib.nr_version.restype = _int
 
 NR_F32 = 0
 NR_BF16 = 1
-ENTRY_POINTS = ("nr_rmsnorm", "nr_qk_norm_rope", "nr_qk_norm_rope_ex", "nr_ln_modulate",
+ENTRY_POINTS = ("nr_rmsnorm", "nr_rmsnorm_quant_fp8", "nr_qk_norm_rope", "nr_qk_norm_rope_ex", "nr_ln_modulate",
                 "nr_silu_and_mul", "nr_gated_residual_ln_modulate",
                 "nr_status_string", "nr_last_error_message", "nr_version")
 
@@ -122,6 +126,27 @@ def rmsnorm(x, w, residual=None, eps=1e-6, gemma=False, out=None):
     _check(lib.nr_rmsnorm(_ptr(out), _ptr(x), _ptr(w), _ptr(residual), x.shape[0], x.shape[1],
                           _dtype_code(x), float(eps), int(bool(gemma)), _stream(x)))
     return out
+
+
+def rmsnorm_quant_fp8(x, w, scale, residual=None, eps=1e-6, gemma=False, codes=None,
+                      out_bf16=False):
+    """RMSNorm of x [rows, hidden] (with the optional residual add), rounded to
+    bf16, then e4m3 codes of that value * (1/scale).  Returns codes (uint8),
+    or (codes, the bf16 values) when out_bf16 is True (or a tensor to fill)."""
+    _cuda(x, w, residual, codes)
+    if x.dim() != 2 or not x.is_contiguous():
+        raise ValueError("x must be a contiguous [rows, hidden] tensor")
+    if codes is None:
+        codes = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    nb = None
+    if out_bf16 is True:
+        nb = torch.empty(x.shape, dtype=torch.bfloat16, device=x.device)
+    elif out_bf16 is not False and out_bf16 is not None:
+        nb = out_bf16
+    _check(lib.nr_rmsnorm_quant_fp8(_ptr(codes), _ptr(nb), _ptr(x), _ptr(w), _ptr(residual),
+                                    x.shape[0], x.shape[1], _dtype_code(x), float(eps),
+                                    int(bool(gemma)), float(scale), _stream(x)))
+    return codes if nb is None else (codes, nb)
 
 
 def qk_norm_rope(q, k, wq, wk, positions, eps=1e-6, theta=10000.0, gemma=False, q_out=None,
@@ -237,7 +262,7 @@ def silu_and_mul(x, out=None):
     return out
 
 
-__all__ = ["rmsnorm", "qk_norm_rope", "qk_norm_rope_ex", "RopeConfig", "ln_modulate",
+__all__ = ["rmsnorm", "rmsnorm_quant_fp8", "qk_norm_rope", "qk_norm_rope_ex", "RopeConfig", "ln_modulate",
            "silu_and_mul",
            "gated_residual_ln_modulate", "NrError", "lib",
            "LIB_PATH", "ENTRY_POINTS", "NR_F32", "NR_BF16"]

@@ -124,6 +124,45 @@ nr_status nr_rmsnorm(void* out, const void* x, const void* w, void* residual, in
                    "nr_rmsnorm launch");
 }
 
+nr_status nr_rmsnorm_quant_fp8(void* codes, void* out_bf16, const void* x, const void* w,
+                               void* residual, int64_t rows, int64_t hidden, nr_dtype dtype,
+                               float eps, int gemma, float scale, cudaStream_t stream) {
+  const char* fn = "nr_rmsnorm_quant_fp8";
+  if (!valid_dtype(dtype)) return fail(NR_ERR_DTYPE, "%s: unknown dtype %d", fn, (int)dtype);
+  if (rows < 0 || hidden <= 0)
+    return fail(NR_ERR_SHAPE, "%s: need rows >= 0 and hidden > 0", fn);
+  if (!eps_ok(eps)) return fail(NR_ERR_VALUE, "%s: eps must be finite and >= 0", fn);
+  if (gemma != 0 && gemma != 1) return fail(NR_ERR_VALUE, "%s: gemma must be 0 or 1", fn);
+  const float inv_scale = 1.0f / scale;
+  if (!(isfinite(scale) && scale > 0.0f && isfinite(inv_scale)))
+    return fail(NR_ERR_VALUE, "%s: scale must be finite and > 0 with a finite reciprocal", fn);
+  if (rows == 0) return ok();
+  if (!codes || !x || !w) return fail(NR_ERR_NULL, "%s: codes, x and w must be non-NULL", fn);
+  const int vec = vec_elems(dtype);
+  if (hidden % vec != 0)
+    return fail(NR_ERR_UNSUPPORTED, "%s: hidden = %lld is not a multiple of %d", fn,
+                (long long)hidden, vec);
+  if (hidden / vec > nr::kQuantMaxVectors)
+    return fail(NR_ERR_UNSUPPORTED, "%s: hidden = %lld is above %lld for this dtype", fn,
+                (long long)hidden, (long long)(nr::kQuantMaxVectors * vec));
+  if (rows > INT32_MAX) return fail(NR_ERR_SHAPE, "%s: rows too large", fn);
+  if (!aligned16(codes) || !aligned16(x) || !aligned16(w) || (residual && !aligned16(residual)) ||
+      (out_bf16 && !aligned16(out_bf16)))
+    return fail(NR_ERR_ALIGN, "%s: pointers must be 16-byte aligned", fn);
+  const int64_t row_bytes = hidden * elem_size(dtype);
+  const Region rc = dense(codes, rows * hidden), rb = dense(out_bf16, out_bf16 ? rows * hidden * 2 : 0);
+  const Region rx = dense(x, rows * row_bytes), rw = dense(w, row_bytes);
+  const Region rr = dense(residual, residual ? rows * row_bytes : 0);
+  if (overlap(rc, rx) || overlap(rc, rw) || overlap(rc, rr) || overlap(rc, rb) || overlap(rb, rx) ||
+      overlap(rb, rw) || overlap(rb, rr))
+    return fail(NR_ERR_ALIAS, "%s: an output overlaps an input or the other output", fn);
+  if (overlap(rr, rx) || overlap(rr, rw))
+    return fail(NR_ERR_ALIAS, "%s: residual overlaps x or w", fn);
+  return from_cuda(nr::launch_rmsnorm_quant_fp8(codes, out_bf16, x, w, residual, rows, hidden,
+                                                dtype == NR_BF16, eps, gemma, inv_scale, stream),
+                   "nr_rmsnorm_quant_fp8 launch");
+}
+
 }  // extern "C"
 
 namespace {

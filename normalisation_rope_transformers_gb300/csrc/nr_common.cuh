@@ -8,6 +8,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -55,6 +56,14 @@ __device__ __forceinline__ void st_stream(void* p, uint4 v) {
   asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y),
                "r"(v.z), "r"(v.w)
                : "memory");
+}
+
+// Streaming stores of 8 and 4 bytes (FP8 codes, bf16 halves of f32 rows).
+__device__ __forceinline__ void st_stream8(void* p, uint2 v) {
+  asm volatile("st.global.cs.v2.u32 [%0], {%1, %2};" ::"l"(p), "r"(v.x), "r"(v.y) : "memory");
+}
+__device__ __forceinline__ void st_stream4(void* p, uint32_t v) {
+  asm volatile("st.global.cs.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
 // Plain store (for data a later pass of the same launch reads back).
@@ -164,6 +173,15 @@ struct Vec<__nv_bfloat16> {
                       pack_bf16x2(f[6], f[7]));
   }
 };
+
+// ---------------------------------------------------------------------------
+// FP8 e4m3 codes: round to nearest even, finite values beyond +-448 saturate
+// (CUDA's conversion, two values per call).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
+  return static_cast<uint32_t>(
+      __nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3));
+}
 
 // ---------------------------------------------------------------------------
 // Reductions

@@ -41,6 +41,13 @@ cudaError_t launch_rmsnorm(void* out, const void* x, const void* w, void* residu
                            int64_t hidden, int is_bf16, float eps, int gemma,
                            cudaStream_t stream);
 
+// RMSNorm + e4m3 quantisation: rows of at most kRowMaxThreads * 16 vectors.
+constexpr int64_t kQuantMaxVectors = kRowMaxThreads * 16;
+
+cudaError_t launch_rmsnorm_quant_fp8(void* codes, void* out_bf16, const void* x, const void* w,
+                                     void* residual, int64_t rows, int64_t hidden, int is_bf16,
+                                     float eps, int gemma, float inv_scale, cudaStream_t stream);
+
 cudaError_t launch_ln_modulate(void* out, const void* x, const void* shift, const void* scale,
                                int64_t rows, int64_t hidden, int64_t rows_per_sample,
                                int is_bf16, float eps, cudaStream_t stream);

@@ -18,11 +18,51 @@
 namespace nr {
 namespace {
 
+// How a normalised vector leaves the kernel.
+struct StoreOut {  // out = round_T(n)
+  void* out;
+};
+struct StoreFp8 {  // e4m3 code of f32(round_bf16(n)) * inv_scale; optionally the bf16 value too
+  uint8_t* codes;
+  __nv_bfloat16* nb;  // may be null
+  float inv_scale;
+};
+
+template <typename T>
+__device__ __forceinline__ void store_normed(const StoreOut& e, int64_t vec_index,
+                                             const float (&v)[Vec<T>::N]) {
+  st_stream(reinterpret_cast<uint4*>(e.out) + vec_index, Vec<T>::pack(v));
+}
+
+template <typename T>
+__device__ __forceinline__ void store_normed(const StoreFp8& e, int64_t vec_index,
+                                             const float (&v)[Vec<T>::N]) {
+  constexpr int N = Vec<T>::N;
+  uint32_t packed[N / 2];
+  float code_in[N];
+#pragma unroll
+  for (int j = 0; j < N / 2; j++) {
+    packed[j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);  // the bf16-rounded normed values
+    code_in[2 * j] = bf16_lo(packed[j]) * e.inv_scale;
+    code_in[2 * j + 1] = bf16_hi(packed[j]) * e.inv_scale;
+  }
+  const int64_t elem = vec_index * N;
+  if constexpr (N == 8) {
+    const uint2 c = make_uint2(e4m3x2(code_in[0], code_in[1]) | (e4m3x2(code_in[2], code_in[3]) << 16),
+                               e4m3x2(code_in[4], code_in[5]) | (e4m3x2(code_in[6], code_in[7]) << 16));
+    st_stream8(e.codes + elem, c);
+    if (e.nb != nullptr) st_stream(e.nb + elem, make_uint4(packed[0], packed[1], packed[2], packed[3]));
+  } else {
+    st_stream4(e.codes + elem, e4m3x2(code_in[0], code_in[1]) | (e4m3x2(code_in[2], code_in[3]) << 16));
+    if (e.nb != nullptr) st_stream8(e.nb + elem, make_uint2(packed[0], packed[1]));
+  }
+}
+
 // One block per row; thread t owns vectors t, t + blockDim, ..., (VPT of them).
 // PW: load the weight together with the row (saves a dependent round trip when
 // there are few rows, e.g. decode; costs registers when there are many).
-template <typename T, int VPT, bool RES, bool PW>
-__global__ void __launch_bounds__(kRowMaxThreads) rmsnorm_row_kernel(T* __restrict__ out,
+template <typename T, int VPT, bool RES, bool PW, typename EPI>
+__global__ void __launch_bounds__(kRowMaxThreads) rmsnorm_row_kernel(const EPI epi,
                                                            const T* __restrict__ x,
                                                            const T* __restrict__ w,
                                                            T* __restrict__ res, int nvec,
@@ -33,7 +73,6 @@ __global__ void __launch_bounds__(kRowMaxThreads) rmsnorm_row_kernel(T* __restri
   const int64_t row_off = static_cast<int64_t>(blockIdx.x) * nvec;  // in vectors
   const uint4* xr = reinterpret_cast<const uint4*>(x) + row_off;
   uint4* rr = RES ? reinterpret_cast<uint4*>(res) + row_off : nullptr;
-  uint4* orow = reinterpret_cast<uint4*>(out) + row_off;
   const uint4* wv = reinterpret_cast<const uint4*>(w);
 
   uint4 xv[VPT];
@@ -85,7 +124,7 @@ __global__ void __launch_bounds__(kRowMaxThreads) rmsnorm_row_kernel(T* __restri
       Vec<T>::unpack(PW ? wpre[PW ? k : 0] : ld_param(wv + vi), wf);
 #pragma unroll
       for (int e = 0; e < N; e++) v[e] = v[e] * inv * (wf[e] + w_add);
-      st_stream(orow + vi, Vec<T>::pack(v));
+      store_normed<T>(epi, row_off + vi, v);
     }
   }
 }
@@ -137,33 +176,55 @@ __global__ void __launch_bounds__(1024) rmsnorm_long_row_kernel(T* __restrict__ 
   }
 }
 
-template <typename T, int VPT, bool PW>
-cudaError_t launch_rows_pw(const RowLaunch& g, void* out, const void* x, const void* w, void* res,
-                           int64_t rows, int nvec, float hidden_f, float eps, float w_add,
-                           cudaStream_t s) {
+template <typename T, int VPT, bool PW, typename EPI>
+cudaError_t launch_rows_pw(const RowLaunch& g, const EPI& epi, const void* x, const void* w,
+                           void* res, int64_t rows, int nvec, float hidden_f, float eps,
+                           float w_add, cudaStream_t s) {
   const dim3 grid(static_cast<unsigned>(rows));
   const dim3 block(g.threads);
   if (res != nullptr)
-    rmsnorm_row_kernel<T, VPT, true, PW><<<grid, block, 0, s>>>(
-        static_cast<T*>(out), static_cast<const T*>(x), static_cast<const T*>(w),
-        static_cast<T*>(res), nvec, hidden_f, eps, w_add);
-  else
-    rmsnorm_row_kernel<T, VPT, false, PW><<<grid, block, 0, s>>>(
-        static_cast<T*>(out), static_cast<const T*>(x), static_cast<const T*>(w), nullptr, nvec,
+    rmsnorm_row_kernel<T, VPT, true, PW, EPI><<<grid, block, 0, s>>>(
+        epi, static_cast<const T*>(x), static_cast<const T*>(w), static_cast<T*>(res), nvec,
         hidden_f, eps, w_add);
+  else
+    rmsnorm_row_kernel<T, VPT, false, PW, EPI><<<grid, block, 0, s>>>(
+        epi, static_cast<const T*>(x), static_cast<const T*>(w), nullptr, nvec, hidden_f, eps,
+        w_add);
   return cudaGetLastError();
 }
 
 // Rows per launch up to which the weight is fetched together with the row.
 constexpr int64_t kPrefetchWeightRows = 1024;
 
-template <typename T, int VPT>
-cudaError_t launch_rows(const RowLaunch& g, void* out, const void* x, const void* w, void* res,
-                        int64_t rows, int nvec, float hidden_f, float eps, float w_add,
+template <typename T, int VPT, typename EPI>
+cudaError_t launch_rows(const RowLaunch& g, const EPI& epi, const void* x, const void* w,
+                        void* res, int64_t rows, int nvec, float hidden_f, float eps, float w_add,
                         cudaStream_t s) {
   if (rows <= kPrefetchWeightRows)
-    return launch_rows_pw<T, VPT, true>(g, out, x, w, res, rows, nvec, hidden_f, eps, w_add, s);
-  return launch_rows_pw<T, VPT, false>(g, out, x, w, res, rows, nvec, hidden_f, eps, w_add, s);
+    return launch_rows_pw<T, VPT, true>(g, epi, x, w, res, rows, nvec, hidden_f, eps, w_add, s);
+  return launch_rows_pw<T, VPT, false>(g, epi, x, w, res, rows, nvec, hidden_f, eps, w_add, s);
+}
+
+// Launch the row kernel for the geometry picked for this row length; false
+// when the row is too long for it (the caller then needs the multi-pass kernel).
+template <typename T, typename EPI>
+bool launch_row_kernel(cudaError_t& err, const EPI& epi, const void* x, const void* w, void* res,
+                       int64_t rows, int64_t nvec, float hidden_f, float eps, float w_add,
+                       cudaStream_t s) {
+  const RowLaunch g = pick_row_launch(nvec);
+  const int nv = static_cast<int>(nvec);
+  switch (g.vpt) {
+    case 1: err = launch_rows<T, 1>(g, epi, x, w, res, rows, nv, hidden_f, eps, w_add, s); return true;
+    case 2: err = launch_rows<T, 2>(g, epi, x, w, res, rows, nv, hidden_f, eps, w_add, s); return true;
+    case 3: err = launch_rows<T, 3>(g, epi, x, w, res, rows, nv, hidden_f, eps, w_add, s); return true;
+    case 4: err = launch_rows<T, 4>(g, epi, x, w, res, rows, nv, hidden_f, eps, w_add, s); return true;
+    case 5: err = launch_rows<T, 5>(g, epi, x, w, res, rows, nv, hidden_f, eps, w_add, s); return true;
+    case 6: err = launch_rows<T, 6>(g, epi, x, w, res, rows, nv, hidden_f, eps, w_add, s); return true;
+    case 8: err = launch_rows<T, 8>(g, epi, x, w, res, rows, nv, hidden_f, eps, w_add, s); return true;
+    case 12: err = launch_rows<T, 12>(g, epi, x, w, res, rows, nv, hidden_f, eps, w_add, s); return true;
+    case 16: err = launch_rows<T, 16>(g, epi, x, w, res, rows, nv, hidden_f, eps, w_add, s); return true;
+    default: return false;
+  }
 }
 
 template <typename T>
@@ -172,19 +233,9 @@ cudaError_t launch_typed(void* out, const void* x, const void* w, void* res, int
   const int64_t nvec = hidden / Vec<T>::N;
   const float hidden_f = static_cast<float>(hidden);
   const float w_add = gemma ? 1.0f : 0.0f;
-  const RowLaunch g = pick_row_launch(nvec);
-  switch (g.vpt) {
-    case 1: return launch_rows<T, 1>(g, out, x, w, res, rows, (int)nvec, hidden_f, eps, w_add, s);
-    case 2: return launch_rows<T, 2>(g, out, x, w, res, rows, (int)nvec, hidden_f, eps, w_add, s);
-    case 3: return launch_rows<T, 3>(g, out, x, w, res, rows, (int)nvec, hidden_f, eps, w_add, s);
-    case 4: return launch_rows<T, 4>(g, out, x, w, res, rows, (int)nvec, hidden_f, eps, w_add, s);
-    case 5: return launch_rows<T, 5>(g, out, x, w, res, rows, (int)nvec, hidden_f, eps, w_add, s);
-    case 6: return launch_rows<T, 6>(g, out, x, w, res, rows, (int)nvec, hidden_f, eps, w_add, s);
-    case 8: return launch_rows<T, 8>(g, out, x, w, res, rows, (int)nvec, hidden_f, eps, w_add, s);
-    case 12: return launch_rows<T, 12>(g, out, x, w, res, rows, (int)nvec, hidden_f, eps, w_add, s);
-    case 16: return launch_rows<T, 16>(g, out, x, w, res, rows, (int)nvec, hidden_f, eps, w_add, s);
-    default: break;
-  }
+  cudaError_t err = cudaSuccess;
+  if (launch_row_kernel<T>(err, StoreOut{out}, x, w, res, rows, nvec, hidden_f, eps, w_add, s))
+    return err;
   // Long rows: 1024 threads stride over the row twice.
   const dim3 grid(static_cast<unsigned>(rows));
   if (res != nullptr)
@@ -206,6 +257,23 @@ cudaError_t launch_rmsnorm(void* out, const void* x, const void* w, void* residu
   if (is_bf16)
     return launch_typed<__nv_bfloat16>(out, x, w, residual, rows, hidden, eps, gemma, stream);
   return launch_typed<float>(out, x, w, residual, rows, hidden, eps, gemma, stream);
+}
+
+cudaError_t launch_rmsnorm_quant_fp8(void* codes, void* out_bf16, const void* x, const void* w,
+                                     void* residual, int64_t rows, int64_t hidden, int is_bf16,
+                                     float eps, int gemma, float inv_scale, cudaStream_t stream) {
+  const StoreFp8 epi{static_cast<uint8_t*>(codes), static_cast<__nv_bfloat16*>(out_bf16),
+                     inv_scale};
+  const float hidden_f = static_cast<float>(hidden);
+  const float w_add = gemma ? 1.0f : 0.0f;
+  cudaError_t err = cudaErrorNotSupported;  // rows past the row kernel (rejected by the ABI first)
+  if (is_bf16)
+    launch_row_kernel<__nv_bfloat16>(err, epi, x, w, residual, rows, hidden / 8, hidden_f, eps,
+                                     w_add, stream);
+  else
+    launch_row_kernel<float>(err, epi, x, w, residual, rows, hidden / 4, hidden_f, eps, w_add,
+                             stream);
+  return err;
 }
 
 }  // namespace nr

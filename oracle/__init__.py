@@ -52,6 +52,13 @@ def configure(lib):
     lib.nro_bf16_value.restype = dbl
     lib.nro_bf16_round_array.argtypes = [vp, vp, i64]
     lib.nro_bf16_round_array.restype = None
+    lib.nro_e4m3_satfinite.argtypes = [ctypes.c_float]
+    lib.nro_e4m3_satfinite.restype = ctypes.c_uint8
+    lib.nro_e4m3_array.argtypes = [vp, vp, i64]
+    lib.nro_e4m3_array.restype = None
+    lib.nro_rmsnorm_quant_fp8.argtypes = [cint, i64, i64, vp, vp, vp, dbl, cint, ctypes.c_float,
+                                          vp, vp, vp, vp]
+    lib.nro_rmsnorm_quant_fp8.restype = None
     lib.nro_rmsnorm.argtypes = [cint, i64, i64, vp, vp, vp, dbl, cint, vp, vp, vp]
     lib.nro_rmsnorm.restype = None
     lib.nro_qk_norm_rope.argtypes = [cint, cint, i64, i64, i64, i64, vp, i64, vp, i64, vp, vp,
@@ -146,6 +153,31 @@ def rmsnorm(x, w, residual=None, eps=1e-6, gemma=False, want_y=False):
     lib.nro_rmsnorm(dt, rows, hidden, _ptr(x), _ptr(w), _ptr(residual), float(eps), int(gemma),
                     _ptr(out), _ptr(res_out), _ptr(y))
     return out, res_out, y
+
+
+def e4m3_array(f: np.ndarray) -> np.ndarray:
+    """e4m3 codes (uint8) of f32 values: nearest, ties to even, saturating at +-448."""
+    f = np.ascontiguousarray(f, dtype=np.float32)
+    codes = np.empty(f.shape, np.uint8)
+    _load().nro_e4m3_array(_ptr(f), _ptr(codes), f.size)
+    return codes
+
+
+def rmsnorm_quant_fp8(x, w, scale, residual=None, eps=1e-6, gemma=False, want_y=False):
+    """RMSNorm (optionally with the residual add), its bf16 rounding nb and the
+    e4m3 code of f32(nb) * (1/scale).  Returns (codes, nb, residual_out, y)."""
+    lib = _load()
+    x, w, residual = _c(x), _c(w), _c(residual)
+    dt = _dtype_code(x)
+    rows, hidden = x.shape
+    codes = np.empty(x.shape, np.uint8)
+    nb = np.empty(x.shape, np.uint16)
+    res_out = None if residual is None else np.empty_like(residual)
+    y = np.empty(x.shape, np.float64) if want_y else None
+    lib.nro_rmsnorm_quant_fp8(dt, rows, hidden, _ptr(x), _ptr(w), _ptr(residual), float(eps),
+                              int(gemma), float(scale), _ptr(codes), _ptr(nb), _ptr(res_out),
+                              _ptr(y))
+    return codes, nb, res_out, y
 
 
 def qk_norm_rope(q, k, wq, wk, positions, eps=1e-6, theta=10000.0, gemma=False, want_y=False):

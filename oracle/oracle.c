@@ -143,6 +143,71 @@ void nro_rmsnorm(int dtype, int64_t rows, int64_t hidden, const void* x, const v
 }
 
 /* ------------------------------------------------------------------------ */
+/* RMSNorm + static FP8 (e4m3) quantisation ([VT] "rmsnorm + static fp8      */
+/* quant"): the RMSNorm above, its output rounded to bf16 (nb), and the code  */
+/*   code_j = e4m3_satfinite( f32(nb_j) * inv_scale ),  inv_scale = 1 / scale  */
+/* where inv_scale and the product are f32 operations (the page computes the  */
+/* code in f32 from the bf16-rounded value), so the code is decided in f32 on */
+/* both sides.                                                                */
+/*                                                                            */
+/* e4m3: 1 sign bit, 4 exponent bits (bias 7), 3 mantissa bits, subnormal     */
+/* step 2^-9, no infinities (0x7f/0xff are NaN), largest finite 448.  Values  */
+/* round to nearest, ties to even; finite values beyond +-448 saturate to     */
+/* +-448.                                                                     */
+/* ------------------------------------------------------------------------ */
+uint8_t nro_e4m3_satfinite(float f) {
+  if (isnan(f)) return (uint8_t)0x7F;
+  const uint8_t sign = signbit(f) ? (uint8_t)0x80 : (uint8_t)0;
+  const double a = fabs((double)f);
+  if (a == 0.0) return sign;
+  int e;
+  frexp(a, &e); /* a in [2^(e-1), 2^e) */
+  int quantum_exp = (e - 1) - 3;
+  if (quantum_exp < -9) quantum_exp = -9;
+  double r = ldexp(nearbyint(ldexp(a, -quantum_exp)), quantum_exp);
+  if (r > 448.0) r = 448.0;
+  if (r < 0x1p-6) return (uint8_t)(sign | (uint8_t)ldexp(r, 9)); /* subnormal: r / 2^-9 */
+  frexp(r, &e);
+  const int exp_field = (e - 1) + 7;
+  const int mant = (int)(ldexp(r, -(e - 1)) * 8.0) - 8; /* (r / 2^(e-1) - 1) * 8 */
+  return (uint8_t)(sign | (uint8_t)(exp_field << 3) | (uint8_t)mant);
+}
+
+void nro_e4m3_array(const float* f, uint8_t* codes, int64_t n) {
+  for (int64_t i = 0; i < n; i++) codes[i] = nro_e4m3_satfinite(f[i]);
+}
+
+void nro_rmsnorm_quant_fp8(int dtype, int64_t rows, int64_t hidden, const void* x, const void* w,
+                           const void* res_in, double eps, int gemma, float scale,
+                           uint8_t* out_fp8, uint16_t* out_bf16, void* res_out, double* y) {
+  const float inv_scale = 1.0f / scale;
+  for (int64_t r = 0; r < rows; r++) {
+    const int64_t base = r * hidden;
+    double sum_sq = 0.0;
+    for (int64_t j = 0; j < hidden; j++) {
+      double v = load(dtype, x, base + j);
+      if (res_in != NULL) {
+        v = round_to(dtype, v + load(dtype, res_in, base + j));
+        store(dtype, res_out, base + j, v);
+      }
+      sum_sq += v * v;
+    }
+    const double inv = 1.0 / sqrt(sum_sq / (double)hidden + eps);
+    for (int64_t j = 0; j < hidden; j++) {
+      const double v = (res_in != NULL) ? load(dtype, res_out, base + j) : load(dtype, x, base + j);
+      double wj = load(dtype, w, j);
+      if (gemma) wj += 1.0;
+      const double yj = v * inv * wj;
+      const uint16_t nb = nro_bf16_round(yj);
+      const float t = (float)nro_bf16_value(nb) * inv_scale; /* f32 multiply */
+      out_fp8[base + j] = nro_e4m3_satfinite(t);
+      if (out_bf16 != NULL) out_bf16[base + j] = nb;
+      if (y != NULL) y[base + j] = yj;
+    }
+  }
+}
+
+/* ------------------------------------------------------------------------ */
 /* Per-head Q/K RMSNorm followed by NeoX RoPE ([VT] "attn_qk_norm_rope_gate",  */
 /* "rope_neox").  For token t and head h of a tensor with its own norm weight */
 /* w (one vector of length D, shared by all heads):                           */

@@ -37,6 +37,7 @@ def lib(lib_path):
                                   f32, f64, cint, cint, vp]
     L.nr_ln_modulate.argtypes = [vp, vp, vp, vp, i64, i64, i64, f32, cint, vp]
     L.nr_silu_and_mul.argtypes = [vp, vp, i64, i64, cint, vp]
+    L.nr_rmsnorm_quant_fp8.argtypes = [vp, vp, vp, vp, vp, i64, i64, cint, f32, cint, f32, vp]
     L.nr_qk_norm_rope_ex.argtypes = [vp, vp, vp, vp, vp, vp, cint, vp, i64, i64, i64, i64, i64,
                                      i64, f32, cint, ctypes.POINTER(RopeConfig), cint, vp]
     L.nr_gated_residual_ln_modulate.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, f32, cint,
@@ -214,3 +215,24 @@ def test_qk_norm_rope_ex_validation(lib):
                  llama3_original_max_position=8192.0) == VALUE  # high < low
     assert qk_ex(lib, sections=(16, 24, 23)) == SHAPE  # sum != 64
     assert qk_ex(lib, sections=(-1, 33, 32)) == SHAPE
+
+
+def quant(lib, codes=A, nb=A + 64 * MB, x=A + 128 * MB, w=A + 192 * MB, res=None, rows=4,
+          hidden=64, dtype=BF16, eps=1e-6, gemma=0, scale=0.5):
+    return lib.nr_rmsnorm_quant_fp8(codes, nb, x, w, res, rows, hidden, dtype, eps, gemma, scale,
+                                    None)
+
+
+def test_rmsnorm_quant_fp8_validation(lib):
+    assert quant(lib, rows=0, codes=None, x=None, w=None) == OK
+    assert quant(lib, dtype=2) == DTYPE
+    assert quant(lib, scale=0.0) == VALUE
+    assert quant(lib, scale=float("inf")) == VALUE
+    assert quant(lib, scale=1e-40) == VALUE  # reciprocal overflows
+    assert quant(lib, codes=None) == NULL
+    assert quant(lib, hidden=12) == UNSUP
+    assert quant(lib, hidden=32776) == UNSUP  # beyond 32768 for bf16
+    assert quant(lib, codes=A + 8) == ALIGN
+    assert quant(lib, codes=A + 128 * MB) == ALIAS  # codes over x
+    assert quant(lib, nb=A) == ALIAS  # the two outputs
+    assert quant(lib, res=A + 128 * MB) == ALIAS  # residual is x

@@ -71,6 +71,14 @@ MUTANTS = [
      "if (i % 3 == 1 && i / 3 <= sections[1]) return 1;"),
     ("rope-ex: mrope contiguous sections", "if (i < sections[0] + sections[1]) return 1;",
      "if (i < sections[1]) return 1;"),
+    ("e4m3 exponent bias 8", "const int exp_field = (e - 1) + 7;", "const int exp_field = (e - 1) + 8;"),
+    ("e4m3 no saturation", "if (r > 448.0) r = 448.0;", "if (r > 480.0) r = 448.0;"),
+    ("e4m3 ties away", "double r = ldexp(nearbyint(ldexp(a, -quantum_exp)), quantum_exp);",
+     "double r = ldexp(floor(ldexp(a, -quantum_exp) + 0.5), quantum_exp);"),
+    ("fp8 code from the unrounded value", "const float t = (float)nro_bf16_value(nb) * inv_scale;",
+     "const float t = (float)yj * inv_scale;"),
+    ("fp8 scale applied the wrong way", "const float inv_scale = 1.0f / scale;",
+     "const float inv_scale = scale;"),
     ("silu exponent sign", "a / (1.0 + exp(-a)) * b", "a / (1.0 + exp(a)) * b"),
     ("silu gate and up swapped", "const double a = load(dtype, x, r * 2 * inter + j);\n      const double b = load(dtype, x, r * 2 * inter + inter + j);",
      "const double b = load(dtype, x, r * 2 * inter + j);\n      const double a = load(dtype, x, r * 2 * inter + inter + j);"),

@@ -96,6 +96,32 @@ def test_bf16_rounding_exact_brute_force_on_doubles():
         assert ours[i] == _nearest_bf16_exact(float(d[i])), d[i]
 
 
+def test_e4m3_golden_cases():
+    n = 0
+    with open(os.path.join(GOLDEN, "e4m3_rounding.txt")) as f:
+        for line in f:
+            if not line.strip() or line.startswith("#"):
+                continue
+            hexval, code, _ = line.split(None, 2)
+            v = np.array([float.fromhex(hexval)], np.float32)
+            assert oracle.e4m3_array(v)[0] == int(code, 16), line
+            n += 1
+    assert n >= 12
+
+
+def test_e4m3_matches_torch_within_range():
+    """Inside +-448 the oracle's e4m3 rounding agrees with torch's f32 ->
+    float8_e4m3fn conversion (a library round-to-nearest-even)."""
+    if not hasattr(torch, "float8_e4m3fn"):
+        pytest.skip("torch without float8_e4m3fn")
+    rng = np.random.default_rng(17)
+    v = np.concatenate([rng.uniform(-448, 448, 20000), rng.standard_normal(20000) * 2.0 ** -7,
+                        np.arange(-448, 448.01, 1 / 64.0)]).astype(np.float32)
+    ours = oracle.e4m3_array(v)
+    ref = torch.from_numpy(v).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(ours, ref)
+
+
 # --------------------------------------------------------------------------
 # residual add
 # --------------------------------------------------------------------------
@@ -239,6 +265,30 @@ def test_rmsnorm_brute_force_4x8():
         for j in range(8):
             exact = vals[j] * inv * (mpmath.mpf(float(wv[j])) + 1)
             assert abs(y[i, j] - float(exact)) <= 4e-16 * abs(float(exact))
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_rmsnorm_quant_fp8_composition(dtype):
+    """The fused op equals RMSNorm (pinned above) rounded to bf16, then the
+    e4m3 code of the f32 product with 1/scale (numpy f32 arithmetic and
+    torch's e4m3 conversion, for codes inside the range)."""
+    x, res, w = synth.rmsnorm_inputs(8, 256, 14, dtype)
+    scale = 0.0123
+    codes, nb, r_out, y = oracle.rmsnorm_quant_fp8(synth.to_oracle(x), synth.to_oracle(w), scale,
+                                                   residual=synth.to_oracle(res), gemma=True,
+                                                   want_y=True)
+    o, r2, y2 = oracle.rmsnorm(synth.to_oracle(x), synth.to_oracle(w),
+                               residual=synth.to_oracle(res), gemma=True, want_y=True)
+    assert np.array_equal(r_out, r2) and np.array_equal(y, y2)
+    assert np.array_equal(nb, oracle.bf16_round_array(y2))
+    t = bf16_to_f64(nb).astype(np.float32) * (np.float32(1.0) / np.float32(scale))
+    assert np.array_equal(codes, oracle.e4m3_array(t))
+    if hasattr(torch, "float8_e4m3fn"):
+        inside = np.abs(t) <= 448
+        ref = torch.from_numpy(t).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+        assert np.array_equal(codes[inside], ref[inside])
+        assert inside.mean() > 0.5 and (~inside).any()  # both regimes exercised
+        assert np.all(codes[~inside] & 0x7F == 0x7E)
 
 
 # --------------------------------------------------------------------------

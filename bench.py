@@ -525,6 +525,11 @@ def next_rows(nr, synth, torch, device, peak):
           lambda: nr.rmsnorm_quant_fp8(x, w, 0.02, residual=res, codes=codes),
           nbytes(x, w, res) + nbytes(res, codes), c["rows"])
     del x, res, w, codes
+    # tanh-GELU gate times up, prefill-sized: 8192 tokens, intermediate 3 * 5120
+    g = synth.silu_inputs(8192, 3 * 5120, 6, torch.bfloat16).to(device)
+    o = torch.empty((8192, 3 * 5120), dtype=torch.bfloat16, device=device)
+    timed("gelu_and_mul_bf16_8192x30720", lambda: nr.gelu_and_mul(g, out=o), nbytes(g, o), 8192)
+    del g, o
     return out
 
 

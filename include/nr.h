@@ -1,12 +1,21 @@
 /*
  * nr.h -- C ABI of the fused row-normalisation library (libnormrope.so).
  *
- * Four ops that sit between a transformer's GEMMs, as hand-written CUDA
- * kernels for sm_103a:
- *   nr_rmsnorm        RMSNorm, optionally with the fused residual add (gemma w+1)
- *   nr_qk_norm_rope   per-head Q/K RMSNorm fused with NeoX rotary embedding
- *   nr_ln_modulate    LayerNorm (no affine) fused with DiT adaLN modulation
- *   nr_silu_and_mul   silu(gate) * up
+ * Ops that sit between a transformer's GEMMs, as hand-written CUDA kernels
+ * for sm_103a:
+ *   nr_rmsnorm                      RMSNorm, optionally with the fused residual
+ *                                   add (gemma w+1)
+ *   nr_rmsnorm_quant_fp8            the same, writing static-scale FP8 e4m3 codes
+ *   nr_qk_norm_rope                 per-head Q/K RMSNorm fused with NeoX rotary
+ *                                   embedding
+ *   nr_qk_norm_rope_ex              the same with RoPE variants (partial rotary,
+ *                                   GPT-J pairs, Llama-3 rescale, M-RoPE)
+ *   nr_ln_modulate                  LayerNorm (no affine) fused with DiT adaLN
+ *                                   modulation
+ *   nr_gated_residual_ln_modulate   residual += gate * y, then LayerNorm +
+ *                                   modulation of the new residual
+ *   nr_silu_and_mul                 silu(gate) * up
+ *   nr_gelu_and_mul                 gelu_tanh(gate) * up
  *
  * Conventions shared by every entry point
  *   - Pointers are DEVICE pointers (CUDA global memory) owned by the caller; the
@@ -251,6 +260,21 @@ nr_status nr_gated_residual_ln_modulate(void* out, void* residual, const void* y
  * Errors: as nr_rmsnorm.
  */
 nr_status nr_silu_and_mul(void* out, const void* x, int64_t rows, int64_t inter, nr_dtype dtype,
+                          cudaStream_t stream);
+
+/*
+ * gelu_and_mul: out[r, j] = gelu_tanh(x[r, j]) * x[r, inter + j], with the
+ * tanh form of GELU
+ *     gelu_tanh(a) = a/2 * (1 + tanh(sqrt(2/pi) * (a + 0.044715 a^3))).
+ *
+ * Follows vllm.cpp src/vt/cuda/cuda_ops.cu, "gelu_and_mul" (the gated MLP of
+ * Gemma-family models; same layout as silu_and_mul).  Evaluated as
+ * a * sigmoid(2z), which equals the formula above and keeps its relative
+ * accuracy for negative gates.
+ *
+ * Arguments, layout and errors: as nr_silu_and_mul.
+ */
+nr_status nr_gelu_and_mul(void* out, const void* x, int64_t rows, int64_t inter, nr_dtype dtype,
                           cudaStream_t stream);
 
 /* Static, human-readable name of a status code. */

@@ -16,6 +16,7 @@ or ``__graft_entry__.build()``).
                     llama3=None, mrope_sections=None, mrope_interleaved=False)
     ln_modulate(x, shift, scale, eps=1e-6, rows_per_sample=None, out=None)
     silu_and_mul(x, out=None)
+    gelu_and_mul(x, out=None)
     gated_residual_ln_modulate(residual, y, gate, shift, scale, eps=1e-6,
                                rows_per_sample=None, out=None)
 """
@@ -66,6 +67,8 @@ lib.nr_gated_residual_ln_modulate.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i64
 lib.nr_gated_residual_ln_modulate.restype = _int
 lib.nr_silu_and_mul.argtypes = [_vp, _vp, _i64, _i64, _int, _vp]
 lib.nr_silu_and_mul.restype = _int
+lib.nr_gelu_and_mul.argtypes = [_vp, _vp, _i64, _i64, _int, _vp]
+lib.nr_gelu_and_mul.restype = _int
 lib.nr_status_string.argtypes = [_int]
 lib.nr_status_string.restype = ctypes.c_char_p
 lib.nr_last_error_message.argtypes = []
@@ -76,7 +79,7 @@ lib.nr_version.restype = _int
 NR_F32 = 0
 NR_BF16 = 1
 ENTRY_POINTS = ("nr_rmsnorm", "nr_rmsnorm_quant_fp8", "nr_qk_norm_rope", "nr_qk_norm_rope_ex", "nr_ln_modulate",
-                "nr_silu_and_mul", "nr_gated_residual_ln_modulate",
+                "nr_silu_and_mul", "nr_gelu_and_mul", "nr_gated_residual_ln_modulate",
                 "nr_status_string", "nr_last_error_message", "nr_version")
 
 
@@ -250,19 +253,28 @@ def gated_residual_ln_modulate(residual, y, gate, shift, scale, eps=1e-6, rows_p
     return out
 
 
-def silu_and_mul(x, out=None):
-    """silu(x[:, :I]) * x[:, I:] for x [rows, 2I].  Returns out [rows, I]."""
+def _act_and_mul(fn, x, out):
     _cuda(x, out)
     if x.dim() != 2 or not x.is_contiguous() or x.shape[1] % 2:
         raise ValueError("x must be a contiguous [rows, 2*inter] tensor")
     inter = x.shape[1] // 2
     if out is None:
         out = torch.empty((x.shape[0], inter), dtype=x.dtype, device=x.device)
-    _check(lib.nr_silu_and_mul(_ptr(out), _ptr(x), x.shape[0], inter, _dtype_code(x), _stream(x)))
+    _check(fn(_ptr(out), _ptr(x), x.shape[0], inter, _dtype_code(x), _stream(x)))
     return out
 
 
+def silu_and_mul(x, out=None):
+    """silu(x[:, :I]) * x[:, I:] for x [rows, 2I].  Returns out [rows, I]."""
+    return _act_and_mul(lib.nr_silu_and_mul, x, out)
+
+
+def gelu_and_mul(x, out=None):
+    """gelu_tanh(x[:, :I]) * x[:, I:] for x [rows, 2I].  Returns out [rows, I]."""
+    return _act_and_mul(lib.nr_gelu_and_mul, x, out)
+
+
 __all__ = ["rmsnorm", "rmsnorm_quant_fp8", "qk_norm_rope", "qk_norm_rope_ex", "RopeConfig", "ln_modulate",
-           "silu_and_mul",
+           "silu_and_mul", "gelu_and_mul",
            "gated_residual_ln_modulate", "NrError", "lib",
            "LIB_PATH", "ENTRY_POINTS", "NR_F32", "NR_BF16"]

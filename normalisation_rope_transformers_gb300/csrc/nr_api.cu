@@ -397,26 +397,43 @@ nr_status nr_gated_residual_ln_modulate(void* out, void* residual, const void* y
                    "nr_gated_residual_ln_modulate launch");
 }
 
-nr_status nr_silu_and_mul(void* out, const void* x, int64_t rows, int64_t inter, nr_dtype dtype,
-                          cudaStream_t stream) {
-  if (!valid_dtype(dtype)) return fail(NR_ERR_DTYPE, "nr_silu_and_mul: unknown dtype %d", (int)dtype);
-  if (rows < 0 || inter <= 0)
-    return fail(NR_ERR_SHAPE, "nr_silu_and_mul: need rows >= 0 and inter > 0");
+}  // extern "C"
+
+namespace {
+
+nr_status act_and_mul(const char* fn, int gelu, void* out, const void* x, int64_t rows,
+                      int64_t inter, nr_dtype dtype, cudaStream_t stream) {
+  if (!valid_dtype(dtype)) return fail(NR_ERR_DTYPE, "%s: unknown dtype %d", fn, (int)dtype);
+  if (rows < 0 || inter <= 0) return fail(NR_ERR_SHAPE, "%s: need rows >= 0 and inter > 0", fn);
   if (rows == 0) return ok();
-  if (!out || !x) return fail(NR_ERR_NULL, "nr_silu_and_mul: out and x must be non-NULL");
+  if (!out || !x) return fail(NR_ERR_NULL, "%s: out and x must be non-NULL", fn);
   const int vec = vec_elems(dtype);
   if (inter % vec != 0)
-    return fail(NR_ERR_UNSUPPORTED, "nr_silu_and_mul: inter = %lld is not a multiple of %d",
+    return fail(NR_ERR_UNSUPPORTED, "%s: inter = %lld is not a multiple of %d", fn,
                 (long long)inter, vec);
-  if (inter / vec > INT32_MAX / 2)
-    return fail(NR_ERR_SHAPE, "nr_silu_and_mul: inter too large");
+  if (inter / vec > INT32_MAX / 2) return fail(NR_ERR_SHAPE, "%s: inter too large", fn);
   if (!aligned16(out) || !aligned16(x))
-    return fail(NR_ERR_ALIGN, "nr_silu_and_mul: pointers must be 16-byte aligned");
+    return fail(NR_ERR_ALIGN, "%s: pointers must be 16-byte aligned", fn);
   const int64_t es = elem_size(dtype);
   if (overlap(dense(out, rows * inter * es), dense(x, rows * 2 * inter * es)))
-    return fail(NR_ERR_ALIAS, "nr_silu_and_mul: out overlaps x");
-  return from_cuda(nr::launch_silu_and_mul(out, x, rows, inter, dtype == NR_BF16, stream),
-                   "nr_silu_and_mul launch");
+    return fail(NR_ERR_ALIAS, "%s: out overlaps x", fn);
+  const cudaError_t e = gelu ? nr::launch_gelu_and_mul(out, x, rows, inter, dtype == NR_BF16, stream)
+                             : nr::launch_silu_and_mul(out, x, rows, inter, dtype == NR_BF16, stream);
+  return from_cuda(e, fn);
+}
+
+}  // namespace
+
+extern "C" {
+
+nr_status nr_silu_and_mul(void* out, const void* x, int64_t rows, int64_t inter, nr_dtype dtype,
+                          cudaStream_t stream) {
+  return act_and_mul("nr_silu_and_mul", 0, out, x, rows, inter, dtype, stream);
+}
+
+nr_status nr_gelu_and_mul(void* out, const void* x, int64_t rows, int64_t inter, nr_dtype dtype,
+                          cudaStream_t stream) {
+  return act_and_mul("nr_gelu_and_mul", 1, out, x, rows, inter, dtype, stream);
 }
 
 }  // extern "C"

@@ -64,6 +64,9 @@ cudaError_t launch_gated_ln_modulate(void* out, void* residual, const void* y, c
 cudaError_t launch_silu_and_mul(void* out, const void* x, int64_t rows, int64_t inter,
                                 int is_bf16, cudaStream_t stream);
 
+cudaError_t launch_gelu_and_mul(void* out, const void* x, int64_t rows, int64_t inter,
+                                int is_bf16, cudaStream_t stream);
+
 // Per-call rotary constants: turn[i] = frac(freq_i / (2*pi)) * 2^64 for pair i
 // (freq_i = theta^(-2i/rotary_dim), Llama-3 rescaled when asked), so that
 // (pos * turn[i]) mod 2^64 is the angle pos*freq_i as a fraction of a full

@@ -1,13 +1,15 @@
-// silu_and_mul for sm_103a: out[r, j] = silu(x[r, j]) * x[r, inter + j].
-//
-// Follows vllm.cpp src/vt/cuda/cuda_ops.cu, "silu_and_mul" (gate = first half
-// of the row, up = second half, f32 math).  Design: a 2-D grid (vector column
-// blocks x rows) so no thread divides a flat index; each thread moves UNROLL
-// 128-bit vectors of gate and of up, issuing every load before any math.  The
-// exponential and division are the cheap hardware forms for bf16 outputs
-// (see silu<T> below), so the kernel stays memory-bound.
+// Gated activations for sm_103a: out[r, j] = act(x[r, j]) * x[r, inter + j]
+// with act = silu (vllm.cpp src/vt/cuda/cuda_ops.cu, "silu_and_mul") or the
+// tanh form of GELU ("gelu_and_mul"); gate = first half of the row, up =
+// second half, f32 math.  Design: a 2-D grid (vector column blocks x rows) so
+// no thread divides a flat index; each thread moves UNROLL 128-bit vectors of
+// gate and of up, issuing every load before any math.  Both activations are
+// a * sigmoid(s * z(a)) evaluated in an overflow-free form (below); bf16
+// outputs use the hardware exponential and reciprocal, so the kernel stays
+// memory-bound.
 #include "nr_common.cuh"
 #include "nr_internal.h"
+
 
 namespace nr {
 namespace {
@@ -34,10 +36,60 @@ __device__ __forceinline__ float silu<float>(float a) {
   return a / (1.0f + expf(-a));
 }
 
+// tanh-GELU: 0.5 a (1 + tanh(z)), z = sqrt(2/pi) (a + 0.044715 a^3), computed
+// as a * sigmoid(2z) (the same function: (1 + tanh z) / 2 = sigmoid(2z)) with
+// the overflow-free sigmoid, which keeps full relative accuracy where
+// 1 + tanh(z) would cancel.  bf16 outputs: 2z in plain f32, exp2f and a fast
+// reciprocal, whose errors stay far inside one bf16 ulp.
+template <typename T>
+__device__ __forceinline__ float gelu_tanh(float a) {
+  const float two_z = 1.5957691216057308f * fmaf(0.044715f * a, a * a, a);  // 2 sqrt(2/pi) (...)
+  const float t = exp2f(-fabsf(two_z) * 1.4426950408889634f);
+  const float r = __fdividef(1.0f, 1.0f + t);
+  return a * (two_z >= 0.0f ? r : t * r);
+}
+
+// f32 outputs.  For a < 0 the result is about a * e^{2z}, so a relative error
+// d in 2z becomes |2z| * d in the result: with 2z rounded a few times in f32
+// that is ~2e-5 at 2z = -70, too much for a 1e-5 relative tolerance.  So
+// 2z = a (kK + kKc a^2), kK = 2 sqrt(2/pi), kKc = 0.044715 kK, is carried as
+// an unevaluated sum r + r_lo of two floats: each constant split into two
+// floats, products made error-free with fmaf, the sum with Knuth's TwoSum.
+// Then e^{-|2z|} = e^{-|r|} (1 -+ r_lo) to first order (|r_lo| <= 5e-6).
+// The gate is clamped to +-20 inside the sigmoid only: beyond it sigmoid(2z)
+// is 1 or 0 exactly in f32, and a^2 stays finite.
+template <>
+__device__ __forceinline__ float gelu_tanh<float>(float a_in) {
+  constexpr float kKHi = 0x1.988454p+0f, kKLo = -0x1.857936p-25f;
+  constexpr float kKcHi = 0x1.2444f2p-4f, kKcLo = 0x1.49b16ap-29f;
+  const float a = fminf(fmaxf(a_in, -20.0f), 20.0f);
+  const float s = a * a, s_lo = fmaf(a, a, -s);  // a^2 = s + s_lo
+  const float p = kKcHi * s;
+  const float p_lo = fmaf(kKcHi, s, -p) + fmaf(kKcHi, s_lo, kKcLo * s);  // kKc a^2
+  const float q = kKHi + p;  // TwoSum(kKHi, p)
+  const float qb = q - kKHi;
+  const float q_lo = ((kKHi - (q - qb)) + (p - qb)) + (kKLo + p_lo);
+  const float r = a * q;
+  const float r_lo = fmaf(a, q, -r) + a * q_lo;  // 2z = r + r_lo
+  const float t0 = expf(-fabsf(r));
+  const float t = fmaf(t0, r >= 0.0f ? -r_lo : r_lo, t0);
+  return a_in * (r >= 0.0f ? 1.0f / (1.0f + t) : t / (1.0f + t));
+}
+
+enum class Act { kSilu, kGeluTanh };
+
+template <typename T, Act ACT>
+__device__ __forceinline__ float activate(float a) {
+  if constexpr (ACT == Act::kSilu)
+    return silu<T>(a);
+  else
+    return gelu_tanh<T>(a);
+}
+
 constexpr unsigned kMaxGridY = 65535;
 
-template <typename T, int UNROLL>
-__global__ void __launch_bounds__(kSiluThreads) silu_and_mul_kernel(T* __restrict__ out,
+template <typename T, int UNROLL, Act ACT>
+__global__ void __launch_bounds__(kSiluThreads) act_and_mul_kernel(T* __restrict__ out,
                                                                     const T* __restrict__ x,
                                                                     int64_t rows, int ivec) {
   constexpr int N = Vec<T>::N;
@@ -63,39 +115,45 @@ __global__ void __launch_bounds__(kSiluThreads) silu_and_mul_kernel(T* __restric
         Vec<T>::unpack(gv[u], a);
         Vec<T>::unpack(uv[u], b);
 #pragma unroll
-        for (int e = 0; e < N; e++) a[e] = silu<T>(a[e]) * b[e];
+        for (int e = 0; e < N; e++) a[e] = activate<T, ACT>(a[e]) * b[e];
         st_stream(o + c, Vec<T>::pack(a));
       }
     }
   }
 }
 
-template <typename T, int UNROLL>
+template <typename T, int UNROLL, Act ACT>
 cudaError_t launch_u(void* out, const void* x, int64_t rows, int ivec, cudaStream_t s) {
   const unsigned gx = static_cast<unsigned>((ivec + kSiluThreads * UNROLL - 1) /
                                             (kSiluThreads * UNROLL));
   const unsigned gy = static_cast<unsigned>(rows < kMaxGridY ? rows : kMaxGridY);
-  silu_and_mul_kernel<T, UNROLL><<<dim3(gx, gy), kSiluThreads, 0, s>>>(
+  act_and_mul_kernel<T, UNROLL, ACT><<<dim3(gx, gy), kSiluThreads, 0, s>>>(
       static_cast<T*>(out), static_cast<const T*>(x), rows, ivec);
   return cudaGetLastError();
 }
 
-template <typename T>
+template <typename T, Act ACT>
 cudaError_t launch_typed(void* out, const void* x, int64_t rows, int64_t inter, cudaStream_t s) {
   const int ivec = static_cast<int>(inter / Vec<T>::N);
   // Small problems (decode) spread one vector per thread over as many SMs as
   // possible; large ones give each thread more bytes in flight.
   if (static_cast<int64_t>(ivec) * rows >= int64_t(152) * 4 * kSiluThreads * 4)
-    return launch_u<T, 4>(out, x, rows, ivec, s);
-  return launch_u<T, 1>(out, x, rows, ivec, s);
+    return launch_u<T, 4, ACT>(out, x, rows, ivec, s);
+  return launch_u<T, 1, ACT>(out, x, rows, ivec, s);
 }
 
 }  // namespace
 
 cudaError_t launch_silu_and_mul(void* out, const void* x, int64_t rows, int64_t inter,
                                 int is_bf16, cudaStream_t stream) {
-  if (is_bf16) return launch_typed<__nv_bfloat16>(out, x, rows, inter, stream);
-  return launch_typed<float>(out, x, rows, inter, stream);
+  if (is_bf16) return launch_typed<__nv_bfloat16, Act::kSilu>(out, x, rows, inter, stream);
+  return launch_typed<float, Act::kSilu>(out, x, rows, inter, stream);
+}
+
+cudaError_t launch_gelu_and_mul(void* out, const void* x, int64_t rows, int64_t inter,
+                                int is_bf16, cudaStream_t stream) {
+  if (is_bf16) return launch_typed<__nv_bfloat16, Act::kGeluTanh>(out, x, rows, inter, stream);
+  return launch_typed<float, Act::kGeluTanh>(out, x, rows, inter, stream);
 }
 
 }  // namespace nr

@@ -73,6 +73,8 @@ def configure(lib):
     lib.nro_gated_ln_modulate.argtypes = [cint, i64, i64, i64, vp, vp, vp, vp, vp, dbl, vp, vp,
                                           vp, vp]
     lib.nro_gated_ln_modulate.restype = None
+    lib.nro_gelu_and_mul.argtypes = [cint, i64, i64, vp, vp, vp]
+    lib.nro_gelu_and_mul.restype = None
     lib.nro_silu_and_mul.argtypes = [cint, i64, i64, vp, vp, vp]
     lib.nro_silu_and_mul.restype = None
     lib.nro_rounding_mode_is_nearest.argtypes = []
@@ -307,4 +309,19 @@ def silu_and_mul(x, want_y=False):
     out = np.empty((rows, inter), x.dtype)
     y = np.empty((rows, inter), np.float64) if want_y else None
     lib.nro_silu_and_mul(dt, rows, inter, _ptr(x), _ptr(out), _ptr(y))
+    return out, y
+
+
+def gelu_and_mul(x, want_y=False):
+    """gelu_tanh(x[:, :I]) * x[:, I:] for x [rows, 2I].  Returns (out, y or None)."""
+    lib = _load()
+    x = _c(x)
+    dt = _dtype_code(x)
+    rows, two_i = x.shape
+    if two_i % 2:
+        raise ValueError("x's last axis must be even")
+    inter = two_i // 2
+    out = np.empty((rows, inter), x.dtype)
+    y = np.empty((rows, inter), np.float64) if want_y else None
+    lib.nro_gelu_and_mul(dt, rows, inter, _ptr(x), _ptr(out), _ptr(y))
     return out, y

@@ -472,6 +472,31 @@ void nro_silu_and_mul(int dtype, int64_t rows, int64_t inter, const void* x, voi
   }
 }
 
+/* ------------------------------------------------------------------------ */
+/* gelu_and_mul ([VT] "gelu_and_mul"): the tanh form of GELU of the gate     */
+/* (first half) times up (second half):                                      */
+/*   gelu(a) = 0.5 a (1 + tanh(z)),  z = sqrt(2/pi) (a + 0.044715 a^3)        */
+/*   y = gelu(a) * b;  out[r, j] = round_dtype(y)                             */
+/* For z < 0 the sum 1 + tanh(z) is taken from tanh z = (e^2z - 1)/(e^2z + 1) */
+/* as 2 e^2z / (1 + e^2z): the same number, without the cancellation that    */
+/* leaves 1 + tanh(z) = 0 in double once z < -19 or so.                      */
+/* ------------------------------------------------------------------------ */
+void nro_gelu_and_mul(int dtype, int64_t rows, int64_t inter, const void* x, void* out,
+                      double* y) {
+  const double k = sqrt(2.0 / 3.14159265358979323846264338327950288);
+  for (int64_t r = 0; r < rows; r++) {
+    for (int64_t j = 0; j < inter; j++) {
+      const double a = load(dtype, x, r * 2 * inter + j);
+      const double b = load(dtype, x, r * 2 * inter + inter + j);
+      const double z = k * (a + 0.044715 * a * a * a);
+      const double one_plus_tanh = z >= 0 ? 1.0 + tanh(z) : 2.0 * exp(2 * z) / (1.0 + exp(2 * z));
+      const double yj = 0.5 * a * one_plus_tanh * b;
+      store(dtype, out, r * inter + j, yj);
+      if (y != NULL) y[r * inter + j] = yj;
+    }
+  }
+}
+
 /* Rounding mode guard: the oracle's nearbyint and conversions assume the
  * default round-to-nearest mode; callers can check it. */
 int nro_rounding_mode_is_nearest(void) { return fegetround() == FE_TONEAREST; }

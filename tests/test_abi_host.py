@@ -37,6 +37,7 @@ def lib(lib_path):
                                   f32, f64, cint, cint, vp]
     L.nr_ln_modulate.argtypes = [vp, vp, vp, vp, i64, i64, i64, f32, cint, vp]
     L.nr_silu_and_mul.argtypes = [vp, vp, i64, i64, cint, vp]
+    L.nr_gelu_and_mul.argtypes = [vp, vp, i64, i64, cint, vp]
     L.nr_rmsnorm_quant_fp8.argtypes = [vp, vp, vp, vp, vp, i64, i64, cint, f32, cint, f32, vp]
     L.nr_qk_norm_rope_ex.argtypes = [vp, vp, vp, vp, vp, vp, cint, vp, i64, i64, i64, i64, i64,
                                      i64, f32, cint, ctypes.POINTER(RopeConfig), cint, vp]
@@ -154,15 +155,18 @@ def test_ln_modulate_validation(lib):
     assert ln(lib, shift=A + 16) == ALIAS
 
 
-def test_silu_and_mul_validation(lib):
-    assert lib.nr_silu_and_mul(None, None, 0, 64, BF16, None) == OK
-    assert lib.nr_silu_and_mul(A, A + MB, 4, 64, 9, None) == DTYPE
-    assert lib.nr_silu_and_mul(A, A + MB, -1, 64, BF16, None) == SHAPE
-    assert lib.nr_silu_and_mul(A, A + MB, 4, 0, BF16, None) == SHAPE
-    assert lib.nr_silu_and_mul(None, A + MB, 4, 64, BF16, None) == NULL
-    assert lib.nr_silu_and_mul(A, A + MB, 4, 60, BF16, None) == UNSUP
-    assert lib.nr_silu_and_mul(A + 4, A + MB, 4, 64, F32, None) == ALIGN
-    assert lib.nr_silu_and_mul(A, A + 256, 4, 64, BF16, None) == ALIAS  # out inside x
+@pytest.mark.parametrize("name", ["nr_silu_and_mul", "nr_gelu_and_mul"])
+def test_act_and_mul_validation(lib, name):
+    fn = getattr(lib, name)
+    assert fn(None, None, 0, 64, BF16, None) == OK
+    assert fn(A, A + MB, 4, 64, 9, None) == DTYPE
+    assert fn(A, A + MB, -1, 64, BF16, None) == SHAPE
+    assert fn(A, A + MB, 4, 0, BF16, None) == SHAPE
+    assert fn(None, A + MB, 4, 64, BF16, None) == NULL
+    assert fn(A, A + MB, 4, 60, BF16, None) == UNSUP
+    assert fn(A + 4, A + MB, 4, 64, F32, None) == ALIGN
+    assert fn(A, A + 256, 4, 64, BF16, None) == ALIAS  # out inside x
+    assert name.encode() in lib.nr_last_error_message()
 
 
 def gated(lib, out=A, res=A + 64 * MB, y=A + 128 * MB, gate=A + 192 * MB, shift=A + 193 * MB,

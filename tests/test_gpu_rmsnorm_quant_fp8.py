@@ -58,10 +58,19 @@ def test_saturation_and_subnormal_codes(nr):
     assert ((got & 0x78) == 0).mean() > 0.3
 
 
-@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
-@pytest.mark.parametrize("hidden", [8, 24, 4096, 8200, 32768])
+@pytest.mark.parametrize("dtype,hidden", [(torch.bfloat16, h) for h in (8, 24, 4096, 8200, 32768)]
+                         + [(torch.float32, h) for h in (4, 12, 4096, 8200, 16384)])
 def test_edge_sizes(nr, dtype, hidden):
+    """Down to one vector per row and up to the largest supported hidden
+    (32768 bf16 / 16384 f32: 4096 vectors of 16 bytes held in registers)."""
     run_case(nr, 3, hidden, dtype=dtype, residual=hidden % 3 == 0, seed=hidden % 31)
+
+
+def test_hidden_above_the_register_limit_is_refused(nr):
+    x = torch.zeros(2, 16388, dtype=torch.float32, device="cuda")
+    w = torch.ones(16388, dtype=torch.float32, device="cuda")
+    with pytest.raises(nr.NrError, match="UNSUPPORTED"):
+        nr.rmsnorm_quant_fp8(x, w, 1.0)
 
 
 def test_codes_only_without_bf16_copy(nr):

@@ -79,6 +79,12 @@ MUTANTS = [
      "const float t = (float)yj * inv_scale;"),
     ("fp8 scale applied the wrong way", "const float inv_scale = 1.0f / scale;",
      "const float inv_scale = scale;"),
+    ("gelu cubic coefficient", "0.044715 * a * a * a", "0.044715 * a * a"),
+    ("gelu missing half", "const double yj = 0.5 * a * one_plus_tanh * b;",
+     "const double yj = a * one_plus_tanh * b;"),
+    ("gelu 1 + tanh by direct sum", "z >= 0 ? 1.0 + tanh(z) :", "1 ? 1.0 + tanh(z) :"),
+    ("gelu negative branch exponent", "2.0 * exp(2 * z) / (1.0 + exp(2 * z))",
+     "2.0 * exp(z) / (1.0 + exp(2 * z))"),
     ("silu exponent sign", "a / (1.0 + exp(-a)) * b", "a / (1.0 + exp(a)) * b"),
     ("silu gate and up swapped", "const double a = load(dtype, x, r * 2 * inter + j);\n      const double b = load(dtype, x, r * 2 * inter + inter + j);",
      "const double b = load(dtype, x, r * 2 * inter + j);\n      const double a = load(dtype, x, r * 2 * inter + inter + j);"),

@@ -710,3 +710,49 @@ def test_silu_up_multiplies():
     _, y1 = oracle.silu_and_mul(x, want_y=True)
     _, y2 = oracle.silu_and_mul(x2, want_y=True)
     assert np.array_equal(y2, 2 * y1)
+
+
+# --------------------------------------------------------------------------
+# gelu_and_mul (tanh GELU)
+# --------------------------------------------------------------------------
+def test_gelu_matches_torch_tanh_gelu_and_operand_order():
+    """up = 1: y is torch's tanh-approximated GELU (float64, a library routine);
+    up = 0: y = 0; doubling up doubles y."""
+    g = synth.tensor(73, 0, (2, 64), torch.float32)
+    x = torch.cat([g, torch.ones_like(g)], dim=1)
+    _, y = oracle.gelu_and_mul(synth.to_oracle(x), want_y=True)
+    ref = torch.nn.functional.gelu(g.double(), approximate="tanh").numpy()
+    assert np.allclose(y, ref, rtol=1e-14, atol=1e-300)
+    x0 = torch.cat([g, torch.zeros_like(g)], dim=1)
+    _, y0 = oracle.gelu_and_mul(synth.to_oracle(x0), want_y=True)
+    assert np.all(y0 == 0)
+    x2 = torch.cat([g, 2 * torch.ones_like(g)], dim=1)
+    _, y2 = oracle.gelu_and_mul(synth.to_oracle(x2), want_y=True)
+    assert np.array_equal(y2, 2 * y)
+
+
+def test_gelu_against_150_digit_evaluation():
+    """Gates from -12 to 12, where for strongly negative gates 1 + tanh(z) is
+    below double's resolution near -1 (down to 1e-71 at a = -12): y within
+    1e-13 (relative) of the tanh formula evaluated with 150 significant
+    digits, enough to resolve 1 + tanh(z) there."""
+    mpmath.mp.dps = 150
+    g = np.concatenate([np.linspace(-12, 12, 97), [-0.5, 1e-30, -1e-30, 0.0]])[None, :]
+    g = g.astype(np.float32)
+    x = np.concatenate([g, np.full_like(g, 1.5)], axis=1)
+    _, y = oracle.gelu_and_mul(x, want_y=True)
+    k = mpmath.sqrt(2 / mpmath.pi)
+    for a, got in zip(g[0], y[0]):
+        am = mpmath.mpf(float(a))
+        ref = mpmath.mpf("0.5") * am * (1 + mpmath.tanh(k * (am + mpmath.mpf("0.044715") * am**3)))
+        ref = float(ref * mpmath.mpf("1.5"))
+        assert abs(got - ref) <= 1e-13 * abs(ref), (a, got, ref)
+
+
+def test_gelu_odd_part_identity():
+    """gelu(a) - gelu(-a) = a (tanh is odd)."""
+    g = synth.tensor(74, 0, (1, 64), torch.float32).numpy()
+    ones = np.ones_like(g)
+    _, yp = oracle.gelu_and_mul(np.concatenate([g, ones], axis=1), want_y=True)
+    _, ym = oracle.gelu_and_mul(np.concatenate([-g, ones], axis=1), want_y=True)
+    assert np.allclose(yp - ym, g.astype(np.float64), rtol=1e-14, atol=1e-15)

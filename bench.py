@@ -61,7 +61,8 @@ def parse_args():
     p.add_argument("--no-decode-sweep", action="store_true")
     p.add_argument("--no-next-rows", action="store_true")
     p.add_argument("--profile", default=None,
-                   help="run only the named call of the step (e.g. qk_norm_rope) --steps times, "
+                   help="run only the named call of the step or of the next rows (e.g. qk_norm_rope, "
+                        "gelu_and_mul) --steps times, "
                         "for ncu; --rows overrides its row/token count; prints no JSON")
     p.add_argument("--rows", type=int, default=None)
     return p.parse_args()
@@ -483,12 +484,53 @@ def run_e2e(args, torch, calls, device, world, barrier, step_bytes):
             "note": "pinned host buffers; H2D, kernels and D2H on three streams ordered per call"}
 
 
+def next_row_cases(nr, synth, torch, device, rows_override=None):
+    """The ops beyond the seven-call step as (name, make) pairs; make() puts
+    the operands on the device and returns (fn, bytes per call, rows).
+    rows_override shrinks the row count (for ncu captures)."""
+    def n_rows(default):
+        return default if rows_override is None else rows_override
+
+    def gated():
+        # gated residual + LayerNorm + modulation at the DiT shape, one sample
+        rows, hidden = n_rows(synth.LN_MODULATE["rows"]), synth.LN_MODULATE["hidden"]
+        res = synth.tensor(5, 20, (rows, hidden), torch.bfloat16).to(device)
+        y = synth.tensor(5, 21, (rows, hidden), torch.bfloat16).to(device)
+        gate, sh, sc = (synth.tensor(5, i, (1, hidden), torch.bfloat16, std=0.1).to(device)
+                        for i in (22, 23, 24))
+        o = torch.empty_like(res)
+        return (lambda: nr.gated_residual_ln_modulate(res, y, gate, sh, sc, out=o),
+                nbytes(res, y, gate, sh, sc) + nbytes(res, o), rows)
+
+    def quant():
+        # RMSNorm + e4m3 quantisation with the residual add, at the dense shape
+        c = synth.ADD_RMSNORM
+        rows = n_rows(c["rows"])
+        x, res, w = synth.rmsnorm_inputs(rows, c["hidden"], c["seed"], torch.bfloat16)
+        x, res, w = x.to(device), res.to(device), w.to(device)
+        codes = torch.empty(x.shape, dtype=torch.uint8, device=device)
+        return (lambda: nr.rmsnorm_quant_fp8(x, w, 0.02, residual=res, codes=codes),
+                nbytes(x, w, res) + nbytes(res, codes), rows)
+
+    def gelu():
+        # tanh-GELU gate times up, prefill-sized: 8192 tokens, intermediate 3 * 5120
+        rows = n_rows(8192)
+        g = synth.silu_inputs(rows, 3 * 5120, 6, torch.bfloat16).to(device)
+        o = torch.empty((rows, 3 * 5120), dtype=torch.bfloat16, device=device)
+        return lambda: nr.gelu_and_mul(g, out=o), nbytes(g, o), rows
+
+    return [("gated_residual_ln_modulate_bf16_26598x3072", gated),
+            ("rmsnorm_quant_fp8_bf16_8192x5120", quant),
+            ("gelu_and_mul_bf16_8192x30720", gelu)]
+
+
 def next_rows(nr, synth, torch, device, peak):
     """The ops beyond the seven-call step, each timed alone on its own workload
     (mean of CUDA-event times over back-to-back calls, operands larger than L2)."""
     out = {}
-
-    def timed(name, fn, nb, rows, iters=50):
+    for name, make in next_row_cases(nr, synth, torch, device):
+        fn, nb, rows = make()
+        iters = 50
         for _ in range(5):
             fn()
         torch.cuda.synchronize()
@@ -504,32 +546,7 @@ def next_rows(nr, synth, torch, device, peak):
                      "frac_of_measured": round(gbs / peak, 4),
                      "frac_of_nominal_8TBs": round(gbs / NOMINAL_HBM_GBS, 4),
                      "rows_per_s": round(rows / (us * 1e-6), 1)}
-
-    # gated residual + LayerNorm + modulation at the DiT shape, one sample
-    rows, hidden = synth.LN_MODULATE["rows"], synth.LN_MODULATE["hidden"]
-    res = synth.tensor(5, 20, (rows, hidden), torch.bfloat16).to(device)
-    y = synth.tensor(5, 21, (rows, hidden), torch.bfloat16).to(device)
-    gate, sh, sc = (synth.tensor(5, i, (1, hidden), torch.bfloat16, std=0.1).to(device)
-                    for i in (22, 23, 24))
-    o = torch.empty_like(res)
-    timed("gated_residual_ln_modulate_bf16_26598x3072",
-          lambda: nr.gated_residual_ln_modulate(res, y, gate, sh, sc, out=o),
-          nbytes(res, y, gate, sh, sc) + nbytes(res, o), rows)
-    del res, y, o
-    # RMSNorm + e4m3 quantisation with the residual add, at the dense shape
-    c = synth.ADD_RMSNORM
-    x, res, w = synth.rmsnorm_inputs(c["rows"], c["hidden"], c["seed"], torch.bfloat16)
-    x, res, w = x.to(device), res.to(device), w.to(device)
-    codes = torch.empty(x.shape, dtype=torch.uint8, device=device)
-    timed("rmsnorm_quant_fp8_bf16_8192x5120",
-          lambda: nr.rmsnorm_quant_fp8(x, w, 0.02, residual=res, codes=codes),
-          nbytes(x, w, res) + nbytes(res, codes), c["rows"])
-    del x, res, w, codes
-    # tanh-GELU gate times up, prefill-sized: 8192 tokens, intermediate 3 * 5120
-    g = synth.silu_inputs(8192, 3 * 5120, 6, torch.bfloat16).to(device)
-    o = torch.empty((8192, 3 * 5120), dtype=torch.bfloat16, device=device)
-    timed("gelu_and_mul_bf16_8192x30720", lambda: nr.gelu_and_mul(g, out=o), nbytes(g, o), 8192)
-    del g, o
+        del fn
     return out
 
 
@@ -717,17 +734,24 @@ def run_profile(args):
                          (synth.LN_MODULATE, "rows")):
             cfg[key] = args.rows
     calls = build_step(nr, synth, torch, device, 0, only=args.profile)
-    if not calls:
-        raise SystemExit("no call named %s*" % args.profile)
-    c = calls[0]
+    if calls:
+        c = calls[0]
+        fn, name, nb, rows, unit = c.fn, c.name, c.nbytes, c.rows, c.rows_unit
+    else:
+        cases = [(n, m) for n, m in next_row_cases(nr, synth, torch, device, args.rows)
+                 if n.startswith(args.profile)]
+        if not cases:
+            raise SystemExit("no call named %s*" % args.profile)
+        name = cases[0][0]
+        fn, nb, rows = cases[0][1]()
+        unit = "rows"
     for _ in range(args.warmup):
-        c.fn()
+        fn()
     torch.cuda.synchronize()
     for _ in range(args.steps):
-        c.fn()
+        fn()
     torch.cuda.synchronize()
-    print("profiled %s x%d (%d bytes per launch, %d %s)" % (c.name, args.steps, c.nbytes, c.rows,
-                                                            c.rows_unit))
+    print("profiled %s x%d (%d bytes per launch, %d %s)" % (name, args.steps, nb, rows, unit))
 
 
 def main():

@@ -15,7 +15,10 @@ The metric is achieved HBM throughput: algorithmic bytes (each input read
 once, each output written once) per second, summed over the step; rows/s and
 per-kernel GB/s with their fractions of the HBM peak are reported beside it.
 The step's footprint (~1.7 GB) is far larger than the 129 MB L2 and every
-large kernel's operands exceed it, so every launch starts from HBM.
+large kernel's operands exceed it, so every launch starts from HBM.  The timed
+region runs the steps back to back with CUDA events around the region and
+around each launch of the dominant kernel (for the roofline); the per-call
+breakdown comes from a second pass with events around every call.
 
 Usage:  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 N > 1 runs under torchrun, one rank per GPU, each rank on its own shard (weak
@@ -284,6 +287,28 @@ def source_hash(rel):
     return h.hexdigest()[:16]
 
 
+def copy_reference(torch, device, nbytes):
+    """GB/s of a device-to-device tensor copy moving `nbytes` in total (half
+    read, half written), the size of one launch of the dominant kernel: how
+    fast plain streaming runs at that size (a copy's start-up and drain weigh
+    more on a smaller transfer than on the peak measurement's)."""
+    n = max(1, nbytes // 4)  # bf16 elements per buffer
+    sets = max(2, (400 * 10 ** 6) // (4 * n) + 1)  # rotate so a buffer is never L2-warm
+    src = [torch.empty(n, dtype=torch.bfloat16, device=device).fill_(1.0) for _ in range(sets)]
+    dst = [torch.empty_like(src[0]) for _ in range(sets)]
+    for i in range(4):
+        dst[i % sets].copy_(src[i % sets])
+    iters = 40
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for i in range(iters):
+        dst[i % sets].copy_(src[i % sets])
+    e.record()
+    torch.cuda.synchronize(device)
+    ms = s.elapsed_time(e) / iters
+    return round(4 * n / (ms * 1e-3) / 1e9, 1)
+
+
 def ncu_traffic(kernel, units):
     """DRAM bytes per launch of `kernel` from the committed ncu capture, scaled
     by the units processed when the capture ran a smaller case (reads grow in
@@ -334,19 +359,40 @@ def run_ours(args):
             dist.barrier()
         torch.cuda.synchronize(device)
 
-    for _ in range(max(args.warmup, 3)):
+    def per_call_times(steps, reduce=statistics.fmean):
+        """Device time of each call over `steps` steps (mean, or `reduce`), from
+        CUDA events recorded on the launching stream around every call."""
+        ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in calls] for _ in range(steps)]
+        for i in range(steps):
+            for j, c in enumerate(calls):
+                ev[i][j][0].record(stream)
+                c.fn()
+                ev[i][j][1].record(stream)
+        torch.cuda.synchronize(device)
+        return [reduce([ev[i][j][0].elapsed_time(ev[i][j][1]) for i in range(steps)])
+                for j in range(len(calls))]
+
+    # Warm-up (untimed), then a short calibration pass with per-call events:
+    # the dominant call (largest median device time) is the one the timed
+    # region brackets for the roofline.
+    W = max(args.warmup, 3)
+    for _ in range(W):
         step()
+    calib = per_call_times(5, reduce=statistics.median)
+    dom = max(range(len(calls)), key=lambda j: calib[j])
     barrier()
 
-    # Timed region: K steps, events around each call (on the launching stream).
+    # Timed region: K steps; CUDA events bracket the whole region and each
+    # launch of the dominant call (no events around the other calls, so the
+    # step is timed as it runs back to back).
     K = args.steps
-    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in calls] for _ in range(K)]
+    dom_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(K)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    for row in ev:  # create the CUDA events now, outside the timed region
-        for a, b in row:
-            a.record(stream)
-            b.record(stream)
+    for a, b in dom_ev:  # create the CUDA events now, outside the timed region
+        a.record(stream)
+        b.record(stream)
     barrier()
     sampler = ClockSampler(gpu_id_for(torch, device))
     with sampler:
@@ -355,18 +401,24 @@ def run_ours(args):
         start.record(stream)
         for i in range(K):
             for j, c in enumerate(calls):
-                ev[i][j][0].record(stream)
-                c.fn()
-                ev[i][j][1].record(stream)
+                if j == dom:
+                    dom_ev[i][0].record(stream)
+                    c.fn()
+                    dom_ev[i][1].record(stream)
+                else:
+                    c.fn()
         end.record(stream)
         barrier()
         t_wall1 = time.time()
     clocks = sampler.summary(t_wall0, t_wall1)
     elapsed_ms = start.elapsed_time(end)
-    per_call_ms = [statistics.fmean(ev[i][j][0].elapsed_time(ev[i][j][1]) for i in range(K))
-                   for j in range(len(calls))]
+    dom_ms = statistics.fmean(a.elapsed_time(b) for a, b in dom_ev)
     if world > 1:
         elapsed_ms = max_over_ranks(elapsed_ms, dist, device)
+
+    # Per-call breakdown, after the timed region: events around every call.
+    breakdown_steps = min(K, 300)
+    per_call_ms = per_call_times(breakdown_steps)
 
     ms_per_step = elapsed_ms / K
     value = world * step_bytes * K / (elapsed_ms * 1e-3) / 1e9
@@ -379,11 +431,10 @@ def run_ours(args):
                            "frac_of_measured": round(gbs / peak, 4),
                            "frac_of_nominal_8TBs": round(gbs / NOMINAL_HBM_GBS, 4),
                            "rows_per_s": round(c.rows / (ms * 1e-3), 1), "rows_unit": c.rows_unit}
-    # dominant kernel: largest share of the step's device time
-    dom = max(range(len(calls)), key=lambda j: per_call_ms[j])
     dc = calls[dom]
-    achieved = dc.nbytes / (per_call_ms[dom] * 1e-3) / 1e9
+    achieved = dc.nbytes / (dom_ms * 1e-3) / 1e9
     traffic = ncu_traffic(dc.kernel, dc.rows)
+    copy_gbs = copy_reference(torch, device, dc.nbytes) if rank == 0 else None
 
     e2e = run_e2e(args, torch, calls, device, world, barrier, step_bytes)
 
@@ -403,9 +454,15 @@ def run_ours(args):
                           "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                           "frac": round(achieved / peak, 4),
                           "frac_of_nominal_8TBs": round(achieved / NOMINAL_HBM_GBS, 4),
-                          "traffic": None, "algorithmic_bytes": dc.nbytes},
+                          "traffic": None, "algorithmic_bytes": dc.nbytes,
+                          "duration_us": round(dom_ms * 1e3, 2),
+                          "copy_same_bytes_GB_s": copy_gbs,
+                          "frac_of_copy_same_bytes": (round(achieved / copy_gbs, 4)
+                                                      if copy_gbs else None)},
                          **(traffic or {})),
         "kernels": kernels,
+        "kernels_timing": "per-call CUDA events over %d steps after the timed region (the "
+                          "timed region brackets only the dominant call)" % breakdown_steps,
         "rows_per_s": round(world * sum(c.rows for c in calls) / (ms_per_step * 1e-3), 1),
         "e2e": e2e,
         "gpu_launches": K * len(calls),

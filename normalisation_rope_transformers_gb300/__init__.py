@@ -46,6 +46,8 @@ lib.nr_rmsnorm_quant_fp8.restype = _int
 lib.nr_qk_norm_rope.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _int, _vp, _i64, _i64, _i64, _i64,
                                 _i64, _i64, _f32, _f64, _int, _int, _vp]
 lib.nr_qk_norm_rope.restype = _int
+
+
 class RopeConfig(ctypes.Structure):
     """Mirror of nr_rope_config (include/nr.h)."""
     _fields_ = [("rotary_dim", ctypes.c_int64), ("interleaved", ctypes.c_int32),

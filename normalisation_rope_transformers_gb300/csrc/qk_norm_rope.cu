@@ -13,11 +13,13 @@
 //    lane and the rotation needs no data exchange.  The row's sum of squares
 //    is a butterfly over the L lanes.
 //  * A warp owns whole tokens (all their Q and K heads), persistently: warp w
-//    of W takes tokens w, w + W, ...  Its head rows form one flat stream of
-//    iterations (32/L rows per iteration) that crosses token boundaries, and a
-//    rolling register prefetch keeps the next R iterations' loads in flight
-//    while the current one is computed.  There is no block-level barrier
-//    after the weights are staged, so warps never wait for each other.
+//    of W takes tokens w, w + W, ..., so at any moment the warps work on one
+//    contiguous window of tokens.  Its head rows form one flat stream of
+//    iterations (32/L rows per iteration) that crosses token boundaries; each
+//    lane copies its vectors RING iterations ahead into a per-warp
+//    shared-memory ring with cp.async, so several iterations are in flight
+//    without holding registers.  There is no block-level barrier after the
+//    weights are staged, so warps never wait for each other.
 //  * Each (token, pair) angle is computed once per warp (a few sincospif per
 //    lane) into a per-warp shared-memory table and reused by all the token's
 //    heads.  The angle pos*freq_i is reduced modulo one turn exactly, as
@@ -34,12 +36,6 @@ namespace {
 // Iterations in flight per warp (shared-memory ring slots); a build-time knob.
 #ifndef NR_QK_RING
 #define NR_QK_RING 5
-#endif
-
-// Minimum resident blocks per SM asked of the register allocator (0: none); a
-// build-time knob.
-#ifndef NR_QK_MINB
-#define NR_QK_MINB 0
 #endif
 
 constexpr int kQkThreads = 128;
@@ -104,7 +100,7 @@ struct QkSmem {
 // unrotated vectors), GPT-J interleaved pairs (both members inside one vector)
 // and M-RoPE (three position rows; pair i takes row axis[i]).
 template <typename T, typename WT, int L, int RING, bool GEN>
-__global__ void __launch_bounds__(kQkThreads, NR_QK_MINB) qk_norm_rope_kernel(const QkArgs a,
+__global__ void __launch_bounds__(kQkThreads) qk_norm_rope_kernel(const QkArgs a,
                                                                   const RopeTurns turns) {
   using S = QkSmem<T, L>;
   constexpr int N = Vec<T>::N;

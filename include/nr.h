@@ -19,7 +19,9 @@
  *
  * Conventions shared by every entry point
  *   - Pointers are DEVICE pointers (CUDA global memory) owned by the caller; the
- *     library allocates nothing, keeps no state between calls and frees nothing.
+ *     library allocates nothing and frees nothing.  Its only state is one
+ *     device status word that kernels set when a bounded wait runs out
+ *     (nr_device_status reads and clears it).
  *   - Every pointer must be 16-byte aligned, and every row start (row stride in
  *     bytes) a multiple of 16, so that each thread moves 128-bit vectors.
  *   - Work is enqueued asynchronously on `stream` (0 = the legacy default
@@ -56,7 +58,8 @@ typedef enum nr_status {
   NR_ERR_ALIAS = 5,       /* an output overlaps an input (or another output) it may not overlap */
   NR_ERR_UNSUPPORTED = 6, /* a valid size the kernels do not cover (e.g. hidden % 8 for bf16) */
   NR_ERR_CUDA = 7,        /* the launch failed; see nr_last_error_message() */
-  NR_ERR_VALUE = 8        /* a scalar is out of range (eps < 0 or not finite, theta <= 0) */
+  NR_ERR_VALUE = 8,       /* a scalar is out of range (eps < 0 or not finite, theta <= 0) */
+  NR_ERR_TIMEOUT = 9      /* a kernel gave up a bounded wait (see nr_device_status) */
 } nr_status;
 
 typedef enum nr_dtype {
@@ -276,6 +279,27 @@ nr_status nr_silu_and_mul(void* out, const void* x, int64_t rows, int64_t inter,
  */
 nr_status nr_gelu_and_mul(void* out, const void* x, int64_t rows, int64_t inter, nr_dtype dtype,
                           cudaStream_t stream);
+
+/*
+ * Device-side failure report.  Kernels that wait on hardware events (the
+ * bulk-copy path of nr_qk_norm_rope waits for its copies on shared-memory
+ * barriers) bound every wait (about one second of SM clock); a wait that runs
+ * out sets a bit in a device status word kept by the library, the kernel
+ * lets its copies in flight finish and returns, and the outputs of that call
+ * are not valid.  nr_device_status synchronises `stream`, reads and clears
+ * the word: NR_OK if no wait ran out since the last read, else
+ * NR_ERR_TIMEOUT (the message names the kernel).  A CUDA error while
+ * synchronising is NR_ERR_CUDA.
+ */
+nr_status nr_device_status(cudaStream_t stream);
+
+/*
+ * Test hook for the failure path above: launches one block whose only wait
+ * is on a barrier nothing completes, given up after `limit_cycles` SM clock
+ * cycles (1 .. 2^32).  nr_device_status then reports NR_ERR_TIMEOUT.  Faults
+ * and hangs nothing: the wait is bounded and the context stays usable.
+ */
+nr_status nr_test_wait_probe(int64_t limit_cycles, cudaStream_t stream);
 
 /* Static, human-readable name of a status code. */
 const char* nr_status_string(nr_status s);

@@ -71,6 +71,10 @@ lib.nr_silu_and_mul.argtypes = [_vp, _vp, _i64, _i64, _int, _vp]
 lib.nr_silu_and_mul.restype = _int
 lib.nr_gelu_and_mul.argtypes = [_vp, _vp, _i64, _i64, _int, _vp]
 lib.nr_gelu_and_mul.restype = _int
+lib.nr_device_status.argtypes = [_vp]
+lib.nr_device_status.restype = _int
+lib.nr_test_wait_probe.argtypes = [_i64, _vp]
+lib.nr_test_wait_probe.restype = _int
 lib.nr_status_string.argtypes = [_int]
 lib.nr_status_string.restype = ctypes.c_char_p
 lib.nr_last_error_message.argtypes = []
@@ -82,6 +86,7 @@ NR_F32 = 0
 NR_BF16 = 1
 ENTRY_POINTS = ("nr_rmsnorm", "nr_rmsnorm_quant_fp8", "nr_qk_norm_rope", "nr_qk_norm_rope_ex", "nr_ln_modulate",
                 "nr_silu_and_mul", "nr_gelu_and_mul", "nr_gated_residual_ln_modulate",
+                "nr_device_status", "nr_test_wait_probe",
                 "nr_status_string", "nr_last_error_message", "nr_version")
 
 
@@ -266,6 +271,18 @@ def _act_and_mul(fn, x, out):
     return out
 
 
+def device_status(device=None):
+    """Wait for the current stream of `device` and raise NrError
+    (NR_ERR_TIMEOUT) if a kernel gave up a bounded wait since the last check."""
+    _check(lib.nr_device_status(torch.cuda.current_stream(device).cuda_stream))
+
+
+def wait_probe(limit_cycles=100000, device=None):
+    """Launch the library's wait probe: one wait that nothing completes, given
+    up after `limit_cycles` SM clock cycles (the next device_status() raises)."""
+    _check(lib.nr_test_wait_probe(int(limit_cycles), torch.cuda.current_stream(device).cuda_stream))
+
+
 def silu_and_mul(x, out=None):
     """silu(x[:, :I]) * x[:, I:] for x [rows, 2I].  Returns out [rows, I]."""
     return _act_and_mul(lib.nr_silu_and_mul, x, out)
@@ -277,6 +294,6 @@ def gelu_and_mul(x, out=None):
 
 
 __all__ = ["rmsnorm", "rmsnorm_quant_fp8", "qk_norm_rope", "qk_norm_rope_ex", "RopeConfig", "ln_modulate",
-           "silu_and_mul", "gelu_and_mul",
+           "silu_and_mul", "gelu_and_mul", "device_status", "wait_probe",
            "gated_residual_ln_modulate", "NrError", "lib",
            "LIB_PATH", "ENTRY_POINTS", "NR_F32", "NR_BF16"]

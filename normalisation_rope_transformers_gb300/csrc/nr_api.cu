@@ -87,6 +87,7 @@ const char* nr_status_string(nr_status s) {
     case NR_ERR_UNSUPPORTED: return "NR_ERR_UNSUPPORTED";
     case NR_ERR_CUDA: return "NR_ERR_CUDA";
     case NR_ERR_VALUE: return "NR_ERR_VALUE";
+    case NR_ERR_TIMEOUT: return "NR_ERR_TIMEOUT";
   }
   return "NR_ERR_UNKNOWN";
 }
@@ -425,6 +426,25 @@ nr_status act_and_mul(const char* fn, int gelu, void* out, const void* x, int64_
 }  // namespace
 
 extern "C" {
+
+nr_status nr_device_status(cudaStream_t stream) {
+  unsigned bits = 0;
+  const cudaError_t e = nr::take_device_status(stream, &bits);
+  if (e != cudaSuccess) return from_cuda(e, "nr_device_status");
+  if (bits & nr::kStatusBitQkBulkWait)
+    return fail(NR_ERR_TIMEOUT, "nr_device_status: a bounded wait for a bulk copy ran out in the "
+                                "Q/K norm + RoPE kernel (status bits 0x%x)", bits);
+  if (bits != 0)
+    return fail(NR_ERR_TIMEOUT, "nr_device_status: the wait probe's wait ran out (status bits "
+                                "0x%x)", bits);
+  return ok();
+}
+
+nr_status nr_test_wait_probe(int64_t limit_cycles, cudaStream_t stream) {
+  if (limit_cycles < 1 || limit_cycles > (int64_t(1) << 32))
+    return fail(NR_ERR_VALUE, "nr_test_wait_probe: limit_cycles must be in [1, 2^32]");
+  return from_cuda(nr::launch_wait_probe(limit_cycles, stream), "nr_test_wait_probe");
+}
 
 nr_status nr_silu_and_mul(void* out, const void* x, int64_t rows, int64_t inter, nr_dtype dtype,
                           cudaStream_t stream) {

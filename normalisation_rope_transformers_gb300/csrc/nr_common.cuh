@@ -109,6 +109,101 @@ __device__ __forceinline__ uint4 lds128(const void* p) {
 }
 
 // ---------------------------------------------------------------------------
+// Bulk copies by the TMA engine (cp.async.bulk, no tensor map) and the
+// shared-memory mbarriers that count their bytes.  Sizes and both addresses
+// must be multiples of 16 bytes.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void mbar_init(unsigned bar, unsigned count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+// Makes initialised mbarriers visible to the async proxy (the TMA engine).
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+// One arrival that also announces `bytes` of copies to be counted.
+__device__ __forceinline__ void mbar_arrive_expect_tx(unsigned bar, unsigned bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
+               "r"(bytes)
+               : "memory");
+}
+
+// True if the phase with the given parity has completed.  Never blocks
+// (test_wait, not try_wait: a try_wait on a phase that nothing completes may
+// keep the thread suspended, so no clock check after it would ever run).
+__device__ __forceinline__ bool mbar_test_wait(unsigned bar, unsigned parity) {
+  unsigned done;
+  asm volatile(
+      "{\n"
+      "  .reg .pred p;\n"
+      "  mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n"
+      "  selp.u32 %0, 1, 0, p;\n"
+      "}"
+      : "=r"(done)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+// Polls the phase (with a short sleep between polls) for at most `limit` SM
+// clock cycles; false if it gave up (the caller records the failure and winds
+// down).  Every poll returns at once, so the bound always holds.
+__device__ __forceinline__ bool mbar_wait_bounded(unsigned bar, unsigned parity, long long limit) {
+  if (mbar_test_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  do {
+    __nanosleep(32);
+    if (mbar_test_wait(bar, parity)) return true;
+  } while (clock64() - t0 <= limit);
+  return false;
+}
+
+// Global -> shared bulk copy; its bytes complete a transaction count on `bar`.
+__device__ __forceinline__ void bulk_load(unsigned dst, const void* src, unsigned bytes,
+                                          unsigned bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+// Asks L2 to fetch `bytes` from global memory (no completion to wait for).
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, unsigned bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
+// Shared -> global bulk copy, tracked by the issuing thread's bulk groups.
+__device__ __forceinline__ void bulk_store(void* dst, unsigned src, unsigned bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+// Until at most `pending` of this thread's bulk groups still read shared memory.
+template <int pending>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(pending) : "memory");
+}
+
+// Until at most `pending` of this thread's bulk groups are incomplete.
+template <int pending>
+__device__ __forceinline__ void bulk_wait() {
+  asm volatile("cp.async.bulk.wait_group %0;" ::"n"(pending) : "memory");
+}
+
+// Orders this thread's ordinary shared-memory writes before later bulk copies
+// (async proxy) that read them.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
 // Element types: a 128-bit vector holds VEC values of T.
 // ---------------------------------------------------------------------------
 template <typename T>

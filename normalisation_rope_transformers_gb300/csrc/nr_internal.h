@@ -84,4 +84,15 @@ cudaError_t launch_qk_norm_rope(void* q_out, void* k_out, const void* q, const v
                                 float eps, const RopeTurns& turns, int gemma, int64_t rotary_dim,
                                 int interleaved, int mrope, int is_bf16, cudaStream_t stream);
 
+// Device status word: bits set by kernels whose bounded waits ran out.
+constexpr unsigned kStatusBitQkBulkWait = 1u;
+constexpr unsigned kStatusBitProbeWait = 2u;
+
+// Waits for `stream`, then reads and clears the status word.
+cudaError_t take_device_status(cudaStream_t stream, unsigned* bits);
+
+// One block whose single wait nothing completes, given up after
+// `limit_cycles` SM clock cycles (it sets kStatusBitProbeWait).
+cudaError_t launch_wait_probe(long long limit_cycles, cudaStream_t stream);
+
 }  // namespace nr

@@ -313,6 +313,253 @@ __global__ void __launch_bounds__(kQkThreads) qk_norm_rope_kernel(const QkArgs a
   cp_async_wait<0>();  // nothing may land after the block's shared memory is released
 }
 
+// ---------------------------------------------------------------------------
+// Bulk-copy variant (full-head NeoX rotation): whole tokens move through
+// shared memory by the TMA engine.
+//
+// A block of 4 warps owns tokens c, c + C, c + 2C, ... (C = grid size, so the
+// blocks sweep one contiguous window of tokens).  Each token's Q rows and K
+// rows are each one contiguous block of memory, so one bulk copy per tensor
+// brings a token into a shared-memory stage; NST stages keep NST - 1 tokens
+// in flight while one is computed.  The four warps split the token's head rows
+// (lanes map to rows exactly as in the ring kernel), normalise and rotate them
+// in place in the stage, and one thread writes the stage back with two bulk
+// stores.  The next token's angle table is computed while the current token's
+// rows are processed (double-buffered), so each token costs one block
+// barrier.  Loads complete on a per-stage mbarrier; every wait on it is
+// bounded and, if it runs out, sets a bit in the device status word and the
+// block winds down (waiting, again bounded, for its copies in flight).
+// ---------------------------------------------------------------------------
+#ifndef NR_QKB_STAGES
+#define NR_QKB_STAGES 3
+#endif
+// Kernel for the full-head NeoX case: 0 ring, 1 bulk copies (a build-time
+// knob for comparisons).
+#ifndef NR_QK_PATH
+#define NR_QK_PATH 1
+#endif
+// Tokens ahead of the stages that the producer also asks L2 to prefetch (0:
+// none); a build-time knob.
+#ifndef NR_QKB_L2PF
+#define NR_QKB_L2PF 0
+#endif
+
+// Warps per block (they split each token's head rows); a build-time knob.
+#ifndef NR_QKB_WARPS
+#define NR_QKB_WARPS 4
+#endif
+constexpr int kBulkWarps = NR_QKB_WARPS;
+constexpr int kBulkThreads = kBulkWarps * kWarp;
+constexpr long long kWaitLimitCycles = 1LL << 31;  // about one second
+
+__device__ unsigned int g_status_word;
+
+__device__ __forceinline__ void record_status(unsigned bit) { atomicOr(&g_status_word, bit); }
+
+struct BulkGeom {
+  unsigned q_bytes;      // one token's Q rows
+  unsigned k_bytes;      // one token's K rows
+  unsigned stage_bytes;  // q_bytes + k_bytes rounded up to 128
+};
+
+template <typename T, int L>
+struct BulkSmem {
+  static constexpr int N = Vec<T>::N;
+  static constexpr int HALF = L * N;
+  static constexpr int D = 2 * HALF;
+  // [NST stages][2 angle tables of HALF float2][2D weights][HALF turns][NST mbarriers][flag]
+  static size_t bytes(int nst, unsigned stage_bytes) {
+    return static_cast<size_t>(nst) * stage_bytes + 2 * HALF * sizeof(float2) +
+           2 * D * sizeof(float) + HALF * sizeof(unsigned long long) +
+           nst * sizeof(unsigned long long) + 16;
+  }
+};
+
+template <typename T, typename WT, int L, int NST>
+__global__ void __launch_bounds__(kBulkThreads) qk_norm_rope_bulk_kernel(const QkArgs a,
+                                                                       const RopeTurns turns,
+                                                                       const BulkGeom geo) {
+  using S = BulkSmem<T, L>;
+  constexpr int N = Vec<T>::N;
+  constexpr int HALF = S::HALF;
+  constexpr int D = S::D;
+  constexpr int GW = kWarp / L;  // head rows per warp pass
+
+  // bulk copies need 16-byte aligned shared addresses: the stages start at the
+  // (16-byte aligned) base and every stage and K block offset is a multiple of 16
+  extern __shared__ __align__(16) unsigned char smem[];
+  unsigned char* stages = smem;
+  float2* table = reinterpret_cast<float2*>(stages + static_cast<size_t>(NST) * geo.stage_bytes);
+  float* wsm = reinterpret_cast<float*>(table + 2 * HALF);
+  unsigned long long* turn_sm = reinterpret_cast<unsigned long long*>(wsm + 2 * D);
+  unsigned long long* bars = turn_sm + HALF;
+  int* abort_flag = reinterpret_cast<int*>(bars + NST);
+
+  const int tid = threadIdx.x;
+  const int warp = tid / kWarp;
+  const int lane32 = tid % kWarp;
+  const WT* wq = static_cast<const WT*>(a.wq);
+  const WT* wk = static_cast<const WT*>(a.wk);
+  for (int i = tid; i < 2 * D; i += kBulkThreads) {
+    float wv = 0.0f;
+    if (i < D)
+      wv = load_w<WT>(wq, i);
+    else if (a.hk > 0)
+      wv = load_w<WT>(wk, i - D);
+    wsm[i] = wv + a.w_add;
+  }
+  for (int i = tid; i < HALF; i += kBulkThreads) turn_sm[i] = turns.turn[i];
+  if (tid == 0) {
+    for (int st = 0; st < NST; st++) mbar_init(smem_addr(bars + st), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  const int64_t C = gridDim.x;
+  const int64_t t0 = blockIdx.x;
+  const int64_t ntok = t0 < a.tokens ? (a.tokens - 1 - t0) / C + 1 : 0;  // this block's tokens
+  const int H = a.hq + a.hk;
+  const int IT = (H + GW - 1) / GW;
+  const T* q = static_cast<const T*>(a.q);
+  const T* k = static_cast<const T*>(a.k);
+  T* q_out = static_cast<T*>(a.q_out);
+  T* k_out = static_cast<T*>(a.k_out);
+  auto stage = [&](int64_t j) { return stages + (j % NST) * geo.stage_bytes; };
+
+  // Producer (thread 0): bring local token j into its stage.
+  int64_t issued = 0;
+  auto issue = [&](int64_t j) {
+    const int64_t tok = t0 + j * C;
+    const unsigned bar = smem_addr(bars + j % NST);
+    mbar_arrive_expect_tx(bar, geo.q_bytes + geo.k_bytes);
+    bulk_load(smem_addr(stage(j)), q + tok * a.q_stride, geo.q_bytes, bar);
+    if (geo.k_bytes) bulk_load(smem_addr(stage(j) + geo.q_bytes), k + tok * a.k_stride,
+                               geo.k_bytes, bar);
+    issued = j + 1;
+    if (NR_QKB_L2PF > 0 && j + NR_QKB_L2PF < ntok) {
+      const int64_t ptok = t0 + (j + NR_QKB_L2PF) * C;
+      bulk_prefetch_l2(q + ptok * a.q_stride, geo.q_bytes);
+      if (geo.k_bytes) bulk_prefetch_l2(k + ptok * a.k_stride, geo.k_bytes);
+    }
+  };
+  if (tid == 0)
+    for (int64_t j = 0; j < NST - 1 && j < ntok; j++) issue(j);
+
+  // Angle table of a token into table buffer b (threads < HALF, strided).
+  auto angles = [&](int b, int p) {
+    for (int i = tid; i < HALF; i += kBulkThreads) {
+      const unsigned long long prod = static_cast<unsigned long long>(static_cast<long long>(p)) *
+                                      turn_sm[i];
+      const int hi = static_cast<int>(prod >> 32);  // signed turn fraction * 2^32
+      float sn, cn;
+      sincospif(static_cast<float>(hi) * 0x1p-31f, &sn, &cn);  // angle = pi * hi / 2^31
+      table[b * HALF + i] = make_float2(cn, sn);
+    }
+  };
+  int pos_next = 0;  // position of local token j + 1, loaded one token ahead
+  if (ntok > 0) {
+    if (tid < HALF) {
+      angles(0, a.pos[t0]);
+      if (ntok > 1) pos_next = a.pos[t0 + C];
+    }
+  }
+  __syncthreads();
+
+  const int g = lane32 / L;
+  const int l = lane32 % L;
+  int64_t j = 0;
+  for (; j < ntok; j++) {
+    const int64_t tok = t0 + j * C;
+    unsigned char* st = stage(j);
+    if (!mbar_wait_bounded(smem_addr(bars + j % NST), static_cast<unsigned>((j / NST) & 1),
+                           kWaitLimitCycles)) {
+      record_status(kStatusBitQkBulkWait);
+      *abort_flag = 1;
+    }
+    // this lane's (cos, sin) for the token
+    float2 cs[N];
+#pragma unroll
+    for (int e = 0; e < N; e++) cs[e] = table[(j & 1) * HALF + l * N + e];
+    for (int it = warp; it < IT; it += kBulkWarps) {  // uniform across the warp
+      const int row = it * GW + g;
+      // Lanes of a row past the last head carry zeros but still join the
+      // butterfly: the shuffles take the full warp.
+      const bool valid = row < H;
+      const bool is_q = row < a.hq;
+      uint4* r = reinterpret_cast<uint4*>(
+          st + (is_q ? 0u : geo.q_bytes) +
+          static_cast<size_t>(valid ? (is_q ? row : row - a.hq) : 0) * D * sizeof(T));
+      float xa[N], xb[N];
+      float ss = 0.0f;
+      if (valid) {
+        Vec<T>::unpack(r[l], xa);
+        Vec<T>::unpack(r[l + L], xb);
+#pragma unroll
+        for (int e = 0; e < N; e++) {
+          ss = fmaf(xa[e], xa[e], ss);
+          ss = fmaf(xb[e], xb[e], ss);
+        }
+      }
+      ss = group_sum<L>(ss);
+      if (!valid) continue;
+      const float inv = rsqrtf(ss * a.inv_d + a.eps);
+      const float* wa = wsm + (is_q ? 0 : D) + l * N;
+      const float* wb = wa + HALF;
+      float oa[N], ob[N];
+#pragma unroll
+      for (int e = 0; e < N; e++) {
+        const float na = xa[e] * inv * wa[e];
+        const float nb = xb[e] * inv * wb[e];
+        oa[e] = fmaf(na, cs[e].x, -nb * cs[e].y);
+        ob[e] = fmaf(na, cs[e].y, nb * cs[e].x);
+      }
+      r[l] = Vec<T>::pack(oa);
+      r[l + L] = Vec<T>::pack(ob);
+    }
+    // the next token's angles, into the other table buffer
+    if (tid < HALF && j + 1 < ntok) {
+      angles(static_cast<int>((j + 1) & 1), pos_next);
+      if (j + 2 < ntok) pos_next = a.pos[t0 + (j + 2) * C];
+    }
+    fence_proxy_async_smem();
+    __syncthreads();
+    if (*abort_flag) break;
+    if (tid == 0) {
+      bulk_store(q_out + tok * a.q_stride, smem_addr(st), geo.q_bytes);
+      if (geo.k_bytes) bulk_store(k_out + tok * a.k_stride, smem_addr(st + geo.q_bytes),
+                                  geo.k_bytes);
+      bulk_commit();
+      if (j + NST - 1 < ntok) {
+        bulk_wait_read<1>();  // the stage of token j - 1 has been read out
+        issue(j + NST - 1);
+      }
+    }
+  }
+  if (tid == 0) {
+    bulk_wait<0>();  // every store has landed before the block's shared memory is released
+    // After an abandoned wait (at token j), let the loads still in flight
+    // finish (bounded); after a normal finish there are none (j == issued).
+    for (int64_t m = j; m < issued; m++)
+      if (!mbar_wait_bounded(smem_addr(bars + m % NST), static_cast<unsigned>((m / NST) & 1),
+                             kWaitLimitCycles))
+        break;
+  }
+}
+
+// A wait that nothing completes: one mbarrier with no arrivals, waited on for
+// `limit` cycles.  Exercises the expiry path that the real kernels take.
+__global__ void wait_probe_kernel(long long limit) {
+  __shared__ __align__(8) unsigned long long bar;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_addr(&bar), 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (!mbar_wait_bounded(smem_addr(&bar), 0, limit) && threadIdx.x == 0)
+    record_status(kStatusBitProbeWait);
+}
+
 // Resident blocks per SM of one kernel instantiation (with its dynamic shared
 // memory), cached per device; also raises the kernel's shared-memory limit.
 template <typename T, typename WT, int L, int RING, bool GEN>
@@ -361,10 +608,55 @@ cudaError_t launch_g(const QkArgs& a, const RopeTurns& turns, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+// Largest shared memory the bulk variant may take per block (stages plus
+// tables): beyond it (very many heads per token) the ring kernel runs.
+constexpr size_t kBulkMaxSmem = 112 * 1024;
+
+template <typename T, typename WT, int L>
+cudaError_t launch_bulk(const QkArgs& a, const RopeTurns& turns, const BulkGeom& geo,
+                        size_t smem, cudaStream_t s) {
+  constexpr int NST = NR_QKB_STAGES;
+  auto kernel = qk_norm_rope_bulk_kernel<T, WT, L, NST>;
+  int device = 0;
+  cudaError_t e = cudaGetDevice(&device);
+  if (e != cudaSuccess) return e;
+  // Per device: raise the shared-memory limit once; cache the occupancy of
+  // the last shared-memory size asked for.
+  static int limit_set[64] = {0};
+  static size_t last_smem[64] = {0};
+  static int last_blocks[64] = {0};
+  if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
+  if (!limit_set[device]) {
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kBulkMaxSmem));
+    if (e != cudaSuccess) return e;
+    limit_set[device] = 1;
+  }
+  if (last_smem[device] != smem) {
+    int n = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, kBulkThreads, smem);
+    if (e != cudaSuccess) return e;
+    last_blocks[device] = n < 1 ? 1 : n;
+    last_smem[device] = smem;
+  }
+  const int64_t resident = static_cast<int64_t>(sm_count(device)) * last_blocks[device];
+  const int64_t blocks = a.tokens < resident ? a.tokens : resident;
+  kernel<<<dim3(static_cast<unsigned>(blocks)), kBulkThreads, smem, s>>>(a, turns, geo);
+  return cudaGetLastError();
+}
+
 template <typename T, typename WT, int L>
 cudaError_t launch_l(const QkArgs& a, const RopeTurns& turns, cudaStream_t s) {
   const bool general = a.rot_vec != 2 * L || a.interleaved || a.mrope;
   if (general) return launch_g<T, WT, L, true>(a, turns, s);
+  // Whole tokens through shared memory when a token's rows fit the stages.
+  constexpr int D = 2 * L * Vec<T>::N;
+  BulkGeom geo;
+  geo.q_bytes = static_cast<unsigned>(a.hq * D * sizeof(T));
+  geo.k_bytes = static_cast<unsigned>(a.hk * D * sizeof(T));
+  geo.stage_bytes = (geo.q_bytes + geo.k_bytes + 127u) & ~127u;
+  const size_t smem = BulkSmem<T, L>::bytes(NR_QKB_STAGES, geo.stage_bytes);
+  if (NR_QK_PATH == 1 && smem <= kBulkMaxSmem) return launch_bulk<T, WT, L>(a, turns, geo, smem, s);
   return launch_g<T, WT, L, false>(a, turns, s);
 }
 
@@ -418,6 +710,26 @@ cudaError_t launch_qk_norm_rope(void* q_out, void* k_out, const void* q, const v
   }
   if (w_is_bf16) return launch_w<float, __nv_bfloat16>(a, lanes, turns, stream);
   return launch_w<float, float>(a, lanes, turns, stream);
+}
+
+cudaError_t take_device_status(cudaStream_t stream, unsigned* bits) {
+  cudaError_t e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return e;
+  unsigned v = 0;
+  e = cudaMemcpyFromSymbol(&v, g_status_word, sizeof(v));
+  if (e != cudaSuccess) return e;
+  if (v != 0) {
+    const unsigned zero = 0;
+    e = cudaMemcpyToSymbol(g_status_word, &zero, sizeof(zero));
+    if (e != cudaSuccess) return e;
+  }
+  *bits = v;
+  return cudaSuccess;
+}
+
+cudaError_t launch_wait_probe(long long limit_cycles, cudaStream_t stream) {
+  wait_probe_kernel<<<1, 32, 0, stream>>>(limit_cycles);
+  return cudaGetLastError();
 }
 
 }  // namespace nr

@@ -12,7 +12,7 @@ import pytest
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "nr.h")
 
-OK, NULL, SHAPE, DTYPE, ALIGN, ALIAS, UNSUP, CUDA, VALUE = range(9)
+OK, NULL, SHAPE, DTYPE, ALIGN, ALIAS, UNSUP, CUDA, VALUE, TIMEOUT = range(10)
 F32, BF16 = 0, 1
 A = 0x7F0000000000  # fake, 16-byte aligned "device" addresses
 MB = 1 << 20
@@ -43,6 +43,8 @@ def lib(lib_path):
                                      i64, f32, cint, ctypes.POINTER(RopeConfig), cint, vp]
     L.nr_gated_residual_ln_modulate.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, f32, cint,
                                                 vp]
+    L.nr_test_wait_probe.argtypes = [i64, vp]
+    L.nr_device_status.argtypes = [vp]
     L.nr_status_string.argtypes = [cint]
     L.nr_status_string.restype = ctypes.c_char_p
     L.nr_last_error_message.restype = ctypes.c_char_p
@@ -69,6 +71,7 @@ def test_library_exports_every_declared_symbol(lib):
 def test_status_strings_and_version(lib):
     assert lib.nr_status_string(OK) == b"NR_OK"
     assert lib.nr_status_string(ALIAS) == b"NR_ERR_ALIAS"
+    assert lib.nr_status_string(TIMEOUT) == b"NR_ERR_TIMEOUT"
     assert lib.nr_status_string(99) == b"NR_ERR_UNKNOWN"
     assert lib.nr_version() >= 100
 
@@ -240,3 +243,11 @@ def test_rmsnorm_quant_fp8_validation(lib):
     assert quant(lib, codes=A + 128 * MB) == ALIAS  # codes over x
     assert quant(lib, nb=A) == ALIAS  # the two outputs
     assert quant(lib, res=A + 128 * MB) == ALIAS  # residual is x
+
+
+def test_wait_probe_limit_is_validated_before_launch(lib):
+    """Out-of-range limits are refused on the host (nothing is launched)."""
+    assert lib.nr_test_wait_probe(0, None) == VALUE
+    assert lib.nr_test_wait_probe(-5, None) == VALUE
+    assert lib.nr_test_wait_probe((1 << 32) + 1, None) == VALUE
+    assert b"limit_cycles" in lib.nr_last_error_message()

@@ -85,6 +85,20 @@ def test_token_and_head_counts(nr, tokens, hq, hk):
     run_case(nr, tokens, hq, hk, 128, seed=tokens + hq)
 
 
+@pytest.mark.parametrize("dtype,tokens,hq,hk,D", [(torch.bfloat16, 9, 48, 16, 512),
+                                                  (torch.float32, 7, 64, 64, 256)])
+def test_token_blocks_too_large_for_the_bulk_stages(nr, dtype, tokens, hq, hk, D):
+    """64 KB / 128 KB of Q and K rows per token: more than the bulk-copy
+    stages hold, so the per-warp ring kernel runs instead."""
+    run_case(nr, tokens, hq, hk, D, dtype=dtype, seed=hq + D)
+
+
+def test_many_tokens_per_block_with_gqa(nr):
+    """Enough tokens that every block cycles through its stages many times,
+    with fewer K heads than Q heads (a K block smaller than the Q block)."""
+    run_case(nr, 20000, 16, 2, 128, seed=41, chunk=5000)
+
+
 def test_large_and_negative_positions(nr):
     """Positions across the whole int32 range, in random order: the angle is
     reduced exactly, so large positions keep full accuracy."""

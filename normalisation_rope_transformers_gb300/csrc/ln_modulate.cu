@@ -55,6 +55,7 @@ __global__ void __launch_bounds__(ln_threads<WPR>()) ln_modulate_rows_kernel(
     T* __restrict__ out, const T* __restrict__ x, const T* __restrict__ shift,
     const T* __restrict__ scale, int64_t rows, int nvec, int64_t rows_per_sample, float hidden_f,
     float eps) {
+  pdl_enter();  // before any global read: the previous kernel may still run
   constexpr int N = Vec<T>::N;
   constexpr int THREADS = ln_threads<WPR>();
   constexpr int TPR = kWarp * WPR;       // threads per row
@@ -174,6 +175,7 @@ __global__ void __launch_bounds__(ln_threads<WPR>(), 4) gated_ln_modulate_kernel
     T* __restrict__ out, T* __restrict__ residual, const T* __restrict__ y,
     const T* __restrict__ gate, const T* __restrict__ shift, const T* __restrict__ scale,
     int64_t rows, int nvec, int64_t rows_per_sample, float hidden_f, float eps) {
+  pdl_enter();  // before any global read: the previous kernel may still run
   constexpr int N = Vec<T>::N;
   constexpr int THREADS = ln_threads<WPR>();
   constexpr int TPR = kWarp * WPR;
@@ -252,6 +254,7 @@ __global__ void __launch_bounds__(1024) ln_modulate_long_row_kernel(
     T* __restrict__ out, const T* __restrict__ x, const T* __restrict__ shift,
     const T* __restrict__ scale, int64_t nvec, int64_t rows_per_sample, float hidden_f,
     float eps) {
+  pdl_enter();  // before any global read: the previous kernel may still run
   constexpr int N = Vec<T>::N;
   __shared__ float scratch_mean[32];
   __shared__ float scratch_var[32];
@@ -311,10 +314,10 @@ cudaError_t launch_rows(const LnArgs& a, cudaStream_t s) {
   constexpr int RPB = THREADS / (kWarp * WPR);
   static_assert(RPB >= 1, "row groups must fit the block");
   const int64_t blocks = (a.rows + RPB - 1) / RPB;
-  ln_modulate_rows_kernel<T, VPT, WPR><<<dim3(static_cast<unsigned>(blocks)), THREADS, 0, s>>>(
+  return launch_pdl(ln_modulate_rows_kernel<T, VPT, WPR>, dim3(static_cast<unsigned>(blocks)),
+                    dim3(THREADS), 0, s,
       static_cast<T*>(a.out), static_cast<const T*>(a.x), static_cast<const T*>(a.shift),
       static_cast<const T*>(a.scale), a.rows, a.nvec, a.rps, a.hidden_f, a.eps);
-  return cudaGetLastError();
 }
 
 // Vectors per thread offered for one-warp rows, and for rows spread over
@@ -357,10 +360,10 @@ cudaError_t launch_typed(const LnArgs& a, cudaStream_t s) {
       default: break;
     }
   }
-  ln_modulate_long_row_kernel<T><<<dim3(static_cast<unsigned>(a.rows)), 1024, 0, s>>>(
+  return launch_pdl(ln_modulate_long_row_kernel<T>, dim3(static_cast<unsigned>(a.rows)), dim3(1024),
+                    0, s,
       static_cast<T*>(a.out), static_cast<const T*>(a.x), static_cast<const T*>(a.shift),
       static_cast<const T*>(a.scale), nvec, a.rps, a.hidden_f, a.eps);
-  return cudaGetLastError();
 }
 
 struct GatedArgs {
@@ -382,11 +385,11 @@ cudaError_t launch_gated_rows(const GatedArgs& a, cudaStream_t s) {
   constexpr int THREADS = ln_threads<WPR>();
   constexpr int RPB = THREADS / (kWarp * WPR);
   const int64_t blocks = (a.rows + RPB - 1) / RPB;
-  gated_ln_modulate_kernel<T, VPT, WPR><<<dim3(static_cast<unsigned>(blocks)), THREADS, 0, s>>>(
+  return launch_pdl(gated_ln_modulate_kernel<T, VPT, WPR>, dim3(static_cast<unsigned>(blocks)),
+                    dim3(THREADS), 0, s,
       static_cast<T*>(a.out), static_cast<T*>(a.residual), static_cast<const T*>(a.y),
       static_cast<const T*>(a.gate), static_cast<const T*>(a.shift),
       static_cast<const T*>(a.scale), a.rows, a.nvec, a.rps, a.hidden_f, a.eps);
-  return cudaGetLastError();
 }
 
 template <typename T>

@@ -74,6 +74,21 @@ __device__ __forceinline__ void st_plain(void* p, uint4 v) {
 }
 
 // ---------------------------------------------------------------------------
+// Programmatic dependent launch.  Every kernel of the library is launched with
+// programmatic stream serialisation, so it may be scheduled while the kernel
+// before it in the stream is still finishing.  pdl_enter, the first statement
+// of every kernel, lets the next kernel in the stream be scheduled early
+// (griddepcontrol.launch_dependents) and then waits until the previous kernel
+// has completed and its writes are visible (griddepcontrol.wait) -- so no
+// global memory is read before that, whoever launched the previous kernel.
+// Without a programmatic predecessor the wait returns at once.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_enter() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
 // Asynchronous global -> shared copies (cp.async).  Each thread copies its own
 // vectors and waits for its own copy groups; the data is then visible to that
 // thread (no other thread reads it), so no barrier is involved.  The wait is

@@ -5,7 +5,33 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 namespace nr {
+
+// 1: launch every kernel with programmatic stream serialisation (the kernels
+// wait for their predecessor on the device; see pdl_enter); 0: plain
+// stream-ordered launches.  A build-time knob.
+#ifndef NR_PDL
+#define NR_PDL 1
+#endif
+
+// Launch `kernel` on `stream` with programmatic stream serialisation.
+template <typename... Params, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = NR_PDL ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // Geometry of the row-resident kernels: one block per row, `threads` threads,
 // each owning up to `vpt` 128-bit vectors.  vpt == 0 selects the multi-pass

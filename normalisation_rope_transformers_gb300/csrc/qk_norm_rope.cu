@@ -102,6 +102,7 @@ struct QkSmem {
 template <typename T, typename WT, int L, int RING, bool GEN>
 __global__ void __launch_bounds__(kQkThreads) qk_norm_rope_kernel(const QkArgs a,
                                                                   const RopeTurns turns) {
+  pdl_enter();  // before any global read: the previous kernel may still run
   using S = QkSmem<T, L>;
   constexpr int N = Vec<T>::N;
   constexpr int HALF = S::HALF;
@@ -379,6 +380,7 @@ template <typename T, typename WT, int L, int NST>
 __global__ void __launch_bounds__(kBulkThreads) qk_norm_rope_bulk_kernel(const QkArgs a,
                                                                        const RopeTurns turns,
                                                                        const BulkGeom geo) {
+  pdl_enter();  // before any global read: the previous kernel may still run
   using S = BulkSmem<T, L>;
   constexpr int N = Vec<T>::N;
   constexpr int HALF = S::HALF;
@@ -602,10 +604,8 @@ cudaError_t launch_g(const QkArgs& a, const RopeTurns& turns, cudaStream_t s) {
       static_cast<int64_t>(sm_count(device)) * blocks_per_sm<T, WT, L, RING, GEN>(device);
   const int64_t needed = (a.tokens + kQkWarps - 1) / kQkWarps;  // one warp per token at most
   const int64_t blocks = needed < resident ? needed : resident;
-  qk_norm_rope_kernel<T, WT, L, RING, GEN><<<dim3(static_cast<unsigned>(blocks)), kQkThreads,
-                                             QkSmem<T, L>::bytes(RING, GEN ? 3 : 1), s>>>(a,
-                                                                                       turns);
-  return cudaGetLastError();
+  return launch_pdl(qk_norm_rope_kernel<T, WT, L, RING, GEN>, dim3(static_cast<unsigned>(blocks)),
+                    dim3(kQkThreads), QkSmem<T, L>::bytes(RING, GEN ? 3 : 1), s, a, turns);
 }
 
 // Largest shared memory the bulk variant may take per block (stages plus
@@ -641,8 +641,8 @@ cudaError_t launch_bulk(const QkArgs& a, const RopeTurns& turns, const BulkGeom&
   }
   const int64_t resident = static_cast<int64_t>(sm_count(device)) * last_blocks[device];
   const int64_t blocks = a.tokens < resident ? a.tokens : resident;
-  kernel<<<dim3(static_cast<unsigned>(blocks)), kBulkThreads, smem, s>>>(a, turns, geo);
-  return cudaGetLastError();
+  return launch_pdl(kernel, dim3(static_cast<unsigned>(blocks)), dim3(kBulkThreads), smem, s, a,
+                    turns, geo);
 }
 
 template <typename T, typename WT, int L>

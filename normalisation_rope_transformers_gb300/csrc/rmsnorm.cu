@@ -68,6 +68,7 @@ __global__ void __launch_bounds__(kRowMaxThreads) rmsnorm_row_kernel(const EPI e
                                                            T* __restrict__ res, int nvec,
                                                            float hidden_f, float eps,
                                                            float w_add) {
+  pdl_enter();  // before any global read: the previous kernel may still run
   constexpr int N = Vec<T>::N;
   __shared__ float scratch[32];
   const int64_t row_off = static_cast<int64_t>(blockIdx.x) * nvec;  // in vectors
@@ -138,6 +139,7 @@ __global__ void __launch_bounds__(1024) rmsnorm_long_row_kernel(T* __restrict__ 
                                                                 T* __restrict__ res, int64_t nvec,
                                                                 float hidden_f, float eps,
                                                                 float w_add) {
+  pdl_enter();  // before any global read: the previous kernel may still run
   constexpr int N = Vec<T>::N;
   __shared__ float scratch[32];
   const int64_t row_off = static_cast<int64_t>(blockIdx.x) * nvec;
@@ -183,14 +185,13 @@ cudaError_t launch_rows_pw(const RowLaunch& g, const EPI& epi, const void* x, co
   const dim3 grid(static_cast<unsigned>(rows));
   const dim3 block(g.threads);
   if (res != nullptr)
-    rmsnorm_row_kernel<T, VPT, true, PW, EPI><<<grid, block, 0, s>>>(
+    return launch_pdl(rmsnorm_row_kernel<T, VPT, true, PW, EPI>, grid, block, 0, s,
         epi, static_cast<const T*>(x), static_cast<const T*>(w), static_cast<T*>(res), nvec,
         hidden_f, eps, w_add);
   else
-    rmsnorm_row_kernel<T, VPT, false, PW, EPI><<<grid, block, 0, s>>>(
+    return launch_pdl(rmsnorm_row_kernel<T, VPT, false, PW, EPI>, grid, block, 0, s,
         epi, static_cast<const T*>(x), static_cast<const T*>(w), nullptr, nvec, hidden_f, eps,
         w_add);
-  return cudaGetLastError();
 }
 
 // Rows per launch up to which the weight is fetched together with the row.
@@ -239,14 +240,13 @@ cudaError_t launch_typed(void* out, const void* x, const void* w, void* res, int
   // Long rows: 1024 threads stride over the row twice.
   const dim3 grid(static_cast<unsigned>(rows));
   if (res != nullptr)
-    rmsnorm_long_row_kernel<T, true><<<grid, 1024, 0, s>>>(
+    return launch_pdl(rmsnorm_long_row_kernel<T, true>, grid, dim3(1024), 0, s,
         static_cast<T*>(out), static_cast<const T*>(x), static_cast<const T*>(w),
         static_cast<T*>(res), nvec, hidden_f, eps, w_add);
   else
-    rmsnorm_long_row_kernel<T, false><<<grid, 1024, 0, s>>>(
+    return launch_pdl(rmsnorm_long_row_kernel<T, false>, grid, dim3(1024), 0, s,
         static_cast<T*>(out), static_cast<const T*>(x), static_cast<const T*>(w), nullptr, nvec,
         hidden_f, eps, w_add);
-  return cudaGetLastError();
 }
 
 }  // namespace

@@ -92,6 +92,7 @@ template <typename T, int UNROLL, Act ACT>
 __global__ void __launch_bounds__(kSiluThreads) act_and_mul_kernel(T* __restrict__ out,
                                                                     const T* __restrict__ x,
                                                                     int64_t rows, int ivec) {
+  pdl_enter();  // before any global read: the previous kernel may still run
   constexpr int N = Vec<T>::N;
   const int col0 = blockIdx.x * (kSiluThreads * UNROLL) + threadIdx.x;
   for (int64_t row = blockIdx.y; row < rows; row += gridDim.y) {
@@ -127,9 +128,8 @@ cudaError_t launch_u(void* out, const void* x, int64_t rows, int ivec, cudaStrea
   const unsigned gx = static_cast<unsigned>((ivec + kSiluThreads * UNROLL - 1) /
                                             (kSiluThreads * UNROLL));
   const unsigned gy = static_cast<unsigned>(rows < kMaxGridY ? rows : kMaxGridY);
-  act_and_mul_kernel<T, UNROLL, ACT><<<dim3(gx, gy), kSiluThreads, 0, s>>>(
+  return launch_pdl(act_and_mul_kernel<T, UNROLL, ACT>, dim3(gx, gy), dim3(kSiluThreads), 0, s,
       static_cast<T*>(out), static_cast<const T*>(x), rows, ivec);
-  return cudaGetLastError();
 }
 
 template <typename T, Act ACT>

@@ -86,6 +86,11 @@ __device__ __forceinline__ float activate(float a) {
     return gelu_tanh<T>(a);
 }
 
+// Vectors of gate and of up per thread for large problems; a build-time knob.
+#ifndef NR_ACT_UNROLL
+#define NR_ACT_UNROLL 4
+#endif
+
 constexpr unsigned kMaxGridY = 65535;
 
 template <typename T, int UNROLL, Act ACT>
@@ -138,7 +143,7 @@ cudaError_t launch_typed(void* out, const void* x, int64_t rows, int64_t inter, 
   // Small problems (decode) spread one vector per thread over as many SMs as
   // possible; large ones give each thread more bytes in flight.
   if (static_cast<int64_t>(ivec) * rows >= int64_t(152) * 4 * kSiluThreads * 4)
-    return launch_u<T, 4, ACT>(out, x, rows, ivec, s);
+    return launch_u<T, NR_ACT_UNROLL, ACT>(out, x, rows, ivec, s);
   return launch_u<T, 1, ACT>(out, x, rows, ivec, s);
 }
 

@@ -32,7 +32,7 @@ LIB_PATH = os.path.join(_PKG, "libnormrope.so")
 
 if not os.path.exists(LIB_PATH):
     raise ImportError("%s is missing: build the CUDA library first "
-                      "(python -m normalisation_rope_transformers_gb300.build)" % LIB_PATH)
+                      "(python normalisation_rope_transformers_gb300/build.py)" % LIB_PATH)
 
 lib = ctypes.CDLL(LIB_PATH)
 

@@ -27,6 +27,11 @@
 //    on the host in double; the top 32 bits feed sincospif.  No f64 math runs
 //    on the device and no cos/sin table is read from HBM.
 //  * Head rows are read once and written once (in place allowed).
+#include <atomic>
+#include <map>
+#include <mutex>
+#include <utility>
+
 #include "nr_common.cuh"
 #include "nr_internal.h"
 
@@ -564,34 +569,36 @@ __global__ void wait_probe_kernel(long long limit) {
 
 // Resident blocks per SM of one kernel instantiation (with its dynamic shared
 // memory), cached per device; also raises the kernel's shared-memory limit.
+// (The host-side caches below may be filled by several threads at once; each
+// entry is an atomic, and a racing thread at worst repeats the query.)
 template <typename T, typename WT, int L, int RING, bool GEN>
 int blocks_per_sm(int device) {
-  static int cached[64] = {0};
+  static std::atomic<int> cached[64];
   if (device < 0 || device >= 64) return 1;
-  if (cached[device] == 0) {
+  int n = cached[device].load(std::memory_order_relaxed);
+  if (n == 0) {
     const size_t smem = QkSmem<T, L>::bytes(RING, GEN ? 3 : 1);
     cudaFuncSetAttribute(qk_norm_rope_kernel<T, WT, L, RING, GEN>,
                          cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    int n = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, qk_norm_rope_kernel<T, WT, L, RING, GEN>,
                                                       kQkThreads, smem) != cudaSuccess ||
         n < 1)
       n = 1;
-    cached[device] = n;
+    cached[device].store(n, std::memory_order_relaxed);
   }
-  return cached[device];
+  return n;
 }
 
 int sm_count(int device) {
-  static int cached[64] = {0};
+  static std::atomic<int> cached[64];
   if (device < 0 || device >= 64) return 1;
-  if (cached[device] == 0) {
-    int n = 0;
+  int n = cached[device].load(std::memory_order_relaxed);
+  if (n == 0) {
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, device) != cudaSuccess || n < 1)
       n = 1;
-    cached[device] = n;
+    cached[device].store(n, std::memory_order_relaxed);
   }
-  return cached[device];
+  return n;
 }
 
 template <typename T, typename WT, int L, bool GEN>
@@ -620,26 +627,32 @@ cudaError_t launch_bulk(const QkArgs& a, const RopeTurns& turns, const BulkGeom&
   int device = 0;
   cudaError_t e = cudaGetDevice(&device);
   if (e != cudaSuccess) return e;
-  // Per device: raise the shared-memory limit once; cache the occupancy of
-  // the last shared-memory size asked for.
-  static int limit_set[64] = {0};
-  static size_t last_smem[64] = {0};
-  static int last_blocks[64] = {0};
+  // Per device: raise the shared-memory limit once; cache the occupancy per
+  // shared-memory size (a few distinct head layouts at most).
+  static std::mutex mu;
+  static std::map<std::pair<int, size_t>, int> occupancy;
+  static std::atomic<int> limit_set[64];
   if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
-  if (!limit_set[device]) {
+  if (!limit_set[device].load(std::memory_order_acquire)) {
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(kBulkMaxSmem));
     if (e != cudaSuccess) return e;
-    limit_set[device] = 1;
+    limit_set[device].store(1, std::memory_order_release);
   }
-  if (last_smem[device] != smem) {
-    int n = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, kBulkThreads, smem);
+  int per_sm = 0;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = occupancy.find({device, smem});
+    if (it != occupancy.end()) per_sm = it->second;
+  }
+  if (per_sm == 0) {
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kBulkThreads, smem);
     if (e != cudaSuccess) return e;
-    last_blocks[device] = n < 1 ? 1 : n;
-    last_smem[device] = smem;
+    if (per_sm < 1) per_sm = 1;
+    std::lock_guard<std::mutex> lock(mu);
+    occupancy[{device, smem}] = per_sm;
   }
-  const int64_t resident = static_cast<int64_t>(sm_count(device)) * last_blocks[device];
+  const int64_t resident = static_cast<int64_t>(sm_count(device)) * per_sm;
   const int64_t blocks = a.tokens < resident ? a.tokens : resident;
   return launch_pdl(kernel, dim3(static_cast<unsigned>(blocks)), dim3(kBulkThreads), smem, s, a,
                     turns, geo);

@@ -100,3 +100,48 @@ def test_across_kernels(nr):
     check_bf16(host_bits(b), oracle.silu_and_mul(host_bits(a))[0], what="stage silu")
     _ln_check(c, host_bits(b), sh, sc, "stage ln")
     check_bf16(host_bits(d), oracle.gelu_and_mul(host_bits(c))[0], what="stage gelu")
+
+
+def test_host_threads_on_their_own_streams(nr):
+    """Four host threads, each on its own stream, launch Q/K calls with
+    different head layouts (first use of each launch configuration races in
+    the library's host-side caches) and LayerNorm calls; every result matches
+    the oracle."""
+    import threading
+
+    layouts = [(300, 8, 2, 128), (300, 16, 4, 64), (200, 32, 8, 128), (200, 4, 4, 256)]
+    inputs = [synth.qk_inputs(T, hq, hk, D, 70 + i, torch.bfloat16, torch.float32)
+              for i, (T, hq, hk, D) in enumerate(layouts)]
+    results = [None] * len(layouts)
+    errors = []
+
+    def work(i):
+        try:
+            q, k, wq, wk, pos = inputs[i]
+            s = torch.cuda.Stream()
+            with torch.cuda.stream(s):
+                qd, kd = q.cuda(non_blocking=False), k.cuda(non_blocking=False)
+                for _ in range(3):
+                    out = nr.qk_norm_rope(qd, kd, wq.cuda(), wk.cuda(), pos.cuda())
+                x = synth.tensor(80 + i, 0, (64, 1024), torch.bfloat16).cuda()
+                p = torch.zeros(1, 1024, dtype=torch.bfloat16, device="cuda")
+                ln = nr.ln_modulate(x, p, p)
+            s.synchronize()
+            results[i] = (out[0].cpu(), out[1].cpu(), x.cpu(), ln.cpu())
+        except Exception as exc:  # reported below, in the main thread
+            errors.append(exc)
+
+    threads = [threading.Thread(target=work, args=(i,)) for i in range(len(layouts))]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors
+    for (q, k, wq, wk, pos), (gq, gk, x, ln) in zip(inputs, results):
+        qo, ko, qy, ky, qm, km = oracle.qk_norm_rope(host_bits(q), host_bits(k), host_bits(wq),
+                                                     host_bits(wk), pos.numpy(), want_y=True)
+        check_bf16(host_bits(gq), qo, qy, qm, k_cancel=32, what="threaded rope q")
+        check_bf16(host_bits(gk), ko, ky, km, k_cancel=32, what="threaded rope k")
+        zero = np.zeros((1, 1024), np.uint16)
+        o_out, o_y, o_mag = oracle.ln_modulate(host_bits(x), zero, zero, want_y=True)
+        check_bf16(host_bits(ln), o_out, o_y, o_mag, k_cancel=K_LN, what="threaded ln")

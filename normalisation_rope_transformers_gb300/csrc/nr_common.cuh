@@ -184,6 +184,30 @@ __device__ __forceinline__ void bulk_load(unsigned dst, const void* src, unsigne
       : "memory");
 }
 
+// An L2 policy that evicts first the lines it covers (for data touched once).
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t policy;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(policy));
+  return policy;
+}
+
+// bulk_load / bulk_store with an L2 cache policy.
+__device__ __forceinline__ void bulk_load_hint(unsigned dst, const void* src, unsigned bytes,
+                                               unsigned bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], "
+      "%2, [%3], %4;" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_store_hint(void* dst, unsigned src, unsigned bytes,
+                                                uint64_t policy) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group.L2::cache_hint [%0], [%1], %2, %3;" ::"l"(
+                   dst),
+               "r"(src), "r"(bytes), "l"(policy)
+               : "memory");
+}
+
 // Asks L2 to fetch `bytes` from global memory (no completion to wait for).
 __device__ __forceinline__ void bulk_prefetch_l2(const void* src, unsigned bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");

@@ -349,6 +349,14 @@ __global__ void __launch_bounds__(kQkThreads) qk_norm_rope_kernel(const QkArgs a
 #ifndef NR_QKB_L2PF
 #define NR_QKB_L2PF 0
 #endif
+// L2 evict-first policy on the bulk loads (bit 0) and stores (bit 1); a
+// build-time knob.  Both (3): the token blocks are touched once, and written
+// lines leave L2 during this kernel instead of being written back while the
+// next kernel runs (measured: this kernel 0.9 us faster, a following
+// LayerNorm 1.7 us faster).
+#ifndef NR_QKB_HINT
+#define NR_QKB_HINT 3
+#endif
 
 // Warps per block (they split each token's head rows); a build-time knob.
 #ifndef NR_QKB_WARPS
@@ -436,13 +444,21 @@ __global__ void __launch_bounds__(kBulkThreads) qk_norm_rope_bulk_kernel(const Q
 
   // Producer (thread 0): bring local token j into its stage.
   int64_t issued = 0;
+  const uint64_t policy = NR_QKB_HINT ? l2_evict_first_policy() : 0;
   auto issue = [&](int64_t j) {
     const int64_t tok = t0 + j * C;
     const unsigned bar = smem_addr(bars + j % NST);
     mbar_arrive_expect_tx(bar, geo.q_bytes + geo.k_bytes);
-    bulk_load(smem_addr(stage(j)), q + tok * a.q_stride, geo.q_bytes, bar);
-    if (geo.k_bytes) bulk_load(smem_addr(stage(j) + geo.q_bytes), k + tok * a.k_stride,
-                               geo.k_bytes, bar);
+    if (NR_QKB_HINT & 1) {
+      bulk_load_hint(smem_addr(stage(j)), q + tok * a.q_stride, geo.q_bytes, bar, policy);
+      if (geo.k_bytes)
+        bulk_load_hint(smem_addr(stage(j) + geo.q_bytes), k + tok * a.k_stride, geo.k_bytes, bar,
+                       policy);
+    } else {
+      bulk_load(smem_addr(stage(j)), q + tok * a.q_stride, geo.q_bytes, bar);
+      if (geo.k_bytes) bulk_load(smem_addr(stage(j) + geo.q_bytes), k + tok * a.k_stride,
+                                 geo.k_bytes, bar);
+    }
     issued = j + 1;
     if (NR_QKB_L2PF > 0 && j + NR_QKB_L2PF < ntok) {
       const int64_t ptok = t0 + (j + NR_QKB_L2PF) * C;
@@ -533,9 +549,15 @@ __global__ void __launch_bounds__(kBulkThreads) qk_norm_rope_bulk_kernel(const Q
     __syncthreads();
     if (*abort_flag) break;
     if (tid == 0) {
-      bulk_store(q_out + tok * a.q_stride, smem_addr(st), geo.q_bytes);
-      if (geo.k_bytes) bulk_store(k_out + tok * a.k_stride, smem_addr(st + geo.q_bytes),
-                                  geo.k_bytes);
+      if (NR_QKB_HINT & 2) {
+        bulk_store_hint(q_out + tok * a.q_stride, smem_addr(st), geo.q_bytes, policy);
+        if (geo.k_bytes) bulk_store_hint(k_out + tok * a.k_stride, smem_addr(st + geo.q_bytes),
+                                         geo.k_bytes, policy);
+      } else {
+        bulk_store(q_out + tok * a.q_stride, smem_addr(st), geo.q_bytes);
+        if (geo.k_bytes) bulk_store(k_out + tok * a.k_stride, smem_addr(st + geo.q_bytes),
+                                    geo.k_bytes);
+      }
       bulk_commit();
       if (j + NST - 1 < ntok) {
         bulk_wait_read<1>();  // the stage of token j - 1 has been read out

@@ -581,9 +581,34 @@ def next_row_cases(nr, synth, torch, device, rows_override=None):
         o = torch.empty((rows, 3 * 5120), dtype=torch.bfloat16, device=device)
         return lambda: nr.gelu_and_mul(g, out=o), nbytes(g, o), rows
 
+    def rope_variant(**kw):
+        # Q/K [26598, 24, 128] bf16 (the Q/K workload's shape) with a RoPE variant
+        def make():
+            c = synth.QK_NORM_ROPE
+            t = n_rows(c["tokens"])
+            q, k, wq, wk, pos = synth.qk_inputs(t, c["hq"], c["hk"], c["head_dim"], 7,
+                                                torch.bfloat16, torch.float32)
+            if kw.get("mrope_sections"):
+                # three position rows (t, h, w), as a vision-language model's image tokens
+                pos = torch.stack([pos // 1024, (pos // 32) % 32, pos % 32]).to(torch.int32)
+            if kw.get("llama3"):
+                pos = (pos * 4).to(torch.int32)  # positions up to ~106k
+            q, k, wq, wk, pos = (v.to(device) for v in (q, k, wq, wk, pos))
+            qo, ko = torch.empty_like(q), torch.empty_like(k)
+            nb = nbytes(q, k, wq, wk, pos) + nbytes(qo, ko)
+            return (lambda: nr.qk_norm_rope_ex(q, k, wq, wk, pos, q_out=qo, k_out=ko, **kw), nb,
+                    t)
+        return make
+
     return [("gated_residual_ln_modulate_bf16_26598x3072", gated),
             ("rmsnorm_quant_fp8_bf16_8192x5120", quant),
-            ("gelu_and_mul_bf16_8192x30720", gelu)]
+            ("gelu_and_mul_bf16_8192x30720", gelu),
+            ("qk_norm_rope_mrope_bf16_26598x24x128", rope_variant(
+                mrope_sections=(16, 24, 24), theta=1e6)),
+            ("qk_norm_rope_gptj_rot64_bf16_26598x24x128", rope_variant(
+                rotary_dim=64, interleaved=True)),
+            ("qk_norm_rope_llama3_bf16_26598x24x128", rope_variant(
+                theta=500000.0, llama3=(8.0, 1.0, 4.0, 8192.0)))]
 
 
 def next_rows(nr, synth, torch, device, peak):

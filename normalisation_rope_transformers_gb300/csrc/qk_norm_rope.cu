@@ -576,6 +576,250 @@ __global__ void __launch_bounds__(kBulkThreads) qk_norm_rope_bulk_kernel(const Q
   }
 }
 
+// The bulk-copy kernel for two RoPE variants (kept as its own kernel so the
+// full-head NeoX kernel above is compiled exactly as measured): a rotary
+// dimension below head_dim (lanes past the rotated block carry two normed,
+// unrotated vectors) and GPT-J interleaved pairs.  The stages, the producer
+// and the bounded waits are those of the kernel above.  (M-RoPE runs the ring
+// kernel, measured faster for it.)
+template <typename T, typename WT, int L, int NST>
+__global__ void __launch_bounds__(kBulkThreads) qk_norm_rope_bulk_var_kernel(const QkArgs a,
+                                                                       const RopeTurns turns,
+                                                                       const BulkGeom geo) {
+  pdl_enter();  // before any global read: the previous kernel may still run
+  using S = BulkSmem<T, L>;
+  constexpr int N = Vec<T>::N;
+  constexpr int HALF = S::HALF;
+  constexpr int D = S::D;
+  constexpr int GW = kWarp / L;  // head rows per warp pass
+
+  // bulk copies need 16-byte aligned shared addresses: the stages start at the
+  // (16-byte aligned) base and every stage and K block offset is a multiple of 16
+  extern __shared__ __align__(16) unsigned char smem[];
+  unsigned char* stages = smem;
+  float2* table = reinterpret_cast<float2*>(stages + static_cast<size_t>(NST) * geo.stage_bytes);
+  float* wsm = reinterpret_cast<float*>(table + 2 * HALF);
+  unsigned long long* turn_sm = reinterpret_cast<unsigned long long*>(wsm + 2 * D);
+  unsigned long long* bars = turn_sm + HALF;
+  int* abort_flag = reinterpret_cast<int*>(bars + NST);
+
+  const int tid = threadIdx.x;
+  const int warp = tid / kWarp;
+  const int lane32 = tid % kWarp;
+  const WT* wq = static_cast<const WT*>(a.wq);
+  const WT* wk = static_cast<const WT*>(a.wk);
+  for (int i = tid; i < 2 * D; i += kBulkThreads) {
+    float wv = 0.0f;
+    if (i < D)
+      wv = load_w<WT>(wq, i);
+    else if (a.hk > 0)
+      wv = load_w<WT>(wk, i - D);
+    wsm[i] = wv + a.w_add;
+  }
+  for (int i = tid; i < HALF; i += kBulkThreads) turn_sm[i] = turns.turn[i];
+  if (tid == 0) {
+    for (int st = 0; st < NST; st++) mbar_init(smem_addr(bars + st), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  const int64_t C = gridDim.x;
+  const int64_t t0 = blockIdx.x;
+  const int64_t ntok = t0 < a.tokens ? (a.tokens - 1 - t0) / C + 1 : 0;  // this block's tokens
+  const int H = a.hq + a.hk;
+  const int IT = (H + GW - 1) / GW;
+  const T* q = static_cast<const T*>(a.q);
+  const T* k = static_cast<const T*>(a.k);
+  T* q_out = static_cast<T*>(a.q_out);
+  T* k_out = static_cast<T*>(a.k_out);
+  auto stage = [&](int64_t j) { return stages + (j % NST) * geo.stage_bytes; };
+
+  // Producer (thread 0): bring local token j into its stage.
+  int64_t issued = 0;
+  const uint64_t policy = NR_QKB_HINT ? l2_evict_first_policy() : 0;
+  auto issue = [&](int64_t j) {
+    const int64_t tok = t0 + j * C;
+    const unsigned bar = smem_addr(bars + j % NST);
+    mbar_arrive_expect_tx(bar, geo.q_bytes + geo.k_bytes);
+    if (NR_QKB_HINT & 1) {
+      bulk_load_hint(smem_addr(stage(j)), q + tok * a.q_stride, geo.q_bytes, bar, policy);
+      if (geo.k_bytes)
+        bulk_load_hint(smem_addr(stage(j) + geo.q_bytes), k + tok * a.k_stride, geo.k_bytes, bar,
+                       policy);
+    } else {
+      bulk_load(smem_addr(stage(j)), q + tok * a.q_stride, geo.q_bytes, bar);
+      if (geo.k_bytes) bulk_load(smem_addr(stage(j) + geo.q_bytes), k + tok * a.k_stride,
+                                 geo.k_bytes, bar);
+    }
+    issued = j + 1;
+    if (NR_QKB_L2PF > 0 && j + NR_QKB_L2PF < ntok) {
+      const int64_t ptok = t0 + (j + NR_QKB_L2PF) * C;
+      bulk_prefetch_l2(q + ptok * a.q_stride, geo.q_bytes);
+      if (geo.k_bytes) bulk_prefetch_l2(k + ptok * a.k_stride, geo.k_bytes);
+    }
+  };
+  if (tid == 0)
+    for (int64_t j = 0; j < NST - 1 && j < ntok; j++) issue(j);
+
+  // Angle table of a token into table buffer b: pairs of the rotated block.
+  const int rot_pairs = a.rot_vec * N / 2;
+  auto angles = [&](int b, int p) {
+    for (int i = tid; i < rot_pairs; i += kBulkThreads) {
+      const unsigned long long prod = static_cast<unsigned long long>(static_cast<long long>(p)) *
+                                      turn_sm[i];
+      const int hi = static_cast<int>(prod >> 32);  // signed turn fraction * 2^32
+      float sn, cn;
+      sincospif(static_cast<float>(hi) * 0x1p-31f, &sn, &cn);  // angle = pi * hi / 2^31
+      table[b * HALF + i] = make_float2(cn, sn);
+    }
+  };
+  int pos_next = 0;  // position of local token j + 1, loaded one token ahead
+  if (ntok > 0) {
+    if (tid < rot_pairs) {
+      angles(0, a.pos[t0]);
+      if (ntok > 1) pos_next = a.pos[t0 + C];
+    }
+  }
+  __syncthreads();
+
+  const int g = lane32 / L;
+  const int l = lane32 % L;
+  // The two vectors of the row this lane owns, as in the ring kernel:
+  // rotate-half lanes of the rotated block take vector l and its partner
+  // l + R/2; lanes past it take two unrotated vectors; interleaved: l, l + L.
+  int va_vec = l, vb_vec = l + L;
+  bool rotates = true;
+  if (!a.interleaved) {
+    const int half_rot = a.rot_vec / 2;
+    if (l < half_rot) {
+      vb_vec = l + half_rot;
+    } else {
+      va_vec = a.rot_vec + 2 * (l - half_rot);
+      vb_vec = va_vec + 1;
+      rotates = false;
+    }
+  }
+  int64_t j = 0;
+  for (; j < ntok; j++) {
+    const int64_t tok = t0 + j * C;
+    unsigned char* st = stage(j);
+    if (!mbar_wait_bounded(smem_addr(bars + j % NST), static_cast<unsigned>((j / NST) & 1),
+                           kWaitLimitCycles)) {
+      record_status(kStatusBitQkBulkWait);
+      *abort_flag = 1;
+    }
+    // this lane's (cos, sin) for the token
+    float2 cs[N];
+    const float2* tb = table + (j & 1) * HALF;
+    if (!a.interleaved) {
+      if (rotates) {
+#pragma unroll
+        for (int e = 0; e < N; e++) cs[e] = tb[l * N + e];
+      }
+    } else {
+#pragma unroll
+      for (int h = 0; h < N / 2; h++) {
+        if (va_vec < a.rot_vec) cs[h] = tb[va_vec * (N / 2) + h];
+        if (vb_vec < a.rot_vec) cs[N / 2 + h] = tb[vb_vec * (N / 2) + h];
+      }
+    }
+    for (int it = warp; it < IT; it += kBulkWarps) {  // uniform across the warp
+      const int row = it * GW + g;
+      // Lanes of a row past the last head carry zeros but still join the
+      // butterfly: the shuffles take the full warp.
+      const bool valid = row < H;
+      const bool is_q = row < a.hq;
+      uint4* r = reinterpret_cast<uint4*>(
+          st + (is_q ? 0u : geo.q_bytes) +
+          static_cast<size_t>(valid ? (is_q ? row : row - a.hq) : 0) * D * sizeof(T));
+      float xa[N], xb[N];
+      float ss = 0.0f;
+      if (valid) {
+        Vec<T>::unpack(r[va_vec], xa);
+        Vec<T>::unpack(r[vb_vec], xb);
+#pragma unroll
+        for (int e = 0; e < N; e++) {
+          ss = fmaf(xa[e], xa[e], ss);
+          ss = fmaf(xb[e], xb[e], ss);
+        }
+      }
+      ss = group_sum<L>(ss);
+      if (!valid) continue;
+      const float inv = rsqrtf(ss * a.inv_d + a.eps);
+      const float* w = wsm + (is_q ? 0 : D);
+      const float* wa = w + va_vec * N;
+      const float* wb = w + vb_vec * N;
+      float oa[N], ob[N];
+      if (!a.interleaved && rotates) {
+#pragma unroll
+        for (int e = 0; e < N; e++) {
+          const float na = xa[e] * inv * wa[e];
+          const float nb = xb[e] * inv * wb[e];
+          oa[e] = fmaf(na, cs[e].x, -nb * cs[e].y);
+          ob[e] = fmaf(na, cs[e].y, nb * cs[e].x);
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < N; e++) {
+          oa[e] = xa[e] * inv * wa[e];
+          ob[e] = xb[e] * inv * wb[e];
+        }
+        if (a.interleaved) {
+#pragma unroll
+          for (int h = 0; h < N / 2; h++) {
+            if (va_vec < a.rot_vec) {
+              const float x0 = oa[2 * h], x1 = oa[2 * h + 1];
+              oa[2 * h] = fmaf(x0, cs[h].x, -x1 * cs[h].y);
+              oa[2 * h + 1] = fmaf(x0, cs[h].y, x1 * cs[h].x);
+            }
+            if (vb_vec < a.rot_vec) {
+              const float x0 = ob[2 * h], x1 = ob[2 * h + 1];
+              ob[2 * h] = fmaf(x0, cs[N / 2 + h].x, -x1 * cs[N / 2 + h].y);
+              ob[2 * h + 1] = fmaf(x0, cs[N / 2 + h].y, x1 * cs[N / 2 + h].x);
+            }
+          }
+        }
+      }
+      r[va_vec] = Vec<T>::pack(oa);
+      r[vb_vec] = Vec<T>::pack(ob);
+    }
+    // the next token's angles, into the other table buffer
+    if (tid < rot_pairs && j + 1 < ntok) {
+      angles(static_cast<int>((j + 1) & 1), pos_next);
+      if (j + 2 < ntok) pos_next = a.pos[t0 + (j + 2) * C];
+    }
+    fence_proxy_async_smem();
+    __syncthreads();
+    if (*abort_flag) break;
+    if (tid == 0) {
+      if (NR_QKB_HINT & 2) {
+        bulk_store_hint(q_out + tok * a.q_stride, smem_addr(st), geo.q_bytes, policy);
+        if (geo.k_bytes) bulk_store_hint(k_out + tok * a.k_stride, smem_addr(st + geo.q_bytes),
+                                         geo.k_bytes, policy);
+      } else {
+        bulk_store(q_out + tok * a.q_stride, smem_addr(st), geo.q_bytes);
+        if (geo.k_bytes) bulk_store(k_out + tok * a.k_stride, smem_addr(st + geo.q_bytes),
+                                    geo.k_bytes);
+      }
+      bulk_commit();
+      if (j + NST - 1 < ntok) {
+        bulk_wait_read<1>();  // the stage of token j - 1 has been read out
+        issue(j + NST - 1);
+      }
+    }
+  }
+  if (tid == 0) {
+    bulk_wait<0>();  // every store has landed before the block's shared memory is released
+    // After an abandoned wait (at token j), let the loads still in flight
+    // finish (bounded); after a normal finish there are none (j == issued).
+    for (int64_t m = j; m < issued; m++)
+      if (!mbar_wait_bounded(smem_addr(bars + m % NST), static_cast<unsigned>((m / NST) & 1),
+                             kWaitLimitCycles))
+        break;
+  }
+}
+
 // A wait that nothing completes: one mbarrier with no arrivals, waited on for
 // `limit` cycles.  Exercises the expiry path that the real kernels take.
 __global__ void wait_probe_kernel(long long limit) {
@@ -641,11 +885,12 @@ cudaError_t launch_g(const QkArgs& a, const RopeTurns& turns, cudaStream_t s) {
 // tables): beyond it (very many heads per token) the ring kernel runs.
 constexpr size_t kBulkMaxSmem = 112 * 1024;
 
-template <typename T, typename WT, int L>
+template <typename T, typename WT, int L, bool VAR>
 cudaError_t launch_bulk(const QkArgs& a, const RopeTurns& turns, const BulkGeom& geo,
                         size_t smem, cudaStream_t s) {
   constexpr int NST = NR_QKB_STAGES;
-  auto kernel = qk_norm_rope_bulk_kernel<T, WT, L, NST>;
+  auto kernel = VAR ? qk_norm_rope_bulk_var_kernel<T, WT, L, NST>
+                    : qk_norm_rope_bulk_kernel<T, WT, L, NST>;
   int device = 0;
   cudaError_t e = cudaGetDevice(&device);
   if (e != cudaSuccess) return e;
@@ -683,7 +928,8 @@ cudaError_t launch_bulk(const QkArgs& a, const RopeTurns& turns, const BulkGeom&
 template <typename T, typename WT, int L>
 cudaError_t launch_l(const QkArgs& a, const RopeTurns& turns, cudaStream_t s) {
   const bool general = a.rot_vec != 2 * L || a.interleaved || a.mrope;
-  if (general) return launch_g<T, WT, L, true>(a, turns, s);
+  // M-RoPE: the ring kernel (measured faster for it than the bulk copies).
+  if (a.mrope) return launch_g<T, WT, L, true>(a, turns, s);
   // Whole tokens through shared memory when a token's rows fit the stages.
   constexpr int D = 2 * L * Vec<T>::N;
   BulkGeom geo;
@@ -691,8 +937,10 @@ cudaError_t launch_l(const QkArgs& a, const RopeTurns& turns, cudaStream_t s) {
   geo.k_bytes = static_cast<unsigned>(a.hk * D * sizeof(T));
   geo.stage_bytes = (geo.q_bytes + geo.k_bytes + 127u) & ~127u;
   const size_t smem = BulkSmem<T, L>::bytes(NR_QKB_STAGES, geo.stage_bytes);
-  if (NR_QK_PATH == 1 && smem <= kBulkMaxSmem) return launch_bulk<T, WT, L>(a, turns, geo, smem, s);
-  return launch_g<T, WT, L, false>(a, turns, s);
+  if (NR_QK_PATH == 1 && smem <= kBulkMaxSmem)
+    return general ? launch_bulk<T, WT, L, true>(a, turns, geo, smem, s)
+                   : launch_bulk<T, WT, L, false>(a, turns, geo, smem, s);
+  return general ? launch_g<T, WT, L, true>(a, turns, s) : launch_g<T, WT, L, false>(a, turns, s);
 }
 
 template <typename T, typename WT>

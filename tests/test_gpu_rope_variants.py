@@ -83,3 +83,38 @@ def test_all_at_once(nr):
     pos = torch.from_numpy(rng.integers(-1000, 100000, (3, T)).astype(np.int32))
     run_variant(nr, T, 5, 3, 256, seed=13, pos=pos, rotary_dim=128, interleaved=True,
                 llama3=LLAMA3, mrope_sections=(24, 20, 20), mrope_interleaved=True)
+
+
+@pytest.mark.parametrize("kw", [dict(rotary_dim=64), dict(rotary_dim=64, interleaved=True),
+                                dict(interleaved=True),
+                                dict(mrope_sections=(16, 24, 24), theta=1e6)],
+                         ids=["partial", "gptj_partial", "gptj", "mrope"])
+def test_variants_at_the_benchmark_shape(nr, kw):
+    """Q, K [26598, 24, 128] bf16 as in the benchmark: every block cycles its
+    stages through ~35 tokens.  Compared with the oracle on every element, in
+    token chunks."""
+    c = synth.QK_NORM_ROPE
+    T = c["tokens"]
+    q, k, wq, wk, pos = synth.qk_inputs(T, c["hq"], c["hk"], c["head_dim"], 17, torch.bfloat16,
+                                        torch.float32)
+    if kw.get("mrope_sections"):
+        pos = torch.stack([pos // 1024, (pos // 32) % 32, pos % 32]).to(torch.int32).contiguous()
+    qd, kd = dev(q), dev(k)
+    qo, ko = nr.qk_norm_rope_ex(qd, kd, dev(wq), dev(wk), dev(pos), **kw)
+    torch.cuda.synchronize()
+    gq, gk = host_bits(qo), host_bits(ko)
+    qb, kb = host_bits(q), host_bits(k)
+    for t0 in range(0, T, 4096):
+        t1 = min(t0 + 4096, T)
+        p = pos[..., t0:t1].contiguous().numpy()
+        ref = oracle.qk_norm_rope_ex(qb[t0:t1], kb[t0:t1], host_bits(wq), host_bits(wk), p,
+                                     want_y=True, **kw)
+        check_bf16(gq[t0:t1], ref[0], ref[2], ref[4], k_cancel=K_ROPE, what="rope-ex q %d" % t0)
+        check_bf16(gk[t0:t1], ref[1], ref[3], ref[5], k_cancel=K_ROPE, what="rope-ex k %d" % t0)
+
+
+def test_gptj_partial_many_tokens_gqa_and_odd_head_counts(nr):
+    """GQA (more Q heads than K heads) with head counts that leave the last
+    pass of a token partly empty, many tokens per block."""
+    run_variant(nr, 5003, 7, 3, 128, seed=19, rotary_dim=96, interleaved=True)
+    run_variant(nr, 4001, 5, 1, 64, seed=20, rotary_dim=32)

@@ -540,10 +540,38 @@ def run_e2e(args, torch, calls, device, world, barrier, step_bytes):
         import torch.distributed as dist
 
         ms = max_over_ranks(ms, dist, device)
+
+    # The same copies with no kernels (the host link's time for this step's
+    # transfers), for context: the end-to-end step cannot be faster.
+    def copies_only():
+        for c, hi, ho in zip(calls, h_in, h_out):
+            with torch.cuda.stream(s_in):
+                for k, v in hi.items():
+                    c.inputs[k].copy_(v, non_blocking=True)
+            with torch.cuda.stream(s_out):
+                for k, v in ho.items():
+                    v.copy_(c.outputs[k], non_blocking=True)
+
+    copies_only()
+    barrier()
+    s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s2.record(main)
+    for st in (s_in, s_out):
+        st.wait_stream(main)
+    for _ in range(n):
+        copies_only()
+    for st in (s_in, s_out):
+        main.wait_stream(st)
+    e2.record(main)
+    barrier()
+    copy_ms = s2.elapsed_time(e2) / n
     return {"value": round(world * step_bytes * n / (ms * 1e-3) / 1e9, 1), "unit": "GB/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n,
             "ms_per_step": round(ms / n, 3),
-            "note": "pinned host buffers; H2D, kernels and D2H on three streams ordered per call"}
+            "copies_only_ms_per_step": round(copy_ms, 3),
+            "frac_of_copies_only": round(copy_ms / (ms / n), 4),
+            "note": "pinned host buffers; H2D, kernels and D2H on three streams ordered per call; "
+                    "copies_only = the same transfers with no kernels (host-link bound)"}
 
 
 def next_row_cases(nr, synth, torch, device, rows_override=None):

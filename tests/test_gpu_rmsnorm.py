@@ -79,6 +79,17 @@ def test_edge_hidden_sizes(nr, dtype, residual, hidden):
     run_case(nr, 3, hidden, dtype, residual=residual, gemma=True, seed=hidden % 97)
 
 
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("rows,hidden", [(1, 8192), (1, 8200), (2, 5128), (5, 1032), (19, 4096),
+                                         (38, 2048), (75, 16392), (76, 4096), (77, 4096),
+                                         (160, 8200), (160, 16384), (160, 32768)])
+def test_few_and_many_rows(nr, dtype, rows, hidden):
+    """Row counts below and above the SM count (one CTA per row either way),
+    vectors-per-thread choices with idle slots, and the largest
+    register-resident rows next to the multi-pass kernel (32768 f32)."""
+    run_case(nr, rows, hidden, dtype, residual=True, gemma=True, seed=rows + hidden)
+
+
 @pytest.mark.parametrize("rows", [1, 2, 7, 1000])
 def test_edge_row_counts(nr, rows):
     run_case(nr, rows, 1024, torch.bfloat16, residual=True, seed=rows)

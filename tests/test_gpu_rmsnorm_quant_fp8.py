@@ -66,6 +66,14 @@ def test_edge_sizes(nr, dtype, hidden):
     run_case(nr, 3, hidden, dtype=dtype, residual=hidden % 3 == 0, seed=hidden % 31)
 
 
+@pytest.mark.parametrize("dtype,hidden", [(torch.bfloat16, 32768), (torch.bfloat16, 5128),
+                                          (torch.float32, 16384)])
+@pytest.mark.parametrize("rows", [1, 19, 160])
+def test_few_and_many_rows(nr, rows, dtype, hidden):
+    """One row, fewer rows than SMs and more, at the largest supported hidden."""
+    run_case(nr, rows, hidden, dtype=dtype, residual=True, seed=rows)
+
+
 def test_hidden_above_the_register_limit_is_refused(nr):
     x = torch.zeros(2, 16388, dtype=torch.float32, device="cuda")
     w = torch.ones(16388, dtype=torch.float32, device="cuda")

@@ -85,6 +85,39 @@ MUTANTS = [
     ("gelu 1 + tanh by direct sum", "z >= 0 ? 1.0 + tanh(z) :", "1 ? 1.0 + tanh(z) :"),
     ("gelu negative branch exponent", "2.0 * exp(2 * z) / (1.0 + exp(2 * z))",
      "2.0 * exp(z) / (1.0 + exp(2 * z))"),
+    ("bf16 subnormal grid one step too fine", "if (quantum_exp < -133) quantum_exp = -133;",
+     "if (quantum_exp < -134) quantum_exp = -134;"),
+    ("rope-ex: llama3 blend weights swapped", "return (1.0 - s) * f / factor + s * f;",
+     "return s * f / factor + (1.0 - s) * f;"),
+    ("rope-ex: llama3 high-frequency bound uses low", "if (wavelength < orig / high) return f;",
+     "if (wavelength < orig / low) return f;"),
+    ("rope-ex: pass-through part not normed", "store(dtype, dst, row0 + j, n[j]);",
+     "store(dtype, dst, row0 + j, load(dtype, src, row0 + j));"),
+    ("rope-ex: partner at D/2 instead of rot/2", "const int64_t b = interleaved ? 2 * i + 1 : i + rot / 2;",
+     "const int64_t b = interleaved ? 2 * i + 1 : i + D / 2;"),
+    ("rope-ex: mrope positions read token-major", "(double)pos[axis * tokens + t]",
+     "(double)pos[axis + 3 * t]"),
+    ("rope-ex: mrope interleaved w axis test", "if (i % 3 == 2 && i / 3 < sections[2]) return 2;",
+     "if (i % 3 == 2 && i / 3 < sections[1]) return 2;"),
+    ("rope position through f32", "const double angle = (double)pos[t] * freq;",
+     "const double angle = (double)(float)pos[t] * (double)(float)freq;"),
+    ("e4m3 subnormal step 2^-10", "return (uint8_t)(sign | (uint8_t)ldexp(r, 9));",
+     "return (uint8_t)(sign | (uint8_t)ldexp(r, 10));"),
+    ("e4m3 sign dropped", "const uint8_t sign = signbit(f) ? (uint8_t)0x80 : (uint8_t)0;",
+     "const uint8_t sign = 0;"),
+    ("fp8: gemma ignored in the quantised norm", "if (gemma) wj += 1.0;\n      const double yj = v * inv * wj;\n      const uint16_t nb",
+     "if (gemma) wj += 0.0;\n      const double yj = v * inv * wj;\n      const uint16_t nb"),
+    ("rope: gemma ignored", "if (gemma) wj += 1.0;\n        n[j] = load(dtype, src, base + j) * inv * wj;",
+     "if (gemma) wj += 0.0;\n        n[j] = load(dtype, src, base + j) * inv * wj;"),
+    ("rope-ex: gemma ignored", "if (gemma) wj += 1.0;\n        n[j] = load(dtype, src, row0 + j) * inv * wj;",
+     "if (gemma) wj += 0.0;\n        n[j] = load(dtype, src, row0 + j) * inv * wj;"),
+    ("silu: up dropped", "const double yj = a / (1.0 + exp(-a)) * b;", "const double yj = a / (1.0 + exp(-a));"),
+    ("gelu: up dropped", "const double yj = 0.5 * a * one_plus_tanh * b;",
+     "const double yj = 0.5 * a * one_plus_tanh;"),
+    ("ln: mean over hidden - 1", "const double mu = sum / (double)hidden;",
+     "const double mu = sum / (double)(hidden - 1);"),
+    ("gated: LayerNorm of the old residual", "nro_ln_modulate(dtype, rows, hidden, rows_per_sample, res_out,",
+     "nro_ln_modulate(dtype, rows, hidden, rows_per_sample, residual,"),
     ("silu exponent sign", "a / (1.0 + exp(-a)) * b", "a / (1.0 + exp(a)) * b"),
     ("silu gate and up swapped", "const double a = load(dtype, x, r * 2 * inter + j);\n      const double b = load(dtype, x, r * 2 * inter + inter + j);",
      "const double b = load(dtype, x, r * 2 * inter + j);\n      const double a = load(dtype, x, r * 2 * inter + inter + j);"),

@@ -454,6 +454,24 @@ def test_rope_ex_defaults_equal_the_plain_rope():
         assert np.array_equal(x, y)
 
 
+@pytest.mark.parametrize("variant", [{}, {"rotary_dim": 32}, {"interleaved": True}])
+def test_rope_gemma_adds_one_to_both_weights(variant):
+    """gemma uses w + 1 for the head norm ("attn_qk_norm_rope_gate"): with
+    weights whose w + 1 is exact, gemma on w equals gemma off on w + 1, for Q
+    and for K, in the plain kernel and the variants."""
+    q, k, _, _, _ = _qk_small(tokens=3, hq=2, hk=2, D=64, seed=94)
+    wq = ((np.arange(64) % 7) - 3).astype(np.float32) / 8
+    wk = ((np.arange(64) % 5) - 2).astype(np.float32) / 4
+    pos = np.array([0, 9, 4000], np.int32)
+    fn = oracle.qk_norm_rope_ex if variant else oracle.qk_norm_rope
+    a = fn(q, k, wq, wk, pos, gemma=True, want_y=True, **variant)
+    b = fn(q, k, wq + 1, wk + 1, pos, gemma=False, want_y=True, **variant)
+    for x, y in zip(a[:4], b[:4]):
+        assert np.array_equal(x, y)
+    c = fn(q, k, wq, wk, pos, gemma=False, want_y=True, **variant)
+    assert not np.array_equal(a[2], c[2]) and not np.array_equal(a[3], c[3])
+
+
 def _onehot_ex(idx, p, D=128, **kw):
     q = np.zeros((1, 1, D), np.float32)
     q[0, 0, idx] = 1.0
@@ -478,8 +496,10 @@ def test_rope_partial_rotary_pairs_and_unrotated_tail():
     wb = synth.to_oracle(torch.from_numpy(wq).to(torch.bfloat16))
     out = oracle.qk_norm_rope_ex(q, k, wb, wb, np.array([7, 70, 700], np.int32), rotary_dim=32,
                                  want_y=True)
-    _, _, ry = oracle.rmsnorm(q.reshape(-1, 64), wb, want_y=True)
+    ro, _, ry = oracle.rmsnorm(q.reshape(-1, 64), wb, want_y=True)
     assert np.array_equal(out[2].reshape(-1, 64)[:, 32:], ry[:, 32:])
+    # the stored tail too: the rounded normed value, not the input
+    assert np.array_equal(out[0].reshape(-1, 64)[:, 32:], ro[:, 32:])
 
 
 def test_rope_interleaved_pairs():
@@ -534,6 +554,18 @@ def test_mrope_axis_selection(interleaved):
         h_pairs = list(range(sec[0], sec[0] + sec[1]))
     changed = [i for i in range(16) if not np.allclose(c[2][..., i], b[2][..., i], atol=1e-14)]
     assert changed == h_pairs
+    # Moving one axis row at a time: each axis owns as many frequency pairs as
+    # its section says, and the three sets split the pairs between them.
+    owned = []
+    for axis in range(3):
+        moved = same.copy()
+        moved[axis] += 1000
+        c = oracle.qk_norm_rope_ex(q, k, wq, wk, moved, mrope_sections=sec,
+                                   mrope_interleaved=interleaved, want_y=True)
+        owned.append({i for i in range(16)
+                      if not np.allclose(c[2][..., i], b[2][..., i], atol=1e-14)})
+    assert [len(s) for s in owned] == list(sec)
+    assert set().union(*owned) == set(range(16))
 
 
 # --------------------------------------------------------------------------
@@ -621,9 +653,12 @@ def test_gated_unit_gate_is_the_residual_add():
     """gate = 1: the residual update is the plain residual add (pinned above)."""
     res, y, gate, shift, scale = _gated_inputs(6, 64, 82)
     one = bf16([[1.0] * 64])
-    _, res_out, _, _ = oracle.gated_ln_modulate(res, y, one, shift, scale)
+    out, res_out, _, _ = oracle.gated_ln_modulate(res, y, one, shift, scale)
     _, r2, _ = oracle.rmsnorm(y, bf16([1.0] * 64), residual=res)
     assert np.array_equal(res_out, r2)
+    # and the LayerNorm + modulation is taken of the updated residual
+    o2, _, _ = oracle.ln_modulate(r2, shift, scale, want_y=True)
+    assert np.array_equal(out, o2)
 
 
 def test_gated_residual_is_one_exact_rounding():

@@ -115,6 +115,46 @@ def nbytes(*ts):
     return sum(t.numel() * t.element_size() for t in ts if t is not None)
 
 
+def step_shapes(synth):
+    """(name, algorithmic bytes, rows, rows unit) of the seven calls of a step,
+    from the workload constants alone (the reference arm reports the same
+    configuration without building device buffers)."""
+    out = []
+    c = synth.RMSNORM_F32
+    n = c["rows"] * c["hidden"]
+    out.append(("rmsnorm_f32_64x1024", 4 * (2 * n + c["hidden"]), c["rows"], "rows"))
+    c = synth.ADD_RMSNORM
+    n = c["rows"] * c["hidden"]
+    for gemma in (0, 1):
+        out.append(("add_rmsnorm_bf16_8192x5120_gemma%d" % gemma, 2 * (4 * n + c["hidden"]),
+                    c["rows"], "rows"))
+    c = synth.QK_NORM_ROPE
+    n = c["tokens"] * (c["hq"] + c["hk"]) * c["head_dim"]
+    out.append(("qk_norm_rope_bf16_26598x24x128", 2 * 2 * n + 2 * 4 * c["head_dim"] + 4 * c["tokens"],
+                c["tokens"] * (c["hq"] + c["hk"]), "head rows"))
+    c = synth.LN_MODULATE
+    n = c["rows"] * c["hidden"]
+    out.append(("ln_modulate_bf16_26598x3072", 2 * (2 * n + 2 * c["hidden"]), c["rows"], "rows"))
+    c = synth.DECODE
+    rows, hidden = max(c["rows"]), max(c["hidden"])
+    out.append(("add_rmsnorm_bf16_256x8192", 2 * (4 * rows * hidden + hidden), rows, "rows"))
+    out.append(("silu_and_mul_bf16_256x49152", 2 * (rows * 6 * hidden + rows * 3 * hidden), rows,
+                "rows"))
+    return out
+
+
+def step_config(shapes, world):
+    """The `config` object of the JSON line (both arms)."""
+    step_bytes = sum(s[1] for s in shapes)
+    return {"workload": "dit_norm_step: " + " + ".join(s[0] for s in shapes),
+            "storage": "bf16 (f32 for the 64x1024 RMSNorm)",
+            "bytes_per_step": step_bytes,
+            "rows_per_step": {s[0]: s[2] for s in shapes},
+            "l2": "no flush: step footprint %.2f GB >> 129 MB L2; each large call's "
+                  "operands exceed L2" % (step_bytes / 1e9),
+            "parallelism": "dp%d (independent row/token shards, no collective)" % world}
+
+
 def build_step(nr, synth, torch, device, rank, only=None):
     """Device buffers and the seven calls of one step for this rank (only the
     calls whose name starts with `only`, when given)."""
@@ -348,6 +388,8 @@ def run_ours(args):
 
     calls = build_step(nr, synth, torch, device, rank)
     step_bytes = sum(c.nbytes for c in calls)
+    assert [(c.name, c.nbytes, c.rows) for c in calls] == [s[:3] for s in step_shapes(synth)], \
+        "step buffers disagree with the workload constants"
     stream = torch.cuda.current_stream(device)
 
     def step():
@@ -446,13 +488,7 @@ def run_ours(args):
         "warmup": max(args.warmup, 3), "ms_per_step": round(ms_per_step, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
-        "config": {"workload": "dit_norm_step: " + " + ".join(c.name for c in calls),
-                   "storage": "bf16 (f32 for the 64x1024 RMSNorm)",
-                   "bytes_per_step": step_bytes,
-                   "rows_per_step": {c.name: c.rows for c in calls},
-                   "l2": "no flush: step footprint %.2f GB >> 129 MB L2; each large call's "
-                         "operands exceed L2" % (step_bytes / 1e9),
-                   "parallelism": "dp%d (independent row/token shards, no collective)" % world},
+        "config": step_config([(c.name, c.nbytes, c.rows, c.rows_unit) for c in calls], world),
         "roofline": dict({"bound": "hbm", "kernel": dc.name, "achieved": round(achieved, 1),
                           "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                           "frac": round(achieved / peak, 4),
@@ -832,6 +868,8 @@ def run_reference(args):
     about two minutes."""
     if int(os.environ.get("RANK", "0")) != 0:
         return
+    import synth
+
     steps, warm = args.steps, max(args.warmup, 3)
     threads = oracle_threads()
     probe_fraction = 1.0 / 256
@@ -855,7 +893,7 @@ def run_reference(args):
         "n_gpus": args.gpus, "steps": steps, "warmup": warm,
         "ms_per_step": round(1e3 * total_s / steps, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": "dit_norm_step (oracle on a row sample of each call)"},
+        "config": step_config(step_shapes(synth), args.gpus),
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads,
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,

@@ -558,25 +558,6 @@ def run_e2e(args, torch, calls, device, world, barrier, step_bytes):
                 ev_out[j] = torch.cuda.Event()
                 ev_out[j].record(s_out)
 
-    step()
-    barrier()
-    n = max(args.e2e_steps, 1)
-    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    s.record(main)
-    for st in (s_in, s_k, s_out):
-        st.wait_stream(main)
-    for _ in range(n):
-        step()
-    for st in (s_in, s_k, s_out):
-        main.wait_stream(st)
-    e.record(main)
-    barrier()
-    ms = s.elapsed_time(e)
-    if world > 1:
-        import torch.distributed as dist
-
-        ms = max_over_ranks(ms, dist, device)
-
     # The same copies with no kernels (the host link's time for this step's
     # transfers), for context: the end-to-end step cannot be faster.
     def copies_only():
@@ -588,26 +569,49 @@ def run_e2e(args, torch, calls, device, world, barrier, step_bytes):
                 for k, v in ho.items():
                     v.copy_(c.outputs[k], non_blocking=True)
 
+    def window(fn, streams, steps):
+        """ms per step of `steps` back-to-back calls of fn, max over ranks."""
+        barrier()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(main)
+        for st in streams:
+            st.wait_stream(main)
+        for _ in range(steps):
+            fn()
+        for st in streams:
+            main.wait_stream(st)
+        e.record(main)
+        barrier()
+        ms = s.elapsed_time(e)
+        if world > 1:
+            import torch.distributed as dist
+
+            ms = max_over_ranks(ms, dist, device)
+        return ms / steps
+
+    step()
     copies_only()
-    barrier()
-    s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    s2.record(main)
-    for st in (s_in, s_out):
-        st.wait_stream(main)
-    for _ in range(n):
-        copies_only()
-    for st in (s_in, s_out):
-        main.wait_stream(st)
-    e2.record(main)
-    barrier()
-    copy_ms = s2.elapsed_time(e2) / n
-    return {"value": round(world * step_bytes * n / (ms * 1e-3) / 1e9, 1), "unit": "GB/s",
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n,
-            "ms_per_step": round(ms / n, 3),
-            "copies_only_ms_per_step": round(copy_ms, 3),
-            "frac_of_copies_only": round(copy_ms / (ms / n), 4),
+    # The host link is shared with the rest of the machine and its rate can
+    # drop for a while, so the two measurements alternate in short windows and
+    # each reports its median window.
+    n = max(args.e2e_steps, 1)
+    windows = 5
+    e2e_ms, copy_ms = [], []
+    for _ in range(windows):
+        e2e_ms.append(window(step, (s_in, s_k, s_out), n))
+        copy_ms.append(window(copies_only, (s_in, s_out), n))
+    ms = statistics.median(e2e_ms)
+    cms = statistics.median(copy_ms)
+    return {"value": round(world * step_bytes / (ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n * windows,
+            "ms_per_step": round(ms, 3),
+            "copies_only_ms_per_step": round(cms, 3),
+            "frac_of_copies_only": round(cms / ms, 4),
+            "windows_ms_per_step": [round(x, 3) for x in e2e_ms],
+            "copies_only_windows_ms_per_step": [round(x, 3) for x in copy_ms],
             "note": "pinned host buffers; H2D, kernels and D2H on three streams ordered per call; "
-                    "copies_only = the same transfers with no kernels (host-link bound)"}
+                    "copies_only = the same transfers with no kernels (host-link bound); %d "
+                    "alternating windows of %d steps each, medians reported" % (windows, n)}
 
 
 def next_row_cases(nr, synth, torch, device, rows_override=None):

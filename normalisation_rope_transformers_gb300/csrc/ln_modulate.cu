@@ -10,8 +10,8 @@
 // Design.  A row belongs to a group of WPR warps, the fewest that hold it
 // with at most 8 128-bit vectors per thread (16 at 8 warps): one warp up to
 // hidden 2048 bf16, two for the benchmark's 3072 (384 vectors = 6 per lane);
-// a block of 128 threads holds 4 / WPR groups (a row of 8 warps is its own
-// block).  The row is loaded once into registers, the mean and the centred
+// a block of 64 threads holds 2 / WPR groups (a row of 2 or more warps is its
+// own block).  The row is loaded once into registers, the mean and the centred
 // variance are two reductions over the register-resident values (warp
 // shuffles, plus one shared-memory step when WPR > 1), and the output is
 // written once.  Rows beyond 16 vectors per thread at 8 warps use a
@@ -33,6 +33,20 @@ __host__ __device__ constexpr int ln_threads() {
   return WPR > 4 ? kWarp * WPR : 128;
 }
 
+// Block size of the LayerNorm kernel (a build-time knob): 64 threads, i.e. one
+// row group of 2 warps per block for hidden 3072.  The same 20 rows are
+// resident per SM at 48 registers, but a row that finishes frees its slot
+// without waiting for a block-mate: measured 55.3 µs instead of 55.9 µs at
+// [26598, 3072] (ncu, 16384 rows: 34.6 instead of 36.3 µs).  The gated kernel
+// keeps 128-thread blocks (its register cap is chosen for them).
+#ifndef NR_LN_BLOCK
+#define NR_LN_BLOCK 64
+#endif
+template <int WPR>
+__host__ __device__ constexpr int ln_row_threads() {
+  return kWarp * WPR > NR_LN_BLOCK ? kWarp * WPR : NR_LN_BLOCK;
+}
+
 // Sum over the WPR warps of a row group; every thread of the group gets the
 // same total.  `scratch` holds one float per warp of the block; the caller
 // separates two uses of one scratch array by a barrier (or uses two arrays).
@@ -51,13 +65,13 @@ __device__ __forceinline__ float row_group_sum(float v, float* scratch) {
 }
 
 template <typename T, int VPT, int WPR>
-__global__ void __launch_bounds__(ln_threads<WPR>()) ln_modulate_rows_kernel(
+__global__ void __launch_bounds__(ln_row_threads<WPR>()) ln_modulate_rows_kernel(
     T* __restrict__ out, const T* __restrict__ x, const T* __restrict__ shift,
     const T* __restrict__ scale, int64_t rows, int nvec, int64_t rows_per_sample, float hidden_f,
     float eps) {
   pdl_enter();  // before any global read: the previous kernel may still run
   constexpr int N = Vec<T>::N;
-  constexpr int THREADS = ln_threads<WPR>();
+  constexpr int THREADS = ln_row_threads<WPR>();
   constexpr int TPR = kWarp * WPR;       // threads per row
   constexpr int RPB = THREADS / TPR;     // rows per block
   static_assert(RPB >= 1 && RPB * TPR == THREADS, "row groups must tile the block");
@@ -326,7 +340,7 @@ struct LnArgs {
 
 template <typename T, int VPT, int WPR>
 cudaError_t launch_rows(const LnArgs& a, cudaStream_t s) {
-  constexpr int THREADS = ln_threads<WPR>();
+  constexpr int THREADS = ln_row_threads<WPR>();
   constexpr int RPB = THREADS / (kWarp * WPR);
   static_assert(RPB >= 1, "row groups must fit the block");
   const int64_t blocks = (a.rows + RPB - 1) / RPB;

@@ -184,12 +184,12 @@ struct GatedAdd<__nv_bfloat16> {
   }
 };
 
-// Minimum resident blocks per SM asked of the compiler for the gated kernel
-// with bf16 rows of at most 6 vectors per thread and stream (a build-time
-// knob): 7 caps it at 72 registers without spills and keeps 7 blocks (14 rows
-// of 3072) in flight per SM, measured 3% faster than the 85-register build
-// (6 blocks) at [26598, 3072]; 8 (64 registers) spills.  Other geometries ask
-// for 4, which leaves them unspilled.
+// Resident 128-thread equivalents per SM asked of the compiler for the gated
+// kernel with bf16 rows of at most 6 vectors per thread and stream (a
+// build-time knob): 7 caps it at 72 registers without spills, so 14 rows of
+// 3072 are in flight per SM instead of 12 with the 85-register build
+// (measured 3% faster at [26598, 3072]); 8 (64 registers) spills.  Other
+// geometries ask for 4, which leaves them unspilled.
 #ifndef NR_GATED_MINB
 #define NR_GATED_MINB 7
 #endif
@@ -210,9 +210,8 @@ __host__ __device__ constexpr int gated_threads() {
 // any block size (NR_GATED_MINB is per 128 threads).
 template <typename T, int VPT, int WPR>
 __host__ __device__ constexpr int gated_min_blocks() {
-  return ((sizeof(T) == 2 && VPT <= 6) ? NR_GATED_MINB : 4) * 128 / gated_threads<WPR>() > 0
-             ? ((sizeof(T) == 2 && VPT <= 6) ? NR_GATED_MINB : 4) * 128 / gated_threads<WPR>()
-             : 1;
+  constexpr int per128 = (sizeof(T) == 2 && VPT <= 6) ? NR_GATED_MINB : 4;
+  return per128 * 128 / gated_threads<WPR>() > 0 ? per128 * 128 / gated_threads<WPR>() : 1;
 }
 
 template <typename T, int VPT, int WPR>

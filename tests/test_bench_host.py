@@ -1,0 +1,45 @@
+"""Host-side pieces of bench.py that every reported number depends on: the
+algorithmic bytes of each call (the numerator of every GB/s and of the
+roofline's `achieved`) and the config object both arms print.  CPU only.
+
+The expected byte counts are worked out here from the workload shapes alone
+(elements read plus elements written, times the element size), independently
+of how bench.py totals them."""
+import bench
+import synth
+
+MB = 1e6
+
+
+def test_algorithmic_bytes_of_each_call():
+    got = {name: (nbytes, rows, unit) for name, nbytes, rows, unit in bench.step_shapes(synth)}
+    # RMSNorm f32 [64, 1024]: read x and w, write out
+    assert got["rmsnorm_f32_64x1024"] == (4 * (64 * 1024 + 1024 + 64 * 1024), 64, "rows")
+    # add + RMSNorm bf16 [8192, 5120]: read x, residual, w; write residual, out
+    add = 2 * (8192 * 5120 * 2 + 5120 + 8192 * 5120 * 2)
+    assert got["add_rmsnorm_bf16_8192x5120_gemma0"] == (add, 8192, "rows")
+    assert got["add_rmsnorm_bf16_8192x5120_gemma1"] == (add, 8192, "rows")
+    assert abs(add / MB - 335.55) < 0.01
+    # Q/K [26598, 24 + 24, 128] bf16: read Q, K; write Q', K'; f32 weights; int32 positions
+    qk_rows = 26598 * 48
+    qk = 2 * 128 * qk_rows * 2 + 2 * 4 * 128 + 4 * 26598
+    assert got["qk_norm_rope_bf16_26598x24x128"] == (qk, qk_rows, "head rows")
+    assert abs(qk / MB - 653.78) < 0.01
+    # LN + modulation bf16 [26598, 3072]: read x, shift, scale; write out
+    ln = 2 * (26598 * 3072 * 2 + 2 * 3072)
+    assert got["ln_modulate_bf16_26598x3072"] == (ln, 26598, "rows")
+    assert abs(ln / MB - 326.85) < 0.01
+    # decode add + RMSNorm [256, 8192] and silu_and_mul [256, 2 x 24576]
+    assert got["add_rmsnorm_bf16_256x8192"] == (2 * (4 * 256 * 8192 + 8192), 256, "rows")
+    assert got["silu_and_mul_bf16_256x49152"] == (2 * (256 * 49152 + 256 * 24576), 256, "rows")
+    assert len(got) == 7
+
+
+def test_config_is_the_same_object_for_both_arms():
+    shapes = bench.step_shapes(synth)
+    cfg = bench.step_config(shapes, 1)
+    assert cfg["bytes_per_step"] == sum(s[1] for s in shapes) == 1706808216
+    assert cfg["workload"].startswith("dit_norm_step: rmsnorm_f32_64x1024 + ")
+    assert cfg["rows_per_step"]["qk_norm_rope_bf16_26598x24x128"] == 26598 * 48
+    assert cfg["parallelism"].startswith("dp1")
+    assert bench.step_config(shapes, 4)["parallelism"].startswith("dp4")

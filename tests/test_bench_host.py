@@ -43,3 +43,28 @@ def test_config_is_the_same_object_for_both_arms():
     assert cfg["rows_per_step"]["qk_norm_rope_bf16_26598x24x128"] == 26598 * 48
     assert cfg["parallelism"].startswith("dp1")
     assert bench.step_config(shapes, 4)["parallelism"].startswith("dp4")
+
+
+def test_algorithmic_bytes_of_the_next_rows():
+    """The next rows' byte counts at a few rows (device buffers built on the
+    CPU; nothing is launched)."""
+    import torch
+
+    r = 4
+    cases = dict(bench.next_row_cases(None, synth, torch, torch.device("cpu"), rows_override=r))
+    want = {
+        # read residual, y, gate, shift, scale; write residual, out
+        "gated_residual_ln_modulate_bf16_26598x3072": 2 * (4 * r * 3072 + 3 * 3072),
+        # read x, residual, w; write residual (bf16) and the codes (1 byte)
+        "rmsnorm_quant_fp8_bf16_8192x5120": 2 * (3 * r * 5120 + 5120) + r * 5120,
+        # read gate and up (2 x 15360), write out (15360)
+        "gelu_and_mul_bf16_8192x30720": 2 * (r * 30720 + r * 15360),
+    }
+    qk = 2 * 2 * r * 48 * 128 + 2 * 4 * 128
+    want["qk_norm_rope_mrope_bf16_26598x24x128"] = qk + 3 * 4 * r  # three position rows
+    want["qk_norm_rope_gptj_rot64_bf16_26598x24x128"] = qk + 4 * r
+    want["qk_norm_rope_llama3_bf16_26598x24x128"] = qk + 4 * r
+    assert set(cases) == set(want)
+    for name, make in cases.items():
+        _, nbytes, rows = make()
+        assert (nbytes, rows) == (want[name], r), name

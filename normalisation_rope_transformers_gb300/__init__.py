@@ -5,7 +5,7 @@ Each function marshals torch CUDA tensors into device pointers, sizes and the
 current CUDA stream, calls the entry point of the same name, and raises on a
 non-OK status.  Every step of the computation runs in the library's kernels;
 there is no CPU or PyTorch fallback.  Importing fails loudly when the library
-has not been built (``python -m normalisation_rope_transformers_gb300.build``
+has not been built (``python normalisation_rope_transformers_gb300/build.py``
 or ``__graft_entry__.build()``).
 
     rmsnorm(x, w, residual=None, eps=1e-6, gemma=False, out=None)

@@ -61,8 +61,12 @@ __device__ __forceinline__ void store_normed(const StoreFp8& e, int64_t vec_inde
 // One block per row; thread t owns vectors t, t + blockDim, ..., (VPT of them).
 // PW: load the weight together with the row (saves a dependent round trip when
 // there are few rows, e.g. decode; costs registers when there are many).
+// Threads per block of the few-row geometry (at most 2 vectors per thread).
+constexpr int kDecodeMaxThreads = 1024;
+
 template <typename T, int VPT, bool RES, bool PW, typename EPI>
-__global__ void __launch_bounds__(kRowMaxThreads) rmsnorm_row_kernel(const EPI epi,
+__global__ void __launch_bounds__((PW && VPT <= 2) ? kDecodeMaxThreads : kRowMaxThreads)
+    rmsnorm_row_kernel(const EPI epi,
                                                            const T* __restrict__ x,
                                                            const T* __restrict__ w,
                                                            T* __restrict__ res, int nvec,
@@ -206,12 +210,26 @@ cudaError_t launch_rows(const RowLaunch& g, const EPI& epi, const void* x, const
   return launch_rows_pw<T, VPT, false>(g, epi, x, w, res, rows, nvec, hidden_f, eps, w_add, s);
 }
 
+// Few rows (decode): at most 2 vectors per thread, up to kDecodeMaxThreads
+// threads, so each thread's chain of loads, adds and stores is short (a
+// build-time knob: 0 keeps the many-row geometry for every launch).
+#ifndef NR_RMS_DECODE_GEOM
+#define NR_RMS_DECODE_GEOM 1
+#endif
+
 // Launch the row kernel for the geometry picked for this row length; false
 // when the row is too long for it (the caller then needs the multi-pass kernel).
 template <typename T, typename EPI>
 bool launch_row_kernel(cudaError_t& err, const EPI& epi, const void* x, const void* w, void* res,
                        int64_t rows, int64_t nvec, float hidden_f, float eps, float w_add,
                        cudaStream_t s) {
+  if (NR_RMS_DECODE_GEOM && rows <= kPrefetchWeightRows && nvec > 2 * kRowMaxThreads / 2 &&
+      nvec <= 2 * kDecodeMaxThreads) {
+    const int nv = static_cast<int>(nvec);
+    const RowLaunch g{2, static_cast<int>(((nvec + 1) / 2 + 31) / 32 * 32)};
+    err = launch_rows_pw<T, 2, true>(g, epi, x, w, res, rows, nv, hidden_f, eps, w_add, s);
+    return true;
+  }
   const RowLaunch g = pick_row_launch(nvec);
   const int nv = static_cast<int>(nvec);
   switch (g.vpt) {

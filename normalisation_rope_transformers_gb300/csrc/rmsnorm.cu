@@ -212,10 +212,12 @@ cudaError_t launch_rows(const RowLaunch& g, const EPI& epi, const void* x, const
 
 // Few rows (decode): at most 2 vectors per thread, up to kDecodeMaxThreads
 // threads, so each thread's chain of loads, adds and stores is short (a
-// build-time knob: 0 keeps the many-row geometry for every launch).
+// build-time knob: 0 keeps the many-row geometry for every launch).  Used up
+// to the largest decode batch measured with it (256 rows).
 #ifndef NR_RMS_DECODE_GEOM
 #define NR_RMS_DECODE_GEOM 1
 #endif
+constexpr int64_t kDecodeGeomRows = 256;
 
 // Launch the row kernel for the geometry picked for this row length; false
 // when the row is too long for it (the caller then needs the multi-pass kernel).
@@ -223,7 +225,7 @@ template <typename T, typename EPI>
 bool launch_row_kernel(cudaError_t& err, const EPI& epi, const void* x, const void* w, void* res,
                        int64_t rows, int64_t nvec, float hidden_f, float eps, float w_add,
                        cudaStream_t s) {
-  if (NR_RMS_DECODE_GEOM && rows <= kPrefetchWeightRows && nvec > 2 * kRowMaxThreads / 2 &&
+  if (NR_RMS_DECODE_GEOM && rows <= kDecodeGeomRows && nvec > kRowMaxThreads &&
       nvec <= 2 * kDecodeMaxThreads) {
     const int nv = static_cast<int>(nvec);
     const RowLaunch g{2, static_cast<int>(((nvec + 1) / 2 + 31) / 32 * 32)};

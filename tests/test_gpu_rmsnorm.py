@@ -82,11 +82,14 @@ def test_edge_hidden_sizes(nr, dtype, residual, hidden):
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
 @pytest.mark.parametrize("rows,hidden", [(1, 8192), (1, 8200), (2, 5128), (5, 1032), (19, 4096),
                                          (38, 2048), (75, 16392), (76, 4096), (77, 4096),
-                                         (160, 8200), (160, 16384), (160, 32768)])
+                                         (160, 8200), (160, 16384), (160, 32768), (256, 8192),
+                                         (257, 8192), (1024, 5120), (1025, 5120)])
 def test_few_and_many_rows(nr, dtype, rows, hidden):
     """Row counts below and above the SM count (one CTA per row either way),
-    vectors-per-thread choices with idle slots, and the largest
-    register-resident rows next to the multi-pass kernel (32768 f32)."""
+    both sides of the few-row geometry (256 / 257 rows) and of the weight
+    prefetch (1024 / 1025 rows), vectors-per-thread choices with idle slots,
+    and the largest register-resident rows next to the multi-pass kernel
+    (32768 f32)."""
     run_case(nr, rows, hidden, dtype, residual=True, gemma=True, seed=rows + hidden)
 
 

@@ -118,6 +118,13 @@ MUTANTS = [
      "const double mu = sum / (double)(hidden - 1);"),
     ("gated: LayerNorm of the old residual", "nro_ln_modulate(dtype, rows, hidden, rows_per_sample, res_out,",
      "nro_ln_modulate(dtype, rows, hidden, rows_per_sample, residual,"),
+    ("fp8: residual not rounded before squaring",
+     "if (res_in != NULL) {\n        v = round_to(dtype, v + load(dtype, res_in, base + j));",
+     "if (res_in != NULL) {\n        store(dtype, res_out, base + j, v + load(dtype, res_in, base + j)); v = v + load(dtype, res_in, base + j);"),
+    ("fp8: eps outside the sqrt", "const double inv = 1.0 / sqrt(sum_sq / (double)hidden + eps);",
+     "const double inv = 1.0 / (sqrt(sum_sq / (double)hidden) + eps);"),
+    ("fp8: mean over h-1", "const double inv = 1.0 / sqrt(sum_sq / (double)hidden + eps);",
+     "const double inv = 1.0 / sqrt(sum_sq / (double)(hidden - 1) + eps);"),
     ("silu exponent sign", "a / (1.0 + exp(-a)) * b", "a / (1.0 + exp(a)) * b"),
     ("silu gate and up swapped", "const double a = load(dtype, x, r * 2 * inter + j);\n      const double b = load(dtype, x, r * 2 * inter + inter + j);",
      "const double b = load(dtype, x, r * 2 * inter + j);\n      const double a = load(dtype, x, r * 2 * inter + inter + j);"),

@@ -428,6 +428,28 @@ void nro_ln_modulate(int dtype, int64_t rows, int64_t hidden, int64_t rows_per_s
 }
 
 /* ------------------------------------------------------------------------ */
+/* a + b rounded to odd in double: the exact sum when it is a double, else    */
+/* whichever of the two doubles around it has an odd last significand bit.   */
+/* Rounding to odd in a format with at least two more significand bits than  */
+/* the target, then to nearest in the target, rounds the exact value once     */
+/* (Boldo and Melquiond, "Emulation of FMA and correctly rounded sums: proved */
+/* algorithms using rounding to odd", IEEE Trans. Computers 57(4), 2008).     */
+/* The error of the nearest sum comes from Knuth's TwoSum (TAOCP vol. 2,      */
+/* 4.2.2), exact in the default rounding mode.                                */
+/* ------------------------------------------------------------------------ */
+static double sum_round_to_odd(double a, double b) {
+  const double s = a + b;
+  const double bb = s - a;
+  const double err = (a - (s - bb)) + (b - bb); /* a + b = s + err exactly */
+  if (err == 0.0) return s;
+  /* the exact sum lies strictly between s and its neighbour toward err */
+  const double other = nextafter(s, err > 0.0 ? INFINITY : -INFINITY);
+  uint64_t bits;
+  memcpy(&bits, &s, sizeof bits);
+  return (bits & 1u) ? s : other;
+}
+
+/* ------------------------------------------------------------------------ */
 /* Gated residual add + LayerNorm + adaLN modulation: the DiT step around the */
 /* fused LayerNorm + modulation ([PAN2], as read above):                      */
 /*   v_j = round_dtype(residual_j + gate_j * y_j)   (the exact value, rounded */
@@ -442,11 +464,12 @@ void nro_gated_ln_modulate(int dtype, int64_t rows, int64_t hidden, int64_t rows
   for (int64_t r = 0; r < rows; r++) {
     const int64_t sample = (r / rows_per_sample) * hidden;
     for (int64_t j = 0; j < hidden; j++) {
-      /* gate*y is exact in double (at most 48 significant bits); the sum is
-       * rounded once to double and then to the storage dtype, which equals
-       * rounding the exact sum once (53 >= 2p + 2 for p = 8 and p = 24). */
-      const double v = load(dtype, residual, r * hidden + j) +
-                       load(dtype, gate, sample + j) * load(dtype, y, r * hidden + j);
+      /* gate*y is exact in double (at most 2*24 = 48 significant bits).  The
+       * sum with the residual is rounded to odd in double (53 >= 24 + 2
+       * bits), so the store's rounding to nearest rounds the exact
+       * residual + gate*y once. */
+      const double gy = load(dtype, gate, sample + j) * load(dtype, y, r * hidden + j);
+      const double v = sum_round_to_odd(load(dtype, residual, r * hidden + j), gy);
       store(dtype, res_out, r * hidden + j, v);
     }
   }

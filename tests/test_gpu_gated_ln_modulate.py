@@ -104,6 +104,31 @@ def test_residual_rounds_the_exact_value_at_f32_midpoints(nr):
     run_case(nr, res, y, gate, zero, zero)
 
 
+def test_f32_residual_rounds_the_exact_value_near_f32_midpoints(nr):
+    """f32 cases whose exact r + g*y sits 2^(e-70) j^2 away from an f32
+    midpoint: r = m 2^e with m odd, g = 1 - j 2^-23, y = +-2^(e-24)(1 + j 2^-23),
+    so g*y = +-(half an ulp of r)(1 - j^2 2^-46).  The sum rounded to double
+    lands on the midpoint and ties to even, picking the wrong neighbour; the one
+    rounding of the exact value keeps r.  Both signs of r and of y."""
+    hidden = 256
+    rng = np.random.default_rng(10)
+    e = rng.integers(-20, 20, hidden)
+    m = (2 ** 23 + 2 * rng.integers(0, 2 ** 22 - 1, hidden) + 1).astype(np.float64)  # odd
+    r = np.ldexp(m, e - 23) * np.where(rng.random(hidden) < 0.5, -1.0, 1.0)
+    j = rng.integers(1, 64, hidden).astype(np.float64)
+    g = 1 - j * 2.0 ** -23
+    y = np.ldexp(1 + j * 2.0 ** -23, e - 24) * np.where(rng.random(hidden) < 0.5, -1.0, 1.0)
+    # m in (2^23, 2^24) keeps r +- half an ulp inside r's binade; all values are f32-exact
+    r, g, y = (torch.from_numpy(a[None]).float() for a in (r, g, y))
+    zero = torch.zeros(1, hidden, dtype=torch.float32)
+    naive = (r.double() + g.double() * y.double()).float()
+    _, o_res, _, _ = oracle.gated_ln_modulate(host_bits(r), host_bits(y), host_bits(g),
+                                              host_bits(zero), host_bits(zero))
+    assert (host_bits(naive) != o_res).sum() >= hidden // 4  # the construction bites
+    assert np.array_equal(o_res, host_bits(r))  # exact value rounds back to r
+    run_case(nr, r, y, g, zero, zero)
+
+
 def test_zero_rows_is_a_no_op(nr):
     z = torch.empty(0, 64, dtype=torch.bfloat16, device="cuda")
     p = torch.zeros(1, 64, dtype=torch.bfloat16, device="cuda")

@@ -55,8 +55,14 @@ MUTANTS = [
     ("ln eps outside the sqrt", "1.0 / sqrt(var + eps)", "1.0 / (sqrt(var) + eps)"),
     ("gated: gate ignored", "load(dtype, gate, sample + j) * load(dtype, y, r * hidden + j)",
      "load(dtype, y, r * hidden + j)"),
-    ("gated: gate on the residual", "const double v = load(dtype, residual, r * hidden + j) +\n                       load(dtype, gate, sample + j) * load(dtype, y, r * hidden + j);",
-     "const double v = load(dtype, residual, r * hidden + j) * load(dtype, gate, sample + j) +\n                       load(dtype, y, r * hidden + j);"),
+    ("gated: gate on the residual",
+     "const double gy = load(dtype, gate, sample + j) * load(dtype, y, r * hidden + j);\n      const double v = sum_round_to_odd(load(dtype, residual, r * hidden + j), gy);",
+     "const double gy = load(dtype, gate, sample + j) * load(dtype, residual, r * hidden + j);\n      const double v = sum_round_to_odd(load(dtype, y, r * hidden + j), gy);"),
+    ("gated: sum rounded to nearest double, then to the dtype",
+     "const double v = sum_round_to_odd(load(dtype, residual, r * hidden + j), gy);",
+     "const double v = load(dtype, residual, r * hidden + j) + gy;"),
+    ("gated: round to odd keeps the even neighbour", "return (bits & 1u) ? s : other;",
+     "return (bits & 1u) ? other : s;"),
     ("gated: sample index", "const int64_t sample = (r / rows_per_sample) * hidden;\n    for (int64_t j = 0; j < hidden; j++) {\n      /* gate",
      "const int64_t sample = (r % rows_per_sample) * hidden;\n    for (int64_t j = 0; j < hidden; j++) {\n      /* gate"),
     ("rope-ex: head stride", "const int64_t row0 = t * tok_stride + h * D;",

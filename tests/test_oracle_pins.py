@@ -85,6 +85,19 @@ def _nearest_bf16_exact(d: float) -> int:
     return best[1]
 
 
+def _nearest_f32_exact(x: Fraction) -> Fraction:
+    """Brute force: the f32 value nearest to the rational x, ties to the even
+    pattern, among the five values around a guess (normal range only)."""
+    guess = np.float32(float(x))
+    cands = [guess]
+    for _ in range(2):
+        cands = ([np.nextafter(cands[0], np.float32(-np.inf), dtype=np.float32)] + cands
+                 + [np.nextafter(cands[-1], np.float32(np.inf), dtype=np.float32)])
+    best = min(cands, key=lambda c: (abs(Fraction(float(c)) - x),
+                                     int(np.array([c], np.float32).view(np.uint32)[0]) & 1))
+    return Fraction(float(best))
+
+
 def test_bf16_rounding_exact_brute_force_on_doubles():
     rng = np.random.default_rng(11)
     d = rng.standard_normal(4000) * np.exp2(rng.integers(-120, 120, 4000))
@@ -697,6 +710,44 @@ def test_gated_residual_rounds_exactly_at_f32_midpoints():
         exact = Fraction(mid) + Fraction(bf16_to_f64(r)[0, j])
         assert res_out[0, j] == _nearest_bf16_exact(float(exact))
     assert list(res_out[0]) == [0x3F82, 0x3F81]
+
+
+def test_gated_f32_residual_rounds_once_below_a_midpoint():
+    """f32: r = 1 + 2^-23, g = 1 - 2^-23, y = 2^-24 (1 + 2^-23).  The exact
+    r + g*y is 1 + 2^-23 + 2^-24 - 2^-70, just below the midpoint between
+    1 + 2^-23 and 1 + 2^-22, so the one rounding gives 1 + 2^-23 (0x3f800001).
+    Rounding the sum to double first lands on the midpoint, which then ties to
+    even (0x3f800002): the double rounding this pin rules out."""
+    r = f32([[1 + 2.0 ** -23, -(1 + 2.0 ** -23)]])
+    g = f32([[1 - 2.0 ** -23, 1 - 2.0 ** -23]])
+    yv = f32([[2.0 ** -24 * (1 + 2.0 ** -23), -(2.0 ** -24 * (1 + 2.0 ** -23))]])
+    zero = f32([[0.0, 0.0]])
+    _, res_out, _, _ = oracle.gated_ln_modulate(r, yv, g, zero, zero)
+    assert list(res_out.view(np.uint32)[0]) == [0x3F800001, 0xBF800001]
+
+
+def test_gated_f32_residual_is_one_exact_rounding():
+    """f32 round(r + g*y) against exact rational arithmetic, with g*y placed
+    near the f32 rounding midpoints of r (where a second rounding would show)
+    and over wide exponent gaps."""
+    rng = np.random.default_rng(84)
+    rows, hidden = 8, 64
+    r = (rng.standard_normal((rows, hidden)) * np.exp2(rng.integers(-8, 8, (rows, hidden))))
+    r = r.astype(np.float32)
+    g = (1 + rng.integers(-2 ** 20, 2 ** 20, (rows, hidden)) * 2.0 ** -23).astype(np.float32)
+    # y near half an f32 ulp of r (divided by g), nudged by a few ulps of y
+    half_ulp = np.spacing(np.abs(r)).astype(np.float64) / 2
+    y = (half_ulp / g.astype(np.float64)).astype(np.float32)
+    y = (y * (1 + rng.integers(-3, 4, (rows, hidden)) * 2.0 ** -23)).astype(np.float32)
+    y[rows // 2:] = (rng.standard_normal((rows - rows // 2, hidden))
+                     * np.exp2(rng.integers(-30, 10, (rows - rows // 2, hidden)))).astype(np.float32)
+    y *= np.where(rng.random((rows, hidden)) < 0.5, -1, 1).astype(np.float32)
+    zero = np.zeros((1, hidden), np.float32)
+    for i in range(rows):
+        _, res_out, _, _ = oracle.gated_ln_modulate(r[i:i + 1], y[i:i + 1], g[i:i + 1], zero, zero)
+        for j in range(hidden):
+            exact = Fraction(float(r[i, j])) + Fraction(float(g[i, j])) * Fraction(float(y[i, j]))
+            assert Fraction(float(res_out[0, j])) == _nearest_f32_exact(exact), (i, j)
 
 
 def test_gated_per_sample_gate_rows():

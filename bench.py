@@ -42,6 +42,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "achieved HBM GB/s and % of GB300 peak per fused norm kernel; rows/sec"
 NOMINAL_HBM_GBS = 8000.0
+L2_BYTES = 129e6
 FALLBACK_HBM_GBS = 6800.0
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.json")
 KERNEL_SOURCES = {
@@ -68,7 +69,34 @@ def parse_args():
                         "gelu_and_mul) --steps times, "
                         "for ncu; --rows overrides its row/token count; prints no JSON")
     p.add_argument("--rows", type=int, default=None)
+    p.add_argument("--config", type=int, choices=sorted(CONFIG_CALLS), default=None,
+                   help="time only the calls of one workload: 1 RMSNorm f32 64x1024, "
+                        "2 add + RMSNorm bf16 8192x5120 (gemma off and on), 3 Q/K norm + RoPE "
+                        "[26598, 24, 128], 4 LayerNorm + modulation [26598, 3072], 5 the decode "
+                        "pair [256, 8192] (and the decode sweep); default: all of them")
+    p.add_argument("--seed", type=int, default=None,
+                   help="seed of every synthetic input (default: each workload's own seed)")
     return p.parse_args()
+
+
+# The step's calls that belong to each workload (--config).
+CONFIG_CALLS = {
+    1: ("rmsnorm_f32_64x1024",),
+    2: ("add_rmsnorm_bf16_8192x5120_gemma0", "add_rmsnorm_bf16_8192x5120_gemma1"),
+    3: ("qk_norm_rope_bf16_26598x24x128",),
+    4: ("ln_modulate_bf16_26598x3072",),
+    5: ("add_rmsnorm_bf16_256x8192", "silu_and_mul_bf16_256x49152"),
+}
+
+
+def apply_workload_args(args, synth):
+    """--seed replaces the seed of every workload's inputs (the tensors keep
+    their own substreams); returns the call names --config selects (None: all)."""
+    if args.seed is not None:
+        for c in (synth.RMSNORM_F32, synth.ADD_RMSNORM, synth.QK_NORM_ROPE, synth.LN_MODULATE,
+                  synth.DECODE):
+            c["seed"] = int(args.seed)
+    return None if args.config is None else CONFIG_CALLS[args.config]
 
 
 # ---------------------------------------------------------------------------
@@ -115,10 +143,11 @@ def nbytes(*ts):
     return sum(t.numel() * t.element_size() for t in ts if t is not None)
 
 
-def step_shapes(synth):
-    """(name, algorithmic bytes, rows, rows unit) of the seven calls of a step,
-    from the workload constants alone (the reference arm reports the same
-    configuration without building device buffers)."""
+def step_shapes(synth, selected=None):
+    """(name, algorithmic bytes, rows, rows unit) of the seven calls of a step
+    (those named in `selected`, when given), from the workload constants alone
+    (the reference arm reports the same configuration without building device
+    buffers)."""
     out = []
     c = synth.RMSNORM_F32
     n = c["rows"] * c["hidden"]
@@ -140,7 +169,7 @@ def step_shapes(synth):
     out.append(("add_rmsnorm_bf16_256x8192", 2 * (4 * rows * hidden + hidden), rows, "rows"))
     out.append(("silu_and_mul_bf16_256x49152", 2 * (rows * 6 * hidden + rows * 3 * hidden), rows,
                 "rows"))
-    return out
+    return [o for o in out if selected is None or o[0] in selected]
 
 
 def step_config(shapes, world):
@@ -150,19 +179,22 @@ def step_config(shapes, world):
             "storage": "bf16 (f32 for the 64x1024 RMSNorm)",
             "bytes_per_step": step_bytes,
             "rows_per_step": {s[0]: s[2] for s in shapes},
-            "l2": "no flush: step footprint %.2f GB >> 129 MB L2; each large call's "
-                  "operands exceed L2" % (step_bytes / 1e9),
+            "l2": ("no flush: step footprint %.2f GB >> 129 MB L2; each large call's "
+                   "operands exceed L2" % (step_bytes / 1e9) if step_bytes > 2 * L2_BYTES else
+                   "no flush: step footprint %.1f MB fits in the 129 MB L2, so steps after the "
+                   "first run from L2 (decode-latency regime)" % (step_bytes / 1e6)),
             "parallelism": "dp%d (independent row/token shards, no collective)" % world}
 
 
-def build_step(nr, synth, torch, device, rank, only=None):
+def build_step(nr, synth, torch, device, rank, only=None, selected=None):
     """Device buffers and the seven calls of one step for this rank (only the
-    calls whose name starts with `only`, when given)."""
+    calls whose name starts with `only`, or is in `selected`, when given)."""
     bf16, f32 = torch.bfloat16, torch.float32
     calls = []
 
     def want(name):
-        return only is None or name.startswith(only)
+        return ((only is None or name.startswith(only))
+                and (selected is None or name in selected))
 
     c = synth.RMSNORM_F32
     if want("rmsnorm_f32_64x1024"):
@@ -265,6 +297,21 @@ class ClockSampler:
 
     def mark(self):
         return time.time()
+
+    def sample_once(self):
+        """One synchronous query (read-only), kept with the streamed samples:
+        taken right before and right after the timed region, so that a timed
+        region shorter than the streaming period still has a clock record."""
+        try:
+            r = subprocess.run(["nvidia-smi", "-i", str(self.gpu_id),
+                                "--query-gpu=" + ",".join(CLOCK_FIELDS),
+                                "--format=csv,noheader,nounits"],
+                               capture_output=True, text=True, timeout=10)
+        except (OSError, subprocess.TimeoutExpired):
+            return
+        for line in r.stdout.splitlines():
+            if line.strip():
+                self.lines.append((time.time(), line.strip()))
 
     def __exit__(self, *exc):
         if self.proc is not None:
@@ -386,9 +433,11 @@ def run_ours(args):
     import normalisation_rope_transformers_gb300 as nr
     import synth
 
-    calls = build_step(nr, synth, torch, device, rank)
+    selected = apply_workload_args(args, synth)
+    calls = build_step(nr, synth, torch, device, rank, selected=selected)
     step_bytes = sum(c.nbytes for c in calls)
-    assert [(c.name, c.nbytes, c.rows) for c in calls] == [s[:3] for s in step_shapes(synth)], \
+    assert [(c.name, c.nbytes, c.rows) for c in calls] == \
+        [s[:3] for s in step_shapes(synth, selected)], \
         "step buffers disagree with the workload constants"
     stream = torch.cuda.current_stream(device)
 
@@ -438,6 +487,8 @@ def run_ours(args):
     barrier()
     sampler = ClockSampler(gpu_id_for(torch, device))
     with sampler:
+        t_clock0 = time.time()
+        sampler.sample_once()
         barrier()
         t_wall0 = time.time()
         start.record(stream)
@@ -452,7 +503,12 @@ def run_ours(args):
         end.record(stream)
         barrier()
         t_wall1 = time.time()
-    clocks = sampler.summary(t_wall0, t_wall1)
+        sampler.sample_once()
+        t_clock1 = time.time()
+    # the streamed samples inside the timed region plus the two synchronous
+    # samples taken just before and just after it
+    clocks = sampler.summary(t_clock0, t_clock1)
+    clocks["window"] = "timed region, with one query just before and one just after it"
     elapsed_ms = start.elapsed_time(end)
     dom_samples = [a.elapsed_time(b) for a, b in dom_ev]
     dom_ms = statistics.fmean(dom_samples)
@@ -509,12 +565,12 @@ def run_ours(args):
         "gpu_launches": K * len(calls),
         "clocks": clocks,
     }
-    if rank == 0 and not args.no_decode_sweep:
+    if rank == 0 and not args.no_decode_sweep and args.config in (None, 5):
         result["decode_sweep"] = decode_sweep(nr, synth, torch, device)
-    if rank == 0 and not args.no_next_rows:
+    if rank == 0 and not args.no_next_rows and args.config is None:
         result["next_rows"] = next_rows(nr, synth, torch, device, peak)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        result["cpu_baseline"] = cpu_baseline(fraction=0.5)
+        result["cpu_baseline"] = cpu_baseline(fraction=0.5, selected=selected)
     if world > 1:
         dist.barrier()
         dist.destroy_process_group()
@@ -765,7 +821,7 @@ def decode_sweep(nr, synth, torch, device):
 # ---------------------------------------------------------------------------
 # CPU oracle (cpu_baseline leg and the reference arm)
 # ---------------------------------------------------------------------------
-def prepare_oracle_step(fraction):
+def prepare_oracle_step(fraction, selected=None):
     """Oracle calls over the first `fraction` of each workload's rows (at least
     one row).  The generator is counter-based, so these inputs are exactly the
     leading rows of the full workloads.  Returns [(fn(lo, hi), rows, algorithmic
@@ -777,7 +833,7 @@ def prepare_oracle_step(fraction):
 
     bf16, f32 = torch.bfloat16, torch.float32
     o = synth.to_oracle
-    ops, desc = [], []
+    ops, desc, names = [], [], []
 
     def rows_of(n):
         return max(1, min(n, int(round(n * fraction))))
@@ -788,6 +844,7 @@ def prepare_oracle_step(fraction):
     ops.append((lambda lo, hi, a=o(x), b=o(w): oracle.rmsnorm(a[lo:hi], b), r,
                 2 * x.numel() * 4 + w.numel() * 4))
     desc.append("rmsnorm_f32 %d/%d rows" % (r, c["rows"]))
+    names.append("rmsnorm_f32_64x1024")
     c = synth.ADD_RMSNORM
     r = rows_of(c["rows"])
     x, res, w = synth.rmsnorm_inputs(r, c["hidden"], c["seed"], bf16)
@@ -796,6 +853,7 @@ def prepare_oracle_step(fraction):
                     oracle.rmsnorm(a[lo:hi], b, residual=rr[lo:hi], gemma=g), r,
                     4 * r * c["hidden"] * 2 + c["hidden"] * 2))
         desc.append("add_rmsnorm gemma%d %d/%d rows" % (gemma, r, c["rows"]))
+        names.append("add_rmsnorm_bf16_8192x5120_gemma%d" % gemma)
     c = synth.QK_NORM_ROPE
     t = rows_of(c["tokens"])
     q, k, wq, wk, pos = synth.qk_inputs(t, c["hq"], c["hk"], c["head_dim"], c["seed"], bf16, f32)
@@ -803,12 +861,14 @@ def prepare_oracle_step(fraction):
                 oracle.qk_norm_rope(a[lo:hi], b[lo:hi], wa, wb, p[lo:hi], theta=th), t,
                 4 * t * c["hq"] * c["head_dim"] * 2 + t * 4 + 2 * c["head_dim"] * 4))
     desc.append("qk_norm_rope %d/%d tokens" % (t, c["tokens"]))
+    names.append("qk_norm_rope_bf16_26598x24x128")
     c = synth.LN_MODULATE
     r = rows_of(c["rows"])
     x, sh, sc = synth.ln_inputs(r, c["hidden"], c["seed"], bf16)
     ops.append((lambda lo, hi, a=o(x), s1=o(sh), s2=o(sc): oracle.ln_modulate(a[lo:hi], s1, s2),
                 r, 2 * r * c["hidden"] * 2 + 2 * c["hidden"] * 2))
     desc.append("ln_modulate %d/%d rows" % (r, c["rows"]))
+    names.append("ln_modulate_bf16_26598x3072")
     c = synth.DECODE
     rows, hidden = max(c["rows"]), max(c["hidden"])
     r = rows_of(rows)
@@ -816,11 +876,14 @@ def prepare_oracle_step(fraction):
     ops.append((lambda lo, hi, a=o(x), b=o(w), rr=o(res):
                 oracle.rmsnorm(a[lo:hi], b, residual=rr[lo:hi]), r, 4 * r * hidden * 2 + hidden * 2))
     desc.append("add_rmsnorm %d/%d rows of 8192" % (r, rows))
+    names.append("add_rmsnorm_bf16_256x8192")
     g = synth.silu_inputs(r, 3 * hidden, c["seed"], bf16)
     ops.append((lambda lo, hi, a=o(g): oracle.silu_and_mul(a[lo:hi]), r, 3 * r * 3 * hidden * 2))
     desc.append("silu_and_mul %d/%d rows" % (r, rows))
+    names.append("silu_and_mul_bf16_256x49152")
     oracle._load()
-    return ops, "; ".join(desc)
+    keep = [i for i, n in enumerate(names) if selected is None or n in selected]
+    return [ops[i] for i in keep], "; ".join(desc[i] for i in keep)
 
 
 def oracle_threads():
@@ -853,8 +916,8 @@ def time_oracle(ops, threads=1):
     return secs, nb
 
 
-def cpu_baseline(fraction):
-    ops, desc = prepare_oracle_step(fraction)
+def cpu_baseline(fraction, selected=None):
+    ops, desc = prepare_oracle_step(fraction, selected)
     secs1, nb = time_oracle(ops)
     threads = oracle_threads()
     secs, _ = time_oracle(ops, threads)
@@ -875,13 +938,14 @@ def run_reference(args):
     import synth
 
     steps, warm = args.steps, max(args.warmup, 3)
+    selected = apply_workload_args(args, synth)
     threads = oracle_threads()
     probe_fraction = 1.0 / 256
-    ops, _ = prepare_oracle_step(probe_fraction)
+    ops, _ = prepare_oracle_step(probe_fraction, selected)
     probe_s, _ = time_oracle(ops, threads)
     per_step_budget = min(2.0, 120.0 / (steps + warm))
     fraction = max(1.0 / 26598, min(0.5, probe_fraction * per_step_budget / max(probe_s, 1e-6)))
-    ops, desc = prepare_oracle_step(fraction)
+    ops, desc = prepare_oracle_step(fraction, selected)
     for _ in range(warm):
         time_oracle(ops, threads)
     total_s, total_b = 0.0, 0
@@ -897,7 +961,7 @@ def run_reference(args):
         "n_gpus": args.gpus, "steps": steps, "warmup": warm,
         "ms_per_step": round(1e3 * total_s / steps, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": step_config(step_shapes(synth), args.gpus),
+        "config": step_config(step_shapes(synth, selected), args.gpus),
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads,
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
@@ -914,6 +978,7 @@ def run_profile(args):
     import synth
 
     device = torch.device("cuda", 0)
+    apply_workload_args(args, synth)
     if args.rows is not None:
         for cfg, key in ((synth.ADD_RMSNORM, "rows"), (synth.QK_NORM_ROPE, "tokens"),
                          (synth.LN_MODULATE, "rows")):

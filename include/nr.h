@@ -20,8 +20,11 @@
  * Conventions shared by every entry point
  *   - Pointers are DEVICE pointers (CUDA global memory) owned by the caller; the
  *     library allocates nothing and frees nothing.  Its only state is one
- *     device status word that kernels set when a bounded wait runs out
+ *     status word per device that kernels set when a bounded wait runs out
  *     (nr_device_status reads and clears it).
+ *   - Each call opens one NVTX range named after the entry point for the
+ *     time of the host call (validation and launch), so profilers can tell
+ *     which call launched which kernel.
  *   - Every pointer must be 16-byte aligned, and every row start (row stride in
  *     bytes) a multiple of 16, so that each thread moves 128-bit vectors.
  *   - Work is enqueued asynchronously on `stream` (0 = the legacy default
@@ -70,9 +73,10 @@ typedef enum nr_dtype {
 /*
  * RMSNorm of each row, with the optional fused residual add.
  *
- * Follows vllm.cpp src/vt/cuda/cuda_ops.cu, "rmsnorm: one block per row"
- * (RmsNormRowKernel) and "ResRound" (the residual is rounded to its storage
- * dtype before it is squared, and that rounded value is what is written back).
+ * Follows the vllm.cpp page src/vt/cuda/cuda_ops.cu, its row-RMSNorm section
+ * and the residual-rounding helper before it (the residual is rounded to its
+ * storage dtype before it is squared, and that rounded value is what is
+ * written back).
  * For row r of x [rows, hidden] (row-major, contiguous):
  *     with a residual:  v_j = round(x_j + residual_j);  residual_j <- v_j   (in place)
  *     without one:      v_j = x_j
@@ -97,9 +101,9 @@ nr_status nr_rmsnorm(void* out, const void* x, const void* w, void* residual, in
  * RMSNorm (optionally with the fused residual add) followed by static FP8
  * quantisation of its output.
  *
- * Follows vllm.cpp src/vt/cuda/cuda_ops.cu, "rmsnorm + static fp8 quant": the
- * normalised value n_j of nr_rmsnorm is rounded to bf16 (nb_j, whatever the
- * input dtype), and
+ * Follows vllm.cpp src/vt/cuda/cuda_ops.cu, fused RMSNorm + static FP8
+ * section: the normalised value n_j of nr_rmsnorm is rounded to bf16 (nb_j,
+ * whatever the input dtype), and
  *     code_j = e4m3_satfinite(f32(nb_j) * inv_scale),   inv_scale = 1.0f / scale
  * with the product in f32: FP8 E4M3 (bias 7, largest finite 448, no
  * infinities), round to nearest even, finite values beyond +-448 saturating.
@@ -119,9 +123,10 @@ nr_status nr_rmsnorm_quant_fp8(void* codes, void* out_bf16, const void* x, const
 /*
  * Per-head RMSNorm of Q and K followed by NeoX rotary embedding, in one pass.
  *
- * Follows vllm.cpp src/vt/cuda/cuda_ops.cu, "attn_qk_norm_rope_gate" (RMSNorm
- * over head_dim per (token, head), then the rotation, with no rounding between
- * them) and "rope_neox" (freq_i = theta^(-2i/head_dim), angle = pos * freq_i,
+ * Follows vllm.cpp src/vt/cuda/cuda_ops.cu, the fused attention-preamble
+ * section (RMSNorm over head_dim per (token, head), then the rotation, with no
+ * rounding between them) and the NeoX RoPE section
+ * (freq_i = theta^(-2i/head_dim), angle = pos * freq_i,
  * rotate-half pairing (i, i + head_dim/2)).  For token t, head h of Q (and of K
  * with wk):
  *     inv  = 1 / sqrt(mean_j v_j^2 + eps);   n_j = v_j * inv * (gemma ? w_j + 1 : w_j)
@@ -159,11 +164,11 @@ nr_status nr_qk_norm_rope(void* q_out, void* k_out, const void* q, const void* k
  * RoPE variants for nr_qk_norm_rope_ex.  Zero-initialise, then set theta.
  *   rotary_dim           0 or head_dim: rotate the whole head; else the first
  *                        rotary_dim elements rotate and the rest keep their
- *                        normed value (vllm.cpp cuda_ops.cu,
- *                        "attn_qk_norm_rope_gate"); freq_i = theta^(-2i/rotary_dim).
+ *                        normed value (vllm.cpp cuda_ops.cu, fused
+ *                        attention-preamble section); freq_i = theta^(-2i/rotary_dim).
  *   interleaved          0: rotate-half pairs (i, i + rotary_dim/2) (NeoX);
- *                        1: GPT-J pairs (2i, 2i + 1) ("Supplied-cache RoPE").
- *   llama3_factor > 0    Llama-3 frequency rescale ("rope_neox", Llama-3
+ *                        1: GPT-J pairs (2i, 2i + 1) (cache-driven RoPE section).
+ *   llama3_factor > 0    Llama-3 frequency rescale (NeoX RoPE section, Llama-3
  *                        rescale): with wavelength L = 2pi / freq, L below
  *                        original_max_position / high_freq_factor keeps freq,
  *                        L above original_max_position / low_freq_factor
@@ -174,7 +179,7 @@ nr_status nr_qk_norm_rope(void* q_out, void* k_out, const void* q, const void* k
  *                        (t, h, w) summing to rotary_dim / 2: contiguous, or
  *                        with mrope_interleaved = 1 the t/h/w rows cycle over
  *                        pairs i % 3 = 0/1/2 while each of h and w has pairs
- *                        left ("Supplied-cache RoPE", M-RoPE axis selection).
+ *                        left (cache-driven RoPE section, M-RoPE axis selection).
  */
 typedef struct nr_rope_config {
   int64_t rotary_dim;
@@ -254,8 +259,11 @@ nr_status nr_gated_residual_ln_modulate(void* out, void* residual, const void* y
 /*
  * silu_and_mul: out[r, j] = silu(x[r, j]) * x[r, inter + j],  silu(a) = a / (1 + e^-a).
  *
- * Follows vllm.cpp src/vt/cuda/cuda_ops.cu, "silu_and_mul" (gate is the first
- * half of each row, up the second; math in f32).
+ * Follows vllm.cpp src/vt/cuda/cuda_ops.cu, SiLU gated-activation section
+ * (gate is the first half of each row, up the second; math in f32).  The
+ * sigmoid is evaluated without forming e^-a, so f32 outputs keep their 1e-5
+ * relative accuracy for every gate whose silu is a normal f32 (down to about
+ * -92); below that silu(a) itself is an f32 subnormal and loses bits.
  *
  * out  [rows, inter], dtype `dtype`; may not overlap x.
  * x    [rows, 2*inter], dtype `dtype`.
@@ -270,8 +278,9 @@ nr_status nr_silu_and_mul(void* out, const void* x, int64_t rows, int64_t inter,
  * tanh form of GELU
  *     gelu_tanh(a) = a/2 * (1 + tanh(sqrt(2/pi) * (a + 0.044715 a^3))).
  *
- * Follows vllm.cpp src/vt/cuda/cuda_ops.cu, "gelu_and_mul" (the gated MLP of
- * Gemma-family models; same layout as silu_and_mul).  Evaluated as
+ * Follows vllm.cpp src/vt/cuda/cuda_ops.cu, GELU gated-activation section
+ * (the gated MLP of Gemma-family models; same layout as silu_and_mul).
+ * Evaluated as
  * a * sigmoid(2z), which equals the formula above and keeps its relative
  * accuracy for negative gates.
  *
@@ -284,10 +293,15 @@ nr_status nr_gelu_and_mul(void* out, const void* x, int64_t rows, int64_t inter,
  * Device-side failure report.  Kernels that wait on hardware events (the
  * bulk-copy path of nr_qk_norm_rope waits for its copies on shared-memory
  * barriers) bound every wait (about one second of SM clock); a wait that runs
- * out sets a bit in a device status word kept by the library, the kernel
- * lets its copies in flight finish and returns, and the outputs of that call
- * are not valid.  nr_device_status synchronises `stream`, reads and clears
- * the word: NR_OK if no wait ran out since the last read, else
+ * out sets a bit in a status word the library keeps on each device, the
+ * kernel lets its copies in flight finish and returns, and the outputs of
+ * that call are not valid.  nr_device_status works on the device that owns
+ * `stream` (whatever device is current; the current device is restored): it
+ * synchronises `stream`, reads that device's word and clears exactly the bits
+ * it read, so a bit set meanwhile by a kernel on another stream is kept for
+ * the next read.  The word is shared by every stream and thread of the
+ * process on that device, so a report may concern a call made on another
+ * stream.  Returns NR_OK if no wait ran out since the last read, else
  * NR_ERR_TIMEOUT (the message names the kernel).  A CUDA error while
  * synchronising is NR_ERR_CUDA.
  */

@@ -120,17 +120,86 @@ def _stream(t: torch.Tensor):
 
 
 def _cuda(*ts):
+    """Every tensor on one CUDA device (checked after the shapes, so that a
+    shape error is reported as such whatever the device)."""
+    dev = None
     for t in ts:
-        if t is not None and not t.is_cuda:
+        if t is None:
+            continue
+        if not t.is_cuda:
             raise ValueError("tensors must be on a CUDA device")
+        if dev is None:
+            dev = t.device
+        elif t.device != dev:
+            raise ValueError("tensors must all be on one CUDA device (%s and %s)" % (dev, t.device))
+
+
+def _expect(t, name, dtype, shape, contiguous=True):
+    """Raise unless `t` is a tensor of `dtype` and `shape` (and contiguous).
+    The C ABI sees only pointers, so a short or mistyped operand would be read
+    or written past its end; this is where the sizes are checked."""
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s must be a torch tensor" % name)
+    if t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError("%s must have shape %s, got %s" % (name, tuple(shape), tuple(t.shape)))
+    if contiguous and not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+
+
+def _rows_2d(t, name):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s must be a torch tensor" % name)
+    if t.dim() != 2 or not t.is_contiguous():
+        raise ValueError("%s must be a contiguous [rows, hidden] tensor" % name)
+    _dtype_code(t)
+
+
+def _heads_3d(t, name):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s must be a torch tensor" % name)
+    if t.dim() != 3 or t.stride(2) != 1 or (t.shape[1] > 1 and t.stride(1) != t.shape[2]):
+        raise ValueError("%s must be [tokens, heads, head_dim] with contiguous heads" % name)
+    _dtype_code(t)
+
+
+def _samples(t, name, dtype, rows, hidden, rows_per_sample):
+    """A modulation operand: [hidden] (one sample) or [samples, hidden], with
+    at least one sample per started group of rows_per_sample rows."""
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s must be a torch tensor" % name)
+    if t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if t.dim() not in (1, 2) or t.shape[-1] != hidden or not t.is_contiguous():
+        raise ValueError("%s must be a contiguous [samples, %d] tensor, got %s"
+                         % (name, hidden, tuple(t.shape)))
+    need = -(-rows // rows_per_sample) if rows > 0 else 0
+    have = 1 if t.dim() == 1 else t.shape[0]
+    if have < need:
+        raise ValueError("%s has %d sample rows; %d rows at %d rows per sample need %d"
+                         % (name, have, rows, rows_per_sample, need))
+
+
+def _rows_per_sample(rows_per_sample, rows):
+    if rows_per_sample is None:
+        return max(rows, 1)
+    rps = int(rows_per_sample)
+    if rps < 1:
+        raise ValueError("rows_per_sample must be >= 1")
+    return rps
 
 
 def rmsnorm(x, w, residual=None, eps=1e-6, gemma=False, out=None):
     """RMSNorm of each row of x [rows, hidden]; with `residual`, first
     residual <- round(x + residual) in place.  Returns out."""
+    _rows_2d(x, "x")
+    _expect(w, "w", x.dtype, (x.shape[1],))
+    if residual is not None:
+        _expect(residual, "residual", x.dtype, x.shape)
+    if out is not None:
+        _expect(out, "out", x.dtype, x.shape)
     _cuda(x, w, residual, out)
-    if x.dim() != 2 or not x.is_contiguous():
-        raise ValueError("x must be a contiguous [rows, hidden] tensor")
     if out is None:
         out = torch.empty_like(x)
     _check(lib.nr_rmsnorm(_ptr(out), _ptr(x), _ptr(w), _ptr(residual), x.shape[0], x.shape[1],
@@ -143,20 +212,48 @@ def rmsnorm_quant_fp8(x, w, scale, residual=None, eps=1e-6, gemma=False, codes=N
     """RMSNorm of x [rows, hidden] (with the optional residual add), rounded to
     bf16, then e4m3 codes of that value * (1/scale).  Returns codes (uint8),
     or (codes, the bf16 values) when out_bf16 is True (or a tensor to fill)."""
-    _cuda(x, w, residual, codes)
-    if x.dim() != 2 or not x.is_contiguous():
-        raise ValueError("x must be a contiguous [rows, hidden] tensor")
+    _rows_2d(x, "x")
+    _expect(w, "w", x.dtype, (x.shape[1],))
+    if residual is not None:
+        _expect(residual, "residual", x.dtype, x.shape)
+    if codes is not None:
+        _expect(codes, "codes", torch.uint8, x.shape)
+    nb = None
+    if out_bf16 is not True and out_bf16 is not False and out_bf16 is not None:
+        nb = out_bf16
+        _expect(nb, "out_bf16", torch.bfloat16, x.shape)
+    _cuda(x, w, residual, codes, nb)
     if codes is None:
         codes = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
-    nb = None
     if out_bf16 is True:
         nb = torch.empty(x.shape, dtype=torch.bfloat16, device=x.device)
-    elif out_bf16 is not False and out_bf16 is not None:
-        nb = out_bf16
     _check(lib.nr_rmsnorm_quant_fp8(_ptr(codes), _ptr(nb), _ptr(x), _ptr(w), _ptr(residual),
                                     x.shape[0], x.shape[1], _dtype_code(x), float(eps),
                                     int(bool(gemma)), float(scale), _stream(x)))
     return codes if nb is None else (codes, nb)
+
+
+def _check_qk(q, k, wq, wk, q_out, k_out):
+    """q, k [tokens, heads, head_dim] of one dtype and token count; wq, wk
+    [head_dim] of one dtype; outputs with the shapes, dtype and strides of
+    their inputs."""
+    _heads_3d(q, "q")
+    _heads_3d(k, "k")
+    if k.dtype != q.dtype:
+        raise TypeError("q and k share one dtype")
+    if k.shape[0] != q.shape[0] or k.shape[2] != q.shape[2]:
+        raise ValueError("q %s and k %s must have the same tokens and head_dim"
+                         % (tuple(q.shape), tuple(k.shape)))
+    if not isinstance(wq, torch.Tensor) or wq.dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("wq must be a float32 or bfloat16 tensor")
+    _expect(wq, "wq", wq.dtype, (q.shape[2],))
+    _expect(wk, "wk", wq.dtype, (q.shape[2],))
+    for o, i, name in ((q_out, q, "q_out"), (k_out, k, "k_out")):
+        if o is None:
+            continue
+        _expect(o, name, i.dtype, i.shape, contiguous=False)
+        if o.stride() != i.stride():
+            raise ValueError("%s must have the strides of its input" % name)
 
 
 def qk_norm_rope(q, k, wq, wk, positions, eps=1e-6, theta=10000.0, gemma=False, q_out=None,
@@ -164,20 +261,13 @@ def qk_norm_rope(q, k, wq, wk, positions, eps=1e-6, theta=10000.0, gemma=False, 
     """Per-head RMSNorm + NeoX RoPE of q [tokens, hq, D] and k [tokens, hk, D].
     q and k may be token-strided views (last two axes contiguous); outputs share
     their strides (q_out=q / k_out=k for in place).  Returns (q_out, k_out)."""
+    _check_qk(q, k, wq, wk, q_out, k_out)
+    _expect(positions, "positions", torch.int32, (q.shape[0],))
     _cuda(q, k, wq, wk, positions, q_out, k_out)
-    for t in (q, k):
-        if t.dim() != 3 or t.stride(2) != 1 or t.stride(1) != t.shape[2]:
-            raise ValueError("q/k must be [tokens, heads, head_dim] with contiguous heads")
-    if positions.dtype != torch.int32 or positions.dim() != 1:
-        raise TypeError("positions must be a 1-D int32 tensor")
     if q_out is None:
         q_out = torch.empty_strided(q.shape, q.stride(), dtype=q.dtype, device=q.device)
     if k_out is None:
         k_out = torch.empty_strided(k.shape, k.stride(), dtype=k.dtype, device=k.device)
-    if q_out.stride() != q.stride() or k_out.stride() != k.stride():
-        raise ValueError("q_out/k_out must have the strides of q/k")
-    if wq.dtype != wk.dtype:
-        raise TypeError("wq and wk share one dtype")
     _check(lib.nr_qk_norm_rope(_ptr(q_out), _ptr(k_out), _ptr(q), _ptr(k), _ptr(wq), _ptr(wk),
                                _dtype_code(wq), _ptr(positions), q.shape[0], q.shape[1],
                                k.shape[1], q.shape[2], q.stride(0), k.stride(0), float(eps),
@@ -192,19 +282,14 @@ def qk_norm_rope_ex(q, k, wq, wk, positions, eps=1e-6, gemma=False, rotary_dim=N
     interleaved pairs, Llama-3 rescale (llama3 = (factor, low_freq_factor,
     high_freq_factor, original_max_position)) and M-RoPE (positions [3, tokens],
     mrope_sections = (t, h, w)).  Returns (q_out, k_out)."""
+    _check_qk(q, k, wq, wk, q_out, k_out)
+    _expect(positions, "positions", torch.int32,
+            (3, q.shape[0]) if mrope_sections is not None else (q.shape[0],))
     _cuda(q, k, wq, wk, positions, q_out, k_out)
-    for t in (q, k):
-        if t.dim() != 3 or t.stride(2) != 1 or t.stride(1) != t.shape[2]:
-            raise ValueError("q/k must be [tokens, heads, head_dim] with contiguous heads")
-    want = 2 if mrope_sections is not None else 1
-    if positions.dtype != torch.int32 or positions.dim() != want or not positions.is_contiguous():
-        raise TypeError("positions must be a contiguous int32 tensor of %d dims" % want)
     if q_out is None:
         q_out = torch.empty_strided(q.shape, q.stride(), dtype=q.dtype, device=q.device)
     if k_out is None:
         k_out = torch.empty_strided(k.shape, k.stride(), dtype=k.dtype, device=k.device)
-    if q_out.stride() != q.stride() or k_out.stride() != k.stride():
-        raise ValueError("q_out/k_out must have the strides of q/k")
     cfg = RopeConfig()
     cfg.rotary_dim = 0 if rotary_dim is None else int(rotary_dim)
     cfg.interleaved = int(bool(interleaved))
@@ -227,11 +312,13 @@ def ln_modulate(x, shift, scale, eps=1e-6, rows_per_sample=None, out=None):
     """LayerNorm (no affine) of x [rows, hidden] then * (1 + scale) + shift,
     with shift/scale [samples, hidden] (row r uses sample r // rows_per_sample).
     Returns out."""
+    _rows_2d(x, "x")
+    rows_per_sample = _rows_per_sample(rows_per_sample, x.shape[0])
+    for t, name in ((shift, "shift"), (scale, "scale")):
+        _samples(t, name, x.dtype, x.shape[0], x.shape[1], rows_per_sample)
+    if out is not None:
+        _expect(out, "out", x.dtype, x.shape)
     _cuda(x, shift, scale, out)
-    if x.dim() != 2 or not x.is_contiguous():
-        raise ValueError("x must be a contiguous [rows, hidden] tensor")
-    if rows_per_sample is None:
-        rows_per_sample = max(x.shape[0], 1)
     if out is None:
         out = torch.empty_like(x)
     _check(lib.nr_ln_modulate(_ptr(out), _ptr(x), _ptr(shift), _ptr(scale), x.shape[0],
@@ -245,12 +332,15 @@ def gated_residual_ln_modulate(residual, y, gate, shift, scale, eps=1e-6, rows_p
     """residual <- round(residual + gate * y) in place, then LayerNorm (no affine)
     of it * (1 + scale) + shift.  gate/shift/scale are [samples, hidden]; row r
     uses sample r // rows_per_sample.  Returns out."""
+    _rows_2d(residual, "residual")
+    _expect(y, "y", residual.dtype, residual.shape)
+    rows, hidden = residual.shape
+    rows_per_sample = _rows_per_sample(rows_per_sample, rows)
+    for t, name in ((gate, "gate"), (shift, "shift"), (scale, "scale")):
+        _samples(t, name, residual.dtype, rows, hidden, rows_per_sample)
+    if out is not None:
+        _expect(out, "out", residual.dtype, residual.shape)
     _cuda(residual, y, gate, shift, scale, out)
-    for t in (residual, y):
-        if t.dim() != 2 or not t.is_contiguous():
-            raise ValueError("residual and y must be contiguous [rows, hidden] tensors")
-    if rows_per_sample is None:
-        rows_per_sample = max(residual.shape[0], 1)
     if out is None:
         out = torch.empty_like(residual)
     _check(lib.nr_gated_residual_ln_modulate(
@@ -261,10 +351,13 @@ def gated_residual_ln_modulate(residual, y, gate, shift, scale, eps=1e-6, rows_p
 
 
 def _act_and_mul(fn, x, out):
-    _cuda(x, out)
-    if x.dim() != 2 or not x.is_contiguous() or x.shape[1] % 2:
+    _rows_2d(x, "x")
+    if x.shape[1] % 2:
         raise ValueError("x must be a contiguous [rows, 2*inter] tensor")
     inter = x.shape[1] // 2
+    if out is not None:
+        _expect(out, "out", x.dtype, (x.shape[0], inter))
+    _cuda(x, out)
     if out is None:
         out = torch.empty((x.shape[0], inter), dtype=x.dtype, device=x.device)
     _check(fn(_ptr(out), _ptr(x), x.shape[0], inter, _dtype_code(x), _stream(x)))

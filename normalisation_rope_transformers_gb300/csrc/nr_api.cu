@@ -6,10 +6,23 @@
 #include <stdint.h>
 #include <stdio.h>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "../../include/nr.h"
 #include "nr_internal.h"
 
 namespace {
+
+// One NVTX range per entry-point call, named after the entry point, so that
+// profilers (nsys, ncu --nvtx) can attribute kernels to the call that
+// launched them.  Without a tool attached the push and pop cost a few
+// nanoseconds.
+struct CallRange {
+  explicit CallRange(const char* name) { nvtxRangePushA(name); }
+  ~CallRange() { nvtxRangePop(); }
+  CallRange(const CallRange&) = delete;
+  CallRange& operator=(const CallRange&) = delete;
+};
 
 thread_local char g_message[512];
 
@@ -94,6 +107,7 @@ const char* nr_status_string(nr_status s) {
 
 nr_status nr_rmsnorm(void* out, const void* x, const void* w, void* residual, int64_t rows,
                      int64_t hidden, nr_dtype dtype, float eps, int gemma, cudaStream_t stream) {
+  CallRange range("nr_rmsnorm");
   if (!valid_dtype(dtype)) return fail(NR_ERR_DTYPE, "nr_rmsnorm: unknown dtype %d", (int)dtype);
   if (rows < 0) return fail(NR_ERR_SHAPE, "nr_rmsnorm: rows = %lld < 0", (long long)rows);
   if (hidden <= 0) return fail(NR_ERR_SHAPE, "nr_rmsnorm: hidden = %lld <= 0", (long long)hidden);
@@ -128,6 +142,7 @@ nr_status nr_rmsnorm(void* out, const void* x, const void* w, void* residual, in
 nr_status nr_rmsnorm_quant_fp8(void* codes, void* out_bf16, const void* x, const void* w,
                                void* residual, int64_t rows, int64_t hidden, nr_dtype dtype,
                                float eps, int gemma, float scale, cudaStream_t stream) {
+  CallRange range("nr_rmsnorm_quant_fp8");
   const char* fn = "nr_rmsnorm_quant_fp8";
   if (!valid_dtype(dtype)) return fail(NR_ERR_DTYPE, "%s: unknown dtype %d", fn, (int)dtype);
   if (rows < 0 || hidden <= 0)
@@ -312,6 +327,7 @@ nr_status nr_qk_norm_rope(void* q_out, void* k_out, const void* q, const void* k
                           int64_t tokens, int64_t hq, int64_t hk, int64_t head_dim,
                           int64_t q_tok_stride, int64_t k_tok_stride, float eps, double theta,
                           int gemma, nr_dtype dtype, cudaStream_t stream) {
+  CallRange range("nr_qk_norm_rope");
   nr_rope_config rope = {};
   rope.theta = theta;
   return qk_norm_rope_impl("nr_qk_norm_rope", q_out, k_out, q, k, wq, wk, w_dtype, positions,
@@ -325,6 +341,7 @@ nr_status nr_qk_norm_rope_ex(void* q_out, void* k_out, const void* q, const void
                              int64_t head_dim, int64_t q_tok_stride, int64_t k_tok_stride,
                              float eps, int gemma, const nr_rope_config* rope, nr_dtype dtype,
                              cudaStream_t stream) {
+  CallRange range("nr_qk_norm_rope_ex");
   if (rope == nullptr) return fail(NR_ERR_NULL, "nr_qk_norm_rope_ex: rope config is NULL");
   return qk_norm_rope_impl("nr_qk_norm_rope_ex", q_out, k_out, q, k, wq, wk, w_dtype, positions,
                            tokens, hq, hk, head_dim, q_tok_stride, k_tok_stride, eps, gemma, *rope,
@@ -334,6 +351,7 @@ nr_status nr_qk_norm_rope_ex(void* q_out, void* k_out, const void* q, const void
 nr_status nr_ln_modulate(void* out, const void* x, const void* shift, const void* scale,
                          int64_t rows, int64_t hidden, int64_t rows_per_sample, float eps,
                          nr_dtype dtype, cudaStream_t stream) {
+  CallRange range("nr_ln_modulate");
   if (!valid_dtype(dtype)) return fail(NR_ERR_DTYPE, "nr_ln_modulate: unknown dtype %d", (int)dtype);
   if (rows < 0 || hidden <= 0 || rows_per_sample < 1)
     return fail(NR_ERR_SHAPE, "nr_ln_modulate: need rows >= 0, hidden > 0, rows_per_sample >= 1");
@@ -365,6 +383,7 @@ nr_status nr_gated_residual_ln_modulate(void* out, void* residual, const void* y
                                         const void* gate, const void* shift, const void* scale,
                                         int64_t rows, int64_t hidden, int64_t rows_per_sample,
                                         float eps, nr_dtype dtype, cudaStream_t stream) {
+  CallRange range("nr_gated_residual_ln_modulate");
   const char* fn = "nr_gated_residual_ln_modulate";
   if (!valid_dtype(dtype)) return fail(NR_ERR_DTYPE, "%s: unknown dtype %d", fn, (int)dtype);
   if (rows < 0 || hidden <= 0 || rows_per_sample < 1)
@@ -428,12 +447,16 @@ nr_status act_and_mul(const char* fn, int gelu, void* out, const void* x, int64_
 extern "C" {
 
 nr_status nr_device_status(cudaStream_t stream) {
+  CallRange range("nr_device_status");
   unsigned bits = 0;
   const cudaError_t e = nr::take_device_status(stream, &bits);
   if (e != cudaSuccess) return from_cuda(e, "nr_device_status");
   if (bits & nr::kStatusBitQkBulkWait)
     return fail(NR_ERR_TIMEOUT, "nr_device_status: a bounded wait for a bulk copy ran out in the "
                                 "Q/K norm + RoPE kernel (status bits 0x%x)", bits);
+  if (bits & nr::kStatusBitLnBulkWait)
+    return fail(NR_ERR_TIMEOUT, "nr_device_status: a bounded wait for a bulk copy ran out in the "
+                                "LayerNorm + modulation kernel (status bits 0x%x)", bits);
   if (bits != 0)
     return fail(NR_ERR_TIMEOUT, "nr_device_status: the wait probe's wait ran out (status bits "
                                 "0x%x)", bits);
@@ -441,6 +464,7 @@ nr_status nr_device_status(cudaStream_t stream) {
 }
 
 nr_status nr_test_wait_probe(int64_t limit_cycles, cudaStream_t stream) {
+  CallRange range("nr_test_wait_probe");
   if (limit_cycles < 1 || limit_cycles > (int64_t(1) << 32))
     return fail(NR_ERR_VALUE, "nr_test_wait_probe: limit_cycles must be in [1, 2^32]");
   return from_cuda(nr::launch_wait_probe(limit_cycles, stream), "nr_test_wait_probe");
@@ -448,11 +472,13 @@ nr_status nr_test_wait_probe(int64_t limit_cycles, cudaStream_t stream) {
 
 nr_status nr_silu_and_mul(void* out, const void* x, int64_t rows, int64_t inter, nr_dtype dtype,
                           cudaStream_t stream) {
+  CallRange range("nr_silu_and_mul");
   return act_and_mul("nr_silu_and_mul", 0, out, x, rows, inter, dtype, stream);
 }
 
 nr_status nr_gelu_and_mul(void* out, const void* x, int64_t rows, int64_t inter, nr_dtype dtype,
                           cudaStream_t stream) {
+  CallRange range("nr_gelu_and_mul");
   return act_and_mul("nr_gelu_and_mul", 1, out, x, rows, inter, dtype, stream);
 }
 

@@ -113,8 +113,14 @@ cudaError_t launch_qk_norm_rope(void* q_out, void* k_out, const void* q, const v
 // Device status word: bits set by kernels whose bounded waits ran out.
 constexpr unsigned kStatusBitQkBulkWait = 1u;
 constexpr unsigned kStatusBitProbeWait = 2u;
+constexpr unsigned kStatusBitLnBulkWait = 4u;
 
-// Waits for `stream`, then reads and clears the status word.
+// Device address of the current device's status word (status.cu), looked up
+// once per device.  Kernels that bound a wait take it as an argument.
+cudaError_t status_word(unsigned** word);
+
+// On the device of `stream`: waits for `stream`, reads the status word and
+// clears the bits it read (bits set after the read stay set).
 cudaError_t take_device_status(cudaStream_t stream, unsigned* bits);
 
 // One block whose single wait nothing completes, given up after

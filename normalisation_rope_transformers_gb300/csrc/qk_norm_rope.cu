@@ -1,9 +1,9 @@
 // Per-head Q/K RMSNorm fused with NeoX rotary embedding, for sm_103a.
 //
-// Computes what vllm.cpp src/vt/cuda/cuda_ops.cu describes in
-// "attn_qk_norm_rope_gate" (RMSNorm over head_dim per (token, head), then the
-// rotation, no rounding in between) with the angles of "rope_neox"
-// (freq_i = theta^(-2i/D), angle = pos * freq_i, pairs (i, i + D/2)).
+// Computes what the vllm.cpp page src/vt/cuda/cuda_ops.cu gives in its fused
+// attention-preamble section (RMSNorm over head_dim per (token, head), then
+// the rotation, no rounding in between) with the angles of its NeoX RoPE
+// section (freq_i = theta^(-2i/D), angle = pos * freq_i, pairs (i, i + D/2)).
 //
 // Design (not the page's, which runs one 256-thread block per (token, head)
 // and reads a precomputed f32 cos/sin table from global memory):
@@ -78,6 +78,7 @@ struct QkArgs {
   int interleaved;         // 0: rotate-half pairs (i, i + rot/2); 1: GPT-J pairs (2i, 2i + 1)
   int mrope;               // 1: three position rows, pair i uses row axis[i]
   int64_t pos_row_stride;  // elements between the position rows (= tokens)
+  unsigned* status;        // the device status word (bounded waits that ran out)
 };
 
 // T: storage dtype of q/k; WT: weight dtype; L: lanes per head row
@@ -366,9 +367,7 @@ constexpr int kBulkWarps = NR_QKB_WARPS;
 constexpr int kBulkThreads = kBulkWarps * kWarp;
 constexpr long long kWaitLimitCycles = 1LL << 31;  // about one second
 
-__device__ unsigned int g_status_word;
-
-__device__ __forceinline__ void record_status(unsigned bit) { atomicOr(&g_status_word, bit); }
+__device__ __forceinline__ void record_status(unsigned* word, unsigned bit) { atomicOr(word, bit); }
 
 struct BulkGeom {
   unsigned q_bytes;      // one token's Q rows
@@ -497,7 +496,7 @@ __global__ void __launch_bounds__(kBulkThreads) qk_norm_rope_bulk_kernel(const Q
     unsigned char* st = stage(j);
     if (!mbar_wait_bounded(smem_addr(bars + j % NST), static_cast<unsigned>((j / NST) & 1),
                            kWaitLimitCycles)) {
-      record_status(kStatusBitQkBulkWait);
+      record_status(a.status, kStatusBitQkBulkWait);
       *abort_flag = 1;
     }
     // this lane's (cos, sin) for the token
@@ -714,7 +713,7 @@ __global__ void __launch_bounds__(kBulkThreads, NR_QKV_MINB) qk_norm_rope_bulk_v
     unsigned char* st = stage(j);
     if (!mbar_wait_bounded(smem_addr(bars + j % NST), static_cast<unsigned>((j / NST) & 1),
                            kWaitLimitCycles)) {
-      record_status(kStatusBitQkBulkWait);
+      record_status(a.status, kStatusBitQkBulkWait);
       *abort_flag = 1;
     }
     // this lane's (cos, sin) for the token
@@ -826,19 +825,6 @@ __global__ void __launch_bounds__(kBulkThreads, NR_QKV_MINB) qk_norm_rope_bulk_v
                              kWaitLimitCycles))
         break;
   }
-}
-
-// A wait that nothing completes: one mbarrier with no arrivals, waited on for
-// `limit` cycles.  Exercises the expiry path that the real kernels take.
-__global__ void wait_probe_kernel(long long limit) {
-  __shared__ __align__(8) unsigned long long bar;
-  if (threadIdx.x == 0) {
-    mbar_init(smem_addr(&bar), 1);
-    fence_mbar_init();
-  }
-  __syncthreads();
-  if (!mbar_wait_bounded(smem_addr(&bar), 0, limit) && threadIdx.x == 0)
-    record_status(kStatusBitProbeWait);
 }
 
 // Resident blocks per SM of one kernel instantiation (with its dynamic shared
@@ -994,6 +980,8 @@ cudaError_t launch_qk_norm_rope(void* q_out, void* k_out, const void* q, const v
   a.interleaved = interleaved;
   a.mrope = mrope;
   a.pos_row_stride = tokens;
+  cudaError_t e = status_word(&a.status);
+  if (e != cudaSuccess) return e;
 
   if (is_bf16) {
     if (w_is_bf16) return launch_w<__nv_bfloat16, __nv_bfloat16>(a, lanes, turns, stream);
@@ -1001,26 +989,6 @@ cudaError_t launch_qk_norm_rope(void* q_out, void* k_out, const void* q, const v
   }
   if (w_is_bf16) return launch_w<float, __nv_bfloat16>(a, lanes, turns, stream);
   return launch_w<float, float>(a, lanes, turns, stream);
-}
-
-cudaError_t take_device_status(cudaStream_t stream, unsigned* bits) {
-  cudaError_t e = cudaStreamSynchronize(stream);
-  if (e != cudaSuccess) return e;
-  unsigned v = 0;
-  e = cudaMemcpyFromSymbol(&v, g_status_word, sizeof(v));
-  if (e != cudaSuccess) return e;
-  if (v != 0) {
-    const unsigned zero = 0;
-    e = cudaMemcpyToSymbol(g_status_word, &zero, sizeof(zero));
-    if (e != cudaSuccess) return e;
-  }
-  *bits = v;
-  return cudaSuccess;
-}
-
-cudaError_t launch_wait_probe(long long limit_cycles, cudaStream_t stream) {
-  wait_probe_kernel<<<1, 32, 0, stream>>>(limit_cycles);
-  return cudaGetLastError();
 }
 
 }  // namespace nr

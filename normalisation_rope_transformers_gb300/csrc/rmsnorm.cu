@@ -1,8 +1,9 @@
 // RMSNorm with the optional fused residual add, for sm_103a.
 //
-// Computes what vllm.cpp src/vt/cuda/cuda_ops.cu describes in "rmsnorm: one
-// block per row" and "ResRound": v = round(x + residual) (written back in
-// place), inv = 1/sqrt(mean(v^2) + eps), out = round(v * inv * (w [+1])).
+// Computes what the vllm.cpp page src/vt/cuda/cuda_ops.cu gives in its
+// row-RMSNorm section and the residual-rounding helper before it:
+// v = round(x + residual) (written back in place),
+// inv = 1/sqrt(mean(v^2) + eps), out = round(v * inv * (w [+1])).
 //
 // Design (not the page's): the page's kernel walks a row twice with scalar
 // loads and a 256-wide shared-memory tree.  Here each row is held in

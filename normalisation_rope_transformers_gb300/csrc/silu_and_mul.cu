@@ -1,7 +1,8 @@
 // Gated activations for sm_103a: out[r, j] = act(x[r, j]) * x[r, inter + j]
-// with act = silu (vllm.cpp src/vt/cuda/cuda_ops.cu, "silu_and_mul") or the
-// tanh form of GELU ("gelu_and_mul"); gate = first half of the row, up =
-// second half, f32 math.  Design: a 2-D grid (vector column blocks x rows) so
+// with act = silu (the vllm.cpp page src/vt/cuda/cuda_ops.cu, SiLU
+// gated-activation section) or the tanh form of GELU (its GELU
+// gated-activation section); gate = first half of the row, up = second half,
+// f32 math.  Design: a 2-D grid (vector column blocks x rows) so
 // no thread divides a flat index; each thread moves UNROLL 128-bit vectors of
 // gate and of up, issuing every load before any math.  Both activations are
 // a * sigmoid(s * z(a)) evaluated in an overflow-free form (below); bf16
@@ -22,7 +23,10 @@ constexpr int kSiluThreads = 128;
 // t = e^-|a| lies in (0, 1], sigmoid(|a|) = 1 / (1 + t) and
 // sigmoid(-|a|) = t / (1 + t), so the divisor stays in [1, 2] and large
 // negative gates keep their tiny (possibly subnormal) result.  f32 outputs use
-// the accurate expf and an IEEE division.
+// the same form with the accurate expf and IEEE divisions: e^-a is never
+// formed, so gates below -88.7 (where e^-a overflows f32) still give a * e^a
+// to a few ulps while that value is a normal f32 (gates down to about -92;
+// t itself loses bits gradually below -87.3, about 2e-6 relative at -90).
 template <typename T>
 __device__ __forceinline__ float silu(float a);
 template <>
@@ -33,7 +37,8 @@ __device__ __forceinline__ float silu<__nv_bfloat16>(float a) {
 }
 template <>
 __device__ __forceinline__ float silu<float>(float a) {
-  return a / (1.0f + expf(-a));
+  const float t = expf(-fabsf(a));
+  return a * (a >= 0.0f ? 1.0f / (1.0f + t) : t / (1.0f + t));
 }
 
 // tanh-GELU: 0.5 a (1 + tanh(z)), z = sqrt(2/pi) (a + 0.044715 a^3), computed

@@ -10,16 +10,21 @@
  * baseline leg may load it.
  *
  * Sources (page title, then the section on that page):
- *   [VT]  vllm.cpp, src/vt/cuda/cuda_ops.cu
- *           - "f32 load/store overloads" (bf16 stores are round-to-nearest-even)
- *           - "ResRound" (residual rounded to its storage dtype before squaring)
- *           - "rmsnorm: one block per row" (RmsNormRowKernel: eps inside the
- *             sqrt, mean over h, gemma uses w+1)
- *           - "rope_neox" (RopeNeoxKernel: freq = base^(-2*pair/rot) in double,
+ *   [VT]  vllm.cpp, src/vt/cuda/cuda_ops.cu, sections named here by what they
+ *         hold:
+ *           - the bf16 load/store helpers (bf16 stores round to nearest even)
+ *           - the residual-rounding helper (the residual is rounded to its
+ *             storage dtype before it is squared)
+ *           - the row-RMSNorm section (eps inside the sqrt, mean over h, gemma
+ *             uses w+1)
+ *           - the NeoX RoPE section (freq = base^(-2*pair/rot) in double,
  *             angle = pos*freq, rotate-half pairing (i, i+rot/2))
- *           - "attn_qk_norm_rope_gate" (per-(token, head) RMSNorm over head_dim,
- *             then the rotation, with no bf16 rounding in between)
- *           - "silu_and_mul" (gate = first half, up = second half)
+ *           - the fused attention-preamble section (per-(token, head) RMSNorm
+ *             over head_dim, then the rotation, with no bf16 rounding between)
+ *           - the SiLU and GELU gated-activation sections (gate = first half,
+ *             up = second half)
+ *           - the cache-driven RoPE section (GPT-J pairing, M-RoPE axes)
+ *           - the fused RMSNorm + static FP8 section
  *   [PAN2] FastVideo compare view feat/pan2-inference-optimizations, PAN2 docs,
  *          "Performance switches" table, row dit_fused_kernels: names the fused
  *          LayerNorm + modulation without printing its formula.  The oracle uses
@@ -55,7 +60,7 @@ double nro_bf16_value(uint16_t bits) {
 }
 
 /* Round a double straight to bf16, round-to-nearest, ties-to-even ([VT]
- * "f32 load/store overloads").  Rounds once, from the double, never via f32.
+ * bf16 load/store helpers).  Rounds once, from the double, never via f32.
  * bf16 keeps 8 significant bits; its normal exponents reach down to 2^-126 and
  * below that the grid is the fixed subnormal step 2^-133. */
 uint16_t nro_bf16_round(double d) {
@@ -104,8 +109,8 @@ static void store(int dtype, void* p, int64_t i, double v) {
 }
 
 /* ------------------------------------------------------------------------ */
-/* RMSNorm, optionally with the fused residual add ([VT] "rmsnorm: one block  */
-/* per row", "ResRound").                                                     */
+/* RMSNorm, optionally with the fused residual add ([VT] row-RMSNorm         */
+/* section and its residual-rounding helper).                                */
 /*                                                                            */
 /*   with a residual: v_j = round_dtype(x_j + res_j), and res_j <- v_j        */
 /*   without one:     v_j = x_j                                               */
@@ -143,8 +148,8 @@ void nro_rmsnorm(int dtype, int64_t rows, int64_t hidden, const void* x, const v
 }
 
 /* ------------------------------------------------------------------------ */
-/* RMSNorm + static FP8 (e4m3) quantisation ([VT] "rmsnorm + static fp8      */
-/* quant"): the RMSNorm above, its output rounded to bf16 (nb), and the code  */
+/* RMSNorm + static FP8 (e4m3) quantisation ([VT] fused RMSNorm + static FP8  */
+/* section): the RMSNorm above, its output rounded to bf16 (nb), and the code */
 /*   code_j = e4m3_satfinite( f32(nb_j) * inv_scale ),  inv_scale = 1 / scale  */
 /* where inv_scale and the product are f32 operations (the page computes the  */
 /* code in f32 from the bf16-rounded value), so the code is decided in f32 on */
@@ -208,9 +213,9 @@ void nro_rmsnorm_quant_fp8(int dtype, int64_t rows, int64_t hidden, const void* 
 }
 
 /* ------------------------------------------------------------------------ */
-/* Per-head Q/K RMSNorm followed by NeoX RoPE ([VT] "attn_qk_norm_rope_gate",  */
-/* "rope_neox").  For token t and head h of a tensor with its own norm weight */
-/* w (one vector of length D, shared by all heads):                           */
+/* Per-head Q/K RMSNorm followed by NeoX RoPE ([VT] fused attention-preamble */
+/* and NeoX RoPE sections).  For token t and head h of a tensor with its own  */
+/* norm weight w (one vector of length D, shared by all heads):               */
 /*                                                                            */
 /*   inv = 1 / sqrt(mean_j v_j^2 + eps),   n_j = v_j * inv * w_j (w_j+1 gemma)  */
 /*   for i < D/2:  f_i = theta^(-2i/D)   (double)                             */
@@ -280,8 +285,8 @@ int nro_qk_norm_rope(int dtype, int w_dtype, int64_t tokens, int64_t hq, int64_t
 }
 
 /* ------------------------------------------------------------------------ */
-/* RoPE variants on top of the per-head RMSNorm ([VT] "rope_neox",            */
-/* "Supplied-cache RoPE", "attn_qk_norm_rope_gate"):                           */
+/* RoPE variants on top of the per-head RMSNorm ([VT] NeoX RoPE, cache-driven */
+/* RoPE and fused attention-preamble sections):                              */
 /*  - rotary dim rot <= D: pairs i < rot/2 rotate; elements [rot, D) keep the */
 /*    normed value;  f_i = theta^(-2i/rot)                                     */
 /*  - pairing: rotate-half (i, i + rot/2) or interleaved GPT-J (2i, 2i + 1)    */
@@ -478,7 +483,7 @@ void nro_gated_ln_modulate(int dtype, int64_t rows, int64_t hidden, int64_t rows
 }
 
 /* ------------------------------------------------------------------------ */
-/* silu_and_mul ([VT] "silu_and_mul").  x is [rows, 2*inter]:                 */
+/* silu_and_mul ([VT] SiLU gated-activation section).  x is [rows, 2*inter]: */
 /*   a = x[r, j] (gate, first half), b = x[r, inter + j] (up, second half)    */
 /*   y = a / (1 + exp(-a)) * b;  out[r, j] = round_dtype(y)                   */
 /* ------------------------------------------------------------------------ */
@@ -496,7 +501,7 @@ void nro_silu_and_mul(int dtype, int64_t rows, int64_t inter, const void* x, voi
 }
 
 /* ------------------------------------------------------------------------ */
-/* gelu_and_mul ([VT] "gelu_and_mul"): the tanh form of GELU of the gate     */
+/* gelu_and_mul ([VT] GELU gated-activation section): tanh GELU of the gate   */
 /* (first half) times up (second half):                                      */
 /*   gelu(a) = 0.5 a (1 + tanh(z)),  z = sqrt(2/pi) (a + 0.044715 a^3)        */
 /*   y = gelu(a) * b;  out[r, j] = round_dtype(y)                             */

@@ -19,9 +19,49 @@ Residual write-back: bit-exact.
 """
 from __future__ import annotations
 
+import contextlib
+
 import numpy as np
 
 U32 = 2.0 ** -24  # unit roundoff of f32
+
+# Reports of the checks made inside recording(name) blocks, as (name, report);
+# tests/conftest.py prints one line per name at the end of the run, so the
+# use of the cancellation allowance on the full-size cases is on record.
+REPORTS: list = []
+_recording: list = []
+
+
+@contextlib.contextmanager
+def recording(name: str):
+    """Record the report of every check made inside the block under `name`."""
+    _recording.append(name)
+    try:
+        yield
+    finally:
+        _recording.pop()
+
+
+def _record(report: dict) -> dict:
+    if _recording:
+        REPORTS.append((_recording[-1], report))
+    return report
+
+
+def summarize_reports():
+    """One dict per recorded name: elements checked, elements beyond 1 bf16 ulp
+    (or beyond the f32 relative bound), how many of those the cancellation
+    allowance admitted, and the largest error over mag in units of 2^-24."""
+    out = {}
+    for name, r in REPORTS:
+        s = out.setdefault(name, {"n": 0, "over_1ulp": 0, "cancel_allowance_used": 0,
+                                  "max_err_over_mag_u": 0.0, "max_ulp": 0})
+        s["n"] += r.get("n", 0)
+        s["over_1ulp"] += r.get("over_1ulp", r.get("over_rel", 0))
+        s["cancel_allowance_used"] += r.get("cancel_allowance_used", 0)
+        s["max_err_over_mag_u"] = max(s["max_err_over_mag_u"], r.get("max_err_over_mag_u", 0.0))
+        s["max_ulp"] = max(s["max_ulp"], r.get("max_ulp", 0))
+    return out
 
 
 def bf16_ordinal(bits: np.ndarray) -> np.ndarray:
@@ -79,19 +119,29 @@ def check_bf16(gpu_bits, oracle_bits, y=None, mag=None, k_cancel=None, what=""):
                                  % (what, int(fail.sum()), g[i], y[i], mag[i], allow[i]))
         # The allowance is for rare cancellations, not a blanket widening.
         assert bad.mean() < 1e-3, "%s: %.2e of elements needed the allowance" % (what, bad.mean())
-    return report
+    return _record(report)
 
 
 def check_f32(gpu, y, rel=1e-5, mag=None, k_cancel=None, what=""):
     gpu = np.asarray(gpu, dtype=np.float64).reshape(-1)
     y = np.asarray(y, dtype=np.float64).reshape(-1)
-    allow = np.maximum(rel * np.abs(y), 1e-30)
-    if mag is not None and k_cancel is not None:
-        allow = allow + k_cancel * U32 * np.asarray(mag).reshape(-1)
+    plain = np.maximum(rel * np.abs(y), 1e-30)
+    allow = plain
     err = np.abs(gpu - y)
+    report = {"n": int(gpu.size),
+              "max_rel": float(np.max(err / np.maximum(np.abs(y), 1e-30))) if gpu.size else 0.0}
+    if mag is not None and k_cancel is not None:
+        mag = np.asarray(mag).reshape(-1)
+        allow = plain + k_cancel * U32 * mag
+        over = err > plain
+        report["over_rel"] = int(over.sum())
+        report["cancel_allowance_used"] = int((over & (err <= allow)).sum())
+        if over.any():
+            report["max_err_over_mag_u"] = float(np.max(err[over] / np.maximum(mag[over], 1e-300))
+                                                 / U32)
     fail = err > allow
     if fail.any():
         i = int(np.argmax(err / allow))
         raise AssertionError("%s: %d of %d f32 elements beyond tolerance (worst: gpu %r exact %r)"
                              % (what, int(fail.sum()), gpu.size, gpu[i], y[i]))
-    return {"n": int(gpu.size), "max_rel": float(np.max(err / np.maximum(np.abs(y), 1e-30)))}
+    return _record(report)

@@ -110,3 +110,53 @@ def test_reference_arm_other_ranks_exit_quietly():
                        text=True, timeout=300, cwd=root, env=env)
     assert r.returncode == 0, r.stderr[-2000:]
     assert r.stdout.strip() == ""
+
+
+def test_config_flag_selects_each_workloads_calls():
+    """--config N keeps the calls of workload N only, in both arms' config."""
+    all_names = [s[0] for s in bench.step_shapes(synth)]
+    covered = []
+    for n, names in bench.CONFIG_CALLS.items():
+        shapes = bench.step_shapes(synth, names)
+        assert [s[0] for s in shapes] == list(names), n
+        covered += names
+        cfg = bench.step_config(shapes, 1)
+        assert cfg["bytes_per_step"] == sum(s[1] for s in shapes)
+    assert sorted(covered) == sorted(all_names)  # every call belongs to exactly one workload
+    small = bench.step_config(bench.step_shapes(synth, bench.CONFIG_CALLS[1]), 1)
+    assert "fits in the 129 MB L2" in small["l2"]
+    big = bench.step_config(bench.step_shapes(synth, bench.CONFIG_CALLS[3]), 1)
+    assert ">> 129 MB L2" in big["l2"]
+
+
+def test_seed_flag_replaces_every_workload_seed():
+    import argparse
+    import copy
+
+    saved = {k: copy.deepcopy(getattr(synth, k)) for k in
+             ("RMSNORM_F32", "ADD_RMSNORM", "QK_NORM_ROPE", "LN_MODULATE", "DECODE")}
+    try:
+        sel = bench.apply_workload_args(argparse.Namespace(seed=77, config=4), synth)
+        assert sel == bench.CONFIG_CALLS[4]
+        assert all(getattr(synth, k)["seed"] == 77 for k in saved)
+        assert bench.apply_workload_args(argparse.Namespace(seed=None, config=None), synth) is None
+    finally:
+        for k, v in saved.items():
+            getattr(synth, k).clear()
+            getattr(synth, k).update(v)
+
+
+def test_reference_arm_with_config_and_seed():
+    import json
+    import os
+    import subprocess
+    import sys
+
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference",
+                        "--steps", "1", "--warmup", "3", "--config", "1", "--seed", "5"],
+                       capture_output=True, text=True, timeout=600, cwd=root)
+    assert r.returncode == 0, r.stderr[-2000:]
+    d = json.loads(r.stdout.strip().splitlines()[-1])
+    assert d["config"] == bench.step_config(bench.step_shapes(synth, bench.CONFIG_CALLS[1]), 1)
+    assert "rmsnorm_f32" in d["cpu_baseline"]["sample"] and "qk_norm" not in d["cpu_baseline"]["sample"]

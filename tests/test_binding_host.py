@@ -68,3 +68,108 @@ def test_import_without_the_library_fails_loudly(tmp_path):
     mod = importlib.util.module_from_spec(spec)
     with pytest.raises(ImportError, match="build"):
         spec.loader.exec_module(mod)
+
+
+def _bf(*shape):
+    return torch.zeros(*shape, dtype=torch.bfloat16)
+
+
+MISMATCHED = {
+    # rmsnorm: weight length, residual / out shape and dtype
+    "rmsnorm short w": lambda b: b.rmsnorm(_bf(4, 64), _bf(32)),
+    "rmsnorm f32 w next to bf16 x": lambda b: b.rmsnorm(_bf(4, 64), torch.ones(64)),
+    "rmsnorm short residual": lambda b: b.rmsnorm(_bf(4, 64), _bf(64), residual=_bf(3, 64)),
+    "rmsnorm f32 residual": lambda b: b.rmsnorm(_bf(4, 64), _bf(64), residual=torch.zeros(4, 64)),
+    "rmsnorm strided residual": lambda b: b.rmsnorm(_bf(4, 64), _bf(64), residual=_bf(4, 128)[:, :64]),
+    "rmsnorm short out": lambda b: b.rmsnorm(_bf(4, 64), _bf(64), out=_bf(4, 32)),
+    "fp8 short codes": lambda b: b.rmsnorm_quant_fp8(_bf(4, 64), _bf(64), 1.0,
+                                                     codes=torch.zeros(4, 32, dtype=torch.uint8)),
+    "fp8 codes not bytes": lambda b: b.rmsnorm_quant_fp8(_bf(4, 64), _bf(64), 1.0, codes=_bf(4, 64)),
+    "fp8 out_bf16 f32": lambda b: b.rmsnorm_quant_fp8(_bf(4, 64), _bf(64), 1.0,
+                                                      out_bf16=torch.zeros(4, 64)),
+    "fp8 short w": lambda b: b.rmsnorm_quant_fp8(_bf(4, 64), _bf(8), 1.0),
+    # qk_norm_rope: token counts, head_dim, positions, weights, outputs
+    "qk k with fewer tokens": lambda b: b.qk_norm_rope(_bf(4, 2, 64), _bf(3, 1, 64), torch.ones(64),
+                                                       torch.ones(64), torch.zeros(4, dtype=torch.int32)),
+    "qk k head_dim": lambda b: b.qk_norm_rope(_bf(4, 2, 64), _bf(4, 1, 32), torch.ones(64),
+                                              torch.ones(64), torch.zeros(4, dtype=torch.int32)),
+    "qk short positions": lambda b: b.qk_norm_rope(_bf(4, 2, 64), _bf(4, 1, 64), torch.ones(64),
+                                                   torch.ones(64), torch.zeros(3, dtype=torch.int32)),
+    "qk int64 positions": lambda b: b.qk_norm_rope(_bf(4, 2, 64), _bf(4, 1, 64), torch.ones(64),
+                                                   torch.ones(64), torch.zeros(4, dtype=torch.int64)),
+    "qk strided positions": lambda b: b.qk_norm_rope(_bf(4, 2, 64), _bf(4, 1, 64), torch.ones(64),
+                                                     torch.ones(64),
+                                                     torch.zeros(8, dtype=torch.int32)[::2]),
+    "qk short wq": lambda b: b.qk_norm_rope(_bf(4, 2, 64), _bf(4, 1, 64), torch.ones(32),
+                                            torch.ones(64), torch.zeros(4, dtype=torch.int32)),
+    "qk wq wk dtypes": lambda b: b.qk_norm_rope(_bf(4, 2, 64), _bf(4, 1, 64), torch.ones(64),
+                                                _bf(64), torch.zeros(4, dtype=torch.int32)),
+    "qk q k dtypes": lambda b: b.qk_norm_rope(_bf(4, 2, 64), torch.zeros(4, 1, 64), torch.ones(64),
+                                              torch.ones(64), torch.zeros(4, dtype=torch.int32)),
+    "qk short q_out": lambda b: b.qk_norm_rope(_bf(4, 2, 64), _bf(4, 1, 64), torch.ones(64),
+                                               torch.ones(64), torch.zeros(4, dtype=torch.int32),
+                                               q_out=_bf(3, 2, 64)),
+    "qk k_out dtype": lambda b: b.qk_norm_rope(_bf(4, 2, 64), _bf(4, 1, 64), torch.ones(64),
+                                               torch.ones(64), torch.zeros(4, dtype=torch.int32),
+                                               k_out=torch.zeros(4, 1, 64)),
+    "qk-ex mrope positions [tokens]": lambda b: b.qk_norm_rope_ex(
+        _bf(4, 2, 64), _bf(4, 1, 64), torch.ones(64), torch.ones(64),
+        torch.zeros(4, dtype=torch.int32), mrope_sections=(16, 8, 8)),
+    "qk-ex short positions": lambda b: b.qk_norm_rope_ex(
+        _bf(4, 2, 64), _bf(4, 1, 64), torch.ones(64), torch.ones(64),
+        torch.zeros(2, dtype=torch.int32)),
+    # ln_modulate / gated: sample rows, dtypes, widths
+    "ln shift too few samples": lambda b: b.ln_modulate(_bf(6, 64), _bf(2, 64), _bf(3, 64),
+                                                        rows_per_sample=2),
+    "ln scale width": lambda b: b.ln_modulate(_bf(6, 64), _bf(1, 64), _bf(1, 32)),
+    "ln f32 shift": lambda b: b.ln_modulate(_bf(6, 64), torch.zeros(1, 64), _bf(1, 64)),
+    "ln out shape": lambda b: b.ln_modulate(_bf(6, 64), _bf(1, 64), _bf(1, 64), out=_bf(5, 64)),
+    "ln rows_per_sample 0": lambda b: b.ln_modulate(_bf(6, 64), _bf(1, 64), _bf(1, 64),
+                                                    rows_per_sample=0),
+    "gated short y": lambda b: b.gated_residual_ln_modulate(_bf(6, 64), _bf(5, 64), _bf(1, 64),
+                                                            _bf(1, 64), _bf(1, 64)),
+    "gated per-token gate too short": lambda b: b.gated_residual_ln_modulate(
+        _bf(6, 64), _bf(6, 64), _bf(5, 64), _bf(6, 64), _bf(6, 64), rows_per_sample=1),
+    "gated f32 y": lambda b: b.gated_residual_ln_modulate(_bf(6, 64), torch.zeros(6, 64), _bf(1, 64),
+                                                          _bf(1, 64), _bf(1, 64)),
+    "gated out dtype": lambda b: b.gated_residual_ln_modulate(_bf(6, 64), _bf(6, 64), _bf(1, 64),
+                                                              _bf(1, 64), _bf(1, 64),
+                                                              out=torch.zeros(6, 64)),
+    # activations: output shape and dtype
+    "silu out width": lambda b: b.silu_and_mul(_bf(4, 128), out=_bf(4, 128)),
+    "gelu out dtype": lambda b: b.gelu_and_mul(_bf(4, 128), out=torch.zeros(4, 64)),
+}
+
+
+@pytest.mark.parametrize("case", sorted(MISMATCHED))
+def test_mismatched_operands_are_refused_before_any_launch(binding, case):
+    """Every operand's dtype, shape and layout is checked against the main
+    tensor before the library is called: the C ABI takes bare pointers, so a
+    short or mistyped operand would otherwise be read or written past its end.
+    On this CPU-only machine the tensors are host tensors, so a check that
+    came after the device check would surface as the "CUDA" error instead."""
+    with pytest.raises((ValueError, TypeError)) as err:
+        MISMATCHED[case](binding)
+    assert "CUDA" not in str(err.value), str(err.value)
+
+
+def test_well_formed_operands_reach_the_device_check(binding):
+    """The same calls with matching operands pass every shape check and stop
+    only at the device check (the tensors here are on the host)."""
+    p4 = torch.zeros(4, dtype=torch.int32)
+    calls = [
+        lambda: binding.rmsnorm(_bf(4, 64), _bf(64), residual=_bf(4, 64), out=_bf(4, 64)),
+        lambda: binding.rmsnorm_quant_fp8(_bf(4, 64), _bf(64), 1.0, out_bf16=True),
+        lambda: binding.qk_norm_rope(_bf(4, 2, 64), _bf(4, 1, 64), torch.ones(64), torch.ones(64), p4),
+        lambda: binding.qk_norm_rope_ex(_bf(4, 2, 64), _bf(4, 1, 64), torch.ones(64), torch.ones(64),
+                                        torch.zeros(3, 4, dtype=torch.int32),
+                                        mrope_sections=(16, 8, 8)),
+        lambda: binding.ln_modulate(_bf(6, 64), _bf(3, 64), _bf(3, 64), rows_per_sample=2),
+        lambda: binding.ln_modulate(_bf(6, 64), _bf(64), _bf(1, 64)),
+        lambda: binding.gated_residual_ln_modulate(_bf(6, 64), _bf(6, 64), _bf(6, 64), _bf(6, 64),
+                                                   _bf(6, 64), rows_per_sample=1),
+        lambda: binding.silu_and_mul(_bf(4, 128), out=_bf(4, 64)),
+    ]
+    for call in calls:
+        with pytest.raises(ValueError, match="CUDA"):
+            call()

@@ -10,6 +10,7 @@ import torch
 
 import oracle
 import synth
+from tests import parity
 from tests.gpu_util import Guarded, dev, host_bits
 from tests.parity import check_bf16, check_f32
 
@@ -56,7 +57,8 @@ def run_case(nr, res, y, gate, shift, scale, rps=None, chunk=None, eps=1e-6):
 
 
 def test_dit_shape_26598x3072(nr):
-    run_case(nr, *gated_inputs(26598, 3072, 5), chunk=4096)
+    with parity.recording("gated residual + ln_modulate bf16 [26598, 3072]"):
+        run_case(nr, *gated_inputs(26598, 3072, 5), chunk=4096)
 
 
 def test_per_token_and_per_sample_modulation(nr):

@@ -3,7 +3,7 @@
 bf16 outputs: at most 1 bf16 ulp; f32 outputs: relative error <= 1e-5 (a
 product of gelu_tanh(a) and b, no cancellation; the f32 kernel carries 2z in
 two floats so that e^{2z} keeps its relative accuracy for negative gates).
-Source: vllm.cpp src/vt/cuda/cuda_ops.cu, "gelu_and_mul" (gate first, up
+Source: vllm.cpp src/vt/cuda/cuda_ops.cu, GELU gated-activation section (gate first, up
 second, the tanh form of GELU)."""
 import numpy as np
 import pytest

@@ -18,6 +18,7 @@ import torch
 
 import oracle
 import synth
+from tests import parity
 from tests.gpu_util import Guarded, dev, host_bits
 from tests.parity import check_bf16, check_f32
 
@@ -57,7 +58,8 @@ def test_config_ln_modulate_26598x3072(nr):
     """The full workload the bench times: x [26598, 3072] bf16, one shift/scale
     sample for all rows; compared in row chunks."""
     c = synth.LN_MODULATE
-    run_case(nr, c["rows"], c["hidden"], eps=c["eps"], seed=c["seed"], chunk=4096)
+    with parity.recording("ln_modulate bf16 [26598, 3072]"):
+        run_case(nr, c["rows"], c["hidden"], eps=c["eps"], seed=c["seed"], chunk=4096)
 
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])

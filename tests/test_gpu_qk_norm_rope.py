@@ -9,8 +9,8 @@ the kernel's f32 roundings: ~19 in the head's sum of squares (16 per lane +
 on n), ~4 absolute on cos/sin (argument conversion + sincospif) plus the
 oracle's own double rounding of pos*freq at |pos| up to 2^31 (~4), and the
 final product and fma: < 32 in all.  f32 outputs: relative 1e-5 plus the same
-allowance.  Sources: vllm.cpp src/vt/cuda/cuda_ops.cu, "attn_qk_norm_rope_gate"
-and "rope_neox".
+allowance.  Sources: the vllm.cpp page src/vt/cuda/cuda_ops.cu,
+its fused attention-preamble and NeoX RoPE sections.
 """
 import numpy as np
 import pytest
@@ -18,6 +18,7 @@ import torch
 
 import oracle
 import synth
+from tests import parity
 from tests.gpu_util import Guarded, dev, host_bits
 from tests.parity import bf16_ulp_distance, check_bf16, check_f32
 
@@ -67,8 +68,10 @@ def test_config_qk_norm_rope_26598x24x128(nr, w_dtype):
     """The full workload the bench times: Q, K [26598, 24, 128] bf16,
     positions 0..26597, theta 1e4; compared in token chunks."""
     c = synth.QK_NORM_ROPE
-    reps = run_case(nr, c["tokens"], c["hq"], c["hk"], c["head_dim"], w_dtype=w_dtype,
-                    eps=c["eps"], theta=c["theta"], seed=c["seed"], chunk=2048)
+    with parity.recording("qk_norm_rope bf16 [26598, 24+24, 128], %s weights"
+                          % str(w_dtype).split(".")[-1]):
+        reps = run_case(nr, c["tokens"], c["hq"], c["hk"], c["head_dim"], w_dtype=w_dtype,
+                        eps=c["eps"], theta=c["theta"], seed=c["seed"], chunk=2048)
     total = sum(r["n"] for r in reps)
     assert total == 2 * c["tokens"] * c["hq"] * c["head_dim"]
 

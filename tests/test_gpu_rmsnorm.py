@@ -3,8 +3,8 @@ against the oracle, element by element, on seeded inputs.
 
 bf16 outputs: at most 1 bf16 ulp; f32 outputs: relative error <= 1e-5;
 residual write-back: bit-exact.  RMSNorm's last step is a product, so no
-cancellation allowance applies.  Source: vllm.cpp src/vt/cuda/cuda_ops.cu,
-"rmsnorm: one block per row" and "ResRound".
+cancellation allowance applies.  Source: the vllm.cpp page src/vt/cuda/cuda_ops.cu,
+its row-RMSNorm section and the residual-rounding helper before it.
 """
 import numpy as np
 import pytest
@@ -12,6 +12,7 @@ import torch
 
 import oracle
 import synth
+from tests import parity
 from tests.gpu_util import Guarded, dev, host_bits
 from tests.parity import check_bf16, check_f32
 
@@ -59,8 +60,9 @@ def test_config_add_rmsnorm_bf16_8192x5120(nr, gemma):
     """bf16 add + RMSNorm, 8192 x 5120, residual in place, gemma false and true
     (the full workload the bench times, same entry point and launch)."""
     c = synth.ADD_RMSNORM
-    run_case(nr, c["rows"], c["hidden"], torch.bfloat16, residual=True, gemma=gemma, eps=c["eps"],
-             seed=c["seed"])
+    with parity.recording("add_rmsnorm bf16 [8192, 5120], gemma %d" % gemma):
+        run_case(nr, c["rows"], c["hidden"], torch.bfloat16, residual=True, gemma=gemma,
+                 eps=c["eps"], seed=c["seed"])
 
 
 @pytest.mark.parametrize("hidden", synth.DECODE["hidden"])

@@ -4,7 +4,7 @@ The bf16 intermediate follows the RMSNorm rule (1 bf16 ulp; residual bit-exact).
 The e4m3 code is decided in f32 from that bf16 value on both sides, so it must
 be bit-exact wherever the GPU's bf16 value equals the oracle's, and elsewhere
 equal to the oracle's conversion of the GPU's own bf16 value.  Source: vllm.cpp
-src/vt/cuda/cuda_ops.cu, "rmsnorm + static fp8 quant"."""
+src/vt/cuda/cuda_ops.cu, its fused RMSNorm + static FP8 section."""
 import numpy as np
 import pytest
 import torch

@@ -1,15 +1,16 @@
 """GPU parity: nr_qk_norm_rope_ex (RoPE variants) against the oracle.
 
 Same tolerance as test_gpu_qk_norm_rope.py (1 bf16 ulp, or the cancellation
-allowance with K = 32).  Sources: vllm.cpp src/vt/cuda/cuda_ops.cu, "rope_neox"
-(Llama-3 rescale), "Supplied-cache RoPE" (GPT-J pairs, M-RoPE axis selection),
-"attn_qk_norm_rope_gate" (partial rotary)."""
+allowance with K = 32).  Sources: vllm.cpp src/vt/cuda/cuda_ops.cu, the NeoX RoPE
+section (Llama-3 rescale), the cache-driven RoPE section (GPT-J pairs, M-RoPE
+axis selection), the fused attention-preamble section (partial rotary)."""
 import numpy as np
 import pytest
 import torch
 
 import oracle
 import synth
+from tests import parity
 from tests.gpu_util import Guarded, dev, host_bits
 from tests.parity import check_bf16, check_f32
 
@@ -104,13 +105,17 @@ def test_variants_at_the_benchmark_shape(nr, kw):
     torch.cuda.synchronize()
     gq, gk = host_bits(qo), host_bits(ko)
     qb, kb = host_bits(q), host_bits(k)
-    for t0 in range(0, T, 4096):
-        t1 = min(t0 + 4096, T)
-        p = pos[..., t0:t1].contiguous().numpy()
-        ref = oracle.qk_norm_rope_ex(qb[t0:t1], kb[t0:t1], host_bits(wq), host_bits(wk), p,
-                                     want_y=True, **kw)
-        check_bf16(gq[t0:t1], ref[0], ref[2], ref[4], k_cancel=K_ROPE, what="rope-ex q %d" % t0)
-        check_bf16(gk[t0:t1], ref[1], ref[3], ref[5], k_cancel=K_ROPE, what="rope-ex k %d" % t0)
+    name = ",".join("%s=%s" % kv for kv in sorted(kw.items()))
+    with parity.recording("rope variant %s bf16 [26598, 24+24, 128]" % name):
+        for t0 in range(0, T, 4096):
+            t1 = min(t0 + 4096, T)
+            p = pos[..., t0:t1].contiguous().numpy()
+            ref = oracle.qk_norm_rope_ex(qb[t0:t1], kb[t0:t1], host_bits(wq), host_bits(wk), p,
+                                         want_y=True, **kw)
+            check_bf16(gq[t0:t1], ref[0], ref[2], ref[4], k_cancel=K_ROPE,
+                       what="rope-ex q %d" % t0)
+            check_bf16(gk[t0:t1], ref[1], ref[3], ref[5], k_cancel=K_ROPE,
+                       what="rope-ex k %d" % t0)
 
 
 def test_gptj_partial_many_tokens_gqa_and_odd_head_counts(nr):

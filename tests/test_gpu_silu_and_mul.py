@@ -2,7 +2,7 @@
 
 bf16 outputs: at most 1 bf16 ulp; f32 outputs: relative error <= 1e-5 (the op
 is a product of silu(a) and b, so there is no cancellation).  Source: vllm.cpp
-src/vt/cuda/cuda_ops.cu, "silu_and_mul" (gate first, up second)."""
+src/vt/cuda/cuda_ops.cu, SiLU gated-activation section (gate first, up second)."""
 import pytest
 import torch
 
@@ -49,13 +49,18 @@ def test_more_rows_than_one_grid_column(nr):
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
 def test_extreme_gates(nr, dtype):
-    """Gates where e^-a overflows or vanishes in f32."""
+    """Gates where e^-a overflows or vanishes in f32.  The gates -89, -90 and
+    -91 (e^-a beyond the f32 range, a * e^a still a normal f32) are paired with
+    ups of +-1e30, so that the product sits far above the comparison's absolute
+    floor and its relative error is what is checked."""
     gates = [-120.0, -100.0, -88.0, -87.0, -50.0, -20.0, -1.0, 0.0, 1.0, 20.0, 50.0, 88.0, 100.0,
-             120.0, -0.0, 1e-30]
+             120.0, -0.0, 1e-30, -89.0, -90.0, -91.0]
     n = len(gates)
     x = torch.empty(1, 2 * n, dtype=torch.float32)
     x[0, :n] = torch.tensor(gates)
     x[0, n:] = torch.linspace(-2, 2, n)
+    if dtype == torch.float32:
+        x[0, 2 * n - 3:] = torch.tensor([1e30, -1e30, 1e30])
     n8 = (n + 7) // 8 * 8
     xp = torch.zeros(1, 2 * n8, dtype=torch.float32)
     xp[0, :n] = x[0, :n]

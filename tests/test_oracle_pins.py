@@ -3,10 +3,10 @@ exact brute force, each chosen so that a plausible slip in the oracle (a dropped
 term, a wrong sign, index or operand order, a misplaced eps, a missing rounding)
 fails at least one of them.  The oracle is never compared with itself here.
 
-Sources (page, section): vllm.cpp src/vt/cuda/cuda_ops.cu -- "f32 load/store
-overloads", "ResRound", "rmsnorm: one block per row", "rope_neox",
-"attn_qk_norm_rope_gate", "silu_and_mul"; FastVideo PAN2 docs, "Performance
-switches" (dit_fused_kernels: LayerNorm + modulation).
+Sources (page, section): vllm.cpp src/vt/cuda/cuda_ops.cu -- the bf16
+load/store helpers, the residual-rounding helper, the row-RMSNorm, NeoX RoPE,
+fused attention-preamble and gated-activation sections; FastVideo PAN2 docs,
+"Performance switches" (dit_fused_kernels: LayerNorm + modulation).
 """
 import math
 import os
@@ -469,7 +469,7 @@ def test_rope_ex_defaults_equal_the_plain_rope():
 
 @pytest.mark.parametrize("variant", [{}, {"rotary_dim": 32}, {"interleaved": True}])
 def test_rope_gemma_adds_one_to_both_weights(variant):
-    """gemma uses w + 1 for the head norm ("attn_qk_norm_rope_gate"): with
+    """gemma uses w + 1 for the head norm (fused attention-preamble section): with
     weights whose w + 1 is exact, gemma on w equals gemma off on w + 1, for Q
     and for K, in the plain kernel and the variants."""
     q, k, _, _, _ = _qk_small(tokens=3, hq=2, hk=2, D=64, seed=94)

@@ -64,6 +64,13 @@ __device__ __forceinline__ float row_group_sum(float v, float* scratch) {
   return total;
 }
 
+// 1: cap the LayerNorm grid at the blocks resident at once, each looping over
+// its row groups (no block launches after the first wave); 0: one block per
+// row group (a build-time knob).
+#ifndef NR_LN_PERSIST
+#define NR_LN_PERSIST 0
+#endif
+
 template <typename T, int VPT, int WPR>
 __global__ void __launch_bounds__(ln_row_threads<WPR>()) ln_modulate_rows_kernel(
     T* __restrict__ out, const T* __restrict__ x, const T* __restrict__ shift,
@@ -78,65 +85,77 @@ __global__ void __launch_bounds__(ln_row_threads<WPR>()) ln_modulate_rows_kernel
   __shared__ float scratch_mean[THREADS / kWarp];
   __shared__ float scratch_var[THREADS / kWarp];
   const int t = threadIdx.x % TPR;
-  const int64_t row = static_cast<int64_t>(blockIdx.x) * RPB + threadIdx.x / TPR;
-  // Rows past the end still take part in the reductions' barriers (WPR > 1).
-  const bool active = row < rows;
-  const int64_t r = active ? row : 0;
-  const uint4* xr = reinterpret_cast<const uint4*>(x) + r * nvec;
-  uint4* orow = reinterpret_cast<uint4*>(out) + r * nvec;
-  const int64_t sample_off = (r / rows_per_sample) * nvec;
-  const uint4* shv = reinterpret_cast<const uint4*>(shift) + sample_off;
-  const uint4* scv = reinterpret_cast<const uint4*>(scale) + sample_off;
+  // One pass over the block's row group; a grid capped at the resident
+  // blocks (NR_LN_PERSIST) loops over row groups.
+  auto pass = [&](int64_t base) {
+    const int64_t row = base + threadIdx.x / TPR;
+    // Rows past the end still take part in the reductions' barriers (WPR > 1).
+    const bool active = row < rows;
+    const int64_t r = active ? row : 0;
+    const uint4* xr = reinterpret_cast<const uint4*>(x) + r * nvec;
+    uint4* orow = reinterpret_cast<uint4*>(out) + r * nvec;
+    const int64_t sample_off = (r / rows_per_sample) * nvec;
+    const uint4* shv = reinterpret_cast<const uint4*>(shift) + sample_off;
+    const uint4* scv = reinterpret_cast<const uint4*>(scale) + sample_off;
 
-  uint4 xv[VPT];
+    uint4 xv[VPT];
 #pragma unroll
-  for (int k = 0; k < VPT; k++) {
-    const int vi = t + k * TPR;
-    if (active && vi < nvec) xv[k] = ld_stream(xr + vi);
-  }
-
-  float sum = 0.0f;
-#pragma unroll
-  for (int k = 0; k < VPT; k++) {
-    const int vi = t + k * TPR;
-    if (active && vi < nvec) {
-      float v[N];
-      Vec<T>::unpack(xv[k], v);
-#pragma unroll
-      for (int e = 0; e < N; e++) sum += v[e];
+    for (int k = 0; k < VPT; k++) {
+      const int vi = t + k * TPR;
+      if (active && vi < nvec) xv[k] = ld_stream(xr + vi);
     }
-  }
-  const float mu = __fdiv_rn(row_group_sum<WPR>(sum, scratch_mean), hidden_f);
 
-  float dev = 0.0f;
+    float sum = 0.0f;
 #pragma unroll
-  for (int k = 0; k < VPT; k++) {
-    const int vi = t + k * TPR;
-    if (active && vi < nvec) {
-      float v[N];
-      Vec<T>::unpack(xv[k], v);
+    for (int k = 0; k < VPT; k++) {
+      const int vi = t + k * TPR;
+      if (active && vi < nvec) {
+        float v[N];
+        Vec<T>::unpack(xv[k], v);
 #pragma unroll
-      for (int e = 0; e < N; e++) {
-        const float d = v[e] - mu;
-        dev = fmaf(d, d, dev);
+        for (int e = 0; e < N; e++) sum += v[e];
       }
     }
-  }
-  const float rstd = 1.0f / sqrtf(__fdiv_rn(row_group_sum<WPR>(dev, scratch_var), hidden_f) + eps);
-  if (!active) return;
+    const float mu = __fdiv_rn(row_group_sum<WPR>(sum, scratch_mean), hidden_f);
+
+    float dev = 0.0f;
+#pragma unroll
+    for (int k = 0; k < VPT; k++) {
+      const int vi = t + k * TPR;
+      if (active && vi < nvec) {
+        float v[N];
+        Vec<T>::unpack(xv[k], v);
+#pragma unroll
+        for (int e = 0; e < N; e++) {
+          const float d = v[e] - mu;
+          dev = fmaf(d, d, dev);
+        }
+      }
+    }
+    const float rstd =
+        1.0f / sqrtf(__fdiv_rn(row_group_sum<WPR>(dev, scratch_var), hidden_f) + eps);
+    if (!active) return;
 
 #pragma unroll
-  for (int k = 0; k < VPT; k++) {
-    const int vi = t + k * TPR;
-    if (vi < nvec) {
-      float v[N], sh[N], sc[N];
-      Vec<T>::unpack(xv[k], v);
-      Vec<T>::unpack(ld_param(shv + vi), sh);
-      Vec<T>::unpack(ld_param(scv + vi), sc);
+    for (int k = 0; k < VPT; k++) {
+      const int vi = t + k * TPR;
+      if (vi < nvec) {
+        float v[N], sh[N], sc[N];
+        Vec<T>::unpack(xv[k], v);
+        Vec<T>::unpack(ld_param(shv + vi), sh);
+        Vec<T>::unpack(ld_param(scv + vi), sc);
 #pragma unroll
-      for (int e = 0; e < N; e++) v[e] = fmaf((v[e] - mu) * rstd, 1.0f + sc[e], sh[e]);
-      st_stream(orow + vi, Vec<T>::pack(v));
+        for (int e = 0; e < N; e++) v[e] = fmaf((v[e] - mu) * rstd, 1.0f + sc[e], sh[e]);
+        st_stream(orow + vi, Vec<T>::pack(v));
+      }
     }
+  };
+  if (NR_LN_PERSIST) {
+    for (int64_t base = static_cast<int64_t>(blockIdx.x) * RPB; base < rows;
+         base += static_cast<int64_t>(gridDim.x) * RPB)
+      pass(base);
+  } else {
+    pass(static_cast<int64_t>(blockIdx.x) * RPB);
   }
 }
 
@@ -163,24 +182,28 @@ struct GatedAdd<float> {
 
 template <>
 struct GatedAdd<__nv_bfloat16> {
-  // g*y of two bf16 values is exact in f32; TwoSum gives the exact error of
-  // adding r, and round_sum_bf16 rounds the exact sum once.
+  // g*y of two bf16 values is exact in f32.  The sum with r is rounded to odd
+  // in f32: the sums rounded down and up are equal when the sum is exact (the
+  // upward one then carries the sign IEEE gives an exact zero), and otherwise
+  // are the two floats around it, of which the one with an odd last bit is
+  // taken.  f32 keeps 16 more bits than bf16 (at least two are needed), so
+  // rounding that to nearest bf16 rounds the exact r + g*y once (Boldo and
+  // Melquiond, "Emulation of FMA and correctly rounded sums: proved
+  // algorithms using rounding to odd", IEEE Trans. Computers 57(4), 2008).
   __device__ __forceinline__ static uint4 apply(const uint4& r, const uint4& g, const uint4& y) {
     float rv[8], gv[8], yv[8];
     Vec<__nv_bfloat16>::unpack(r, rv);
     Vec<__nv_bfloat16>::unpack(g, gv);
     Vec<__nv_bfloat16>::unpack(y, yv);
-    uint32_t bits[8];
+    float odd[8];
 #pragma unroll
     for (int e = 0; e < 8; e++) {
       const float p = gv[e] * yv[e];
-      const float sum = p + rv[e];
-      const float bb = sum - p;
-      const float err = (p - (sum - bb)) + (rv[e] - bb);
-      bits[e] = round_sum_bf16(sum, err);
+      const float down = __fadd_rd(p, rv[e]);
+      const float up = __fadd_ru(p, rv[e]);
+      odd[e] = (down != up && (__float_as_uint(down) & 1u)) ? down : up;
     }
-    return make_uint4(bits[0] | (bits[1] << 16), bits[2] | (bits[3] << 16),
-                      bits[4] | (bits[5] << 16), bits[6] | (bits[7] << 16));
+    return Vec<__nv_bfloat16>::pack(odd);
   }
 };
 
@@ -358,7 +381,18 @@ cudaError_t launch_rows(const LnArgs& a, cudaStream_t s) {
   constexpr int THREADS = ln_row_threads<WPR>();
   constexpr int RPB = THREADS / (kWarp * WPR);
   static_assert(RPB >= 1, "row groups must fit the block");
-  const int64_t blocks = (a.rows + RPB - 1) / RPB;
+  int64_t blocks = (a.rows + RPB - 1) / RPB;
+  if (NR_LN_PERSIST) {
+    int device = 0, sms = 0, per_sm = 0;
+    cudaError_t e = cudaGetDevice(&device);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
+    if (e == cudaSuccess)
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+          &per_sm, ln_modulate_rows_kernel<T, VPT, WPR>, THREADS, 0);
+    if (e != cudaSuccess) return e;
+    const int64_t resident = static_cast<int64_t>(sms) * (per_sm > 0 ? per_sm : 1);
+    if (blocks > resident) blocks = resident;
+  }
   return launch_pdl(ln_modulate_rows_kernel<T, VPT, WPR>, dim3(static_cast<unsigned>(blocks)),
                     dim3(THREADS), 0, s,
       static_cast<T*>(a.out), static_cast<const T*>(a.x), static_cast<const T*>(a.shift),

@@ -454,9 +454,6 @@ nr_status nr_device_status(cudaStream_t stream) {
   if (bits & nr::kStatusBitQkBulkWait)
     return fail(NR_ERR_TIMEOUT, "nr_device_status: a bounded wait for a bulk copy ran out in the "
                                 "Q/K norm + RoPE kernel (status bits 0x%x)", bits);
-  if (bits & nr::kStatusBitLnBulkWait)
-    return fail(NR_ERR_TIMEOUT, "nr_device_status: a bounded wait for a bulk copy ran out in the "
-                                "LayerNorm + modulation kernel (status bits 0x%x)", bits);
   if (bits != 0)
     return fail(NR_ERR_TIMEOUT, "nr_device_status: the wait probe's wait ran out (status bits "
                                 "0x%x)", bits);

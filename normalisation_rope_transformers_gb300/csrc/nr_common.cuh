@@ -274,21 +274,6 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&h);
 }
 
-// round_bf16(s + e) for an f32 sum s and the exact error e of the addition
-// that produced it (|e| <= half an f32 ulp of s): the result is round_bf16(s),
-// except when s sits exactly on a bf16 midpoint and e moves the true value off
-// it, where e's direction decides.  Returns the 16-bit pattern.
-__device__ __forceinline__ uint32_t round_sum_bf16(float s, float e) {
-  const uint32_t u = __float_as_uint(s);
-  const __nv_bfloat16 b = __float2bfloat16_rn(s);
-  uint32_t bits = *reinterpret_cast<const unsigned short*>(&b);
-  if ((u & 0xFFFFu) == 0x8000u && e != 0.0f) {
-    const bool away_from_zero = (e > 0.0f) == (s > 0.0f);
-    bits = (u >> 16) + (away_from_zero ? 1u : 0u);
-  }
-  return bits;
-}
-
 template <>
 struct Vec<__nv_bfloat16> {
   static constexpr int N = 8;

@@ -113,7 +113,6 @@ cudaError_t launch_qk_norm_rope(void* q_out, void* k_out, const void* q, const v
 // Device status word: bits set by kernels whose bounded waits ran out.
 constexpr unsigned kStatusBitQkBulkWait = 1u;
 constexpr unsigned kStatusBitProbeWait = 2u;
-constexpr unsigned kStatusBitLnBulkWait = 4u;
 
 // Device address of the current device's status word (status.cu), looked up
 // once per device.  Kernels that bound a wait take it as an argument.

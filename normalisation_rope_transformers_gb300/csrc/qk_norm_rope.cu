@@ -359,6 +359,34 @@ __global__ void __launch_bounds__(kQkThreads) qk_norm_rope_kernel(const QkArgs a
 #define NR_QKB_HINT 3
 #endif
 
+// 1: each lane keeps its Q and K weights in registers (16 + 16 floats for
+// head_dim 128 bf16) instead of reading them from shared memory for every
+// head row; a build-time knob.
+#ifndef NR_QKB_WREG
+#define NR_QKB_WREG 0
+#endif
+
+// Minimum resident blocks per SM asked of the compiler for the full-head bulk
+// kernel (a build-time knob; 0: none asked; shared memory allows 5 at 24 + 24
+// heads of 128).
+#ifndef NR_QKB_MINB
+#define NR_QKB_MINB 0
+#endif
+#if NR_QKB_MINB > 0
+#define NR_QKB_BOUNDS __launch_bounds__(kBulkThreads, NR_QKB_MINB)
+#else
+#define NR_QKB_BOUNDS __launch_bounds__(kBulkThreads)
+#endif
+
+// Where the full-head bulk kernel writes its results (a build-time knob):
+// 0: back into the stage, then two bulk stores per token, the stage refilled
+// once the stores have read it; 1: straight from registers to global memory
+// (streaming stores), so a stage is refilled as soon as the block has read
+// it and NST tokens stay in flight instead of NST - 1.
+#ifndef NR_QKB_STORE
+#define NR_QKB_STORE 0
+#endif
+
 // Warps per block (they split each token's head rows); a build-time knob.
 #ifndef NR_QKB_WARPS
 #define NR_QKB_WARPS 4
@@ -389,10 +417,9 @@ struct BulkSmem {
 };
 
 template <typename T, typename WT, int L, int NST>
-__global__ void __launch_bounds__(kBulkThreads) qk_norm_rope_bulk_kernel(const QkArgs a,
+__global__ void NR_QKB_BOUNDS qk_norm_rope_bulk_kernel(const QkArgs a,
                                                                        const RopeTurns turns,
                                                                        const BulkGeom geo) {
-  pdl_enter();  // before any global read: the previous kernel may still run
   using S = BulkSmem<T, L>;
   constexpr int N = Vec<T>::N;
   constexpr int HALF = S::HALF;
@@ -414,21 +441,14 @@ __global__ void __launch_bounds__(kBulkThreads) qk_norm_rope_bulk_kernel(const Q
   const int lane32 = tid % kWarp;
   const WT* wq = static_cast<const WT*>(a.wq);
   const WT* wk = static_cast<const WT*>(a.wk);
-  for (int i = tid; i < 2 * D; i += kBulkThreads) {
-    float wv = 0.0f;
-    if (i < D)
-      wv = load_w<WT>(wq, i);
-    else if (a.hk > 0)
-      wv = load_w<WT>(wk, i - D);
-    wsm[i] = wv + a.w_add;
-  }
+  // Set-up from kernel parameters into shared memory (no global read), before
+  // the wait for the previous kernel: the rotary turns and the barriers.
   for (int i = tid; i < HALF; i += kBulkThreads) turn_sm[i] = turns.turn[i];
   if (tid == 0) {
     for (int st = 0; st < NST; st++) mbar_init(smem_addr(bars + st), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  __syncthreads();
 
   const int64_t C = gridDim.x;
   const int64_t t0 = blockIdx.x;
@@ -465,8 +485,20 @@ __global__ void __launch_bounds__(kBulkThreads) qk_norm_rope_bulk_kernel(const Q
       if (geo.k_bytes) bulk_prefetch_l2(k + ptok * a.k_stride, geo.k_bytes);
     }
   };
+  pdl_enter();  // before any global read: the previous kernel may still run
+  // The first tokens' loads go out before the weights are read, so their
+  // latency overlaps the rest of the set-up.
   if (tid == 0)
-    for (int64_t j = 0; j < NST - 1 && j < ntok; j++) issue(j);
+    for (int64_t j = 0; j < (NR_QKB_STORE ? NST : NST - 1) && j < ntok; j++) issue(j);
+  for (int i = tid; i < 2 * D; i += kBulkThreads) {
+    float wv = 0.0f;
+    if (i < D)
+      wv = load_w<WT>(wq, i);
+    else if (a.hk > 0)
+      wv = load_w<WT>(wk, i - D);
+    wsm[i] = wv + a.w_add;
+  }
+  __syncthreads();  // weights, turns and barriers visible to every thread
 
   // Angle table of a token into table buffer b (threads < HALF, strided).
   auto angles = [&](int b, int p) {
@@ -490,6 +522,20 @@ __global__ void __launch_bounds__(kBulkThreads) qk_norm_rope_bulk_kernel(const Q
 
   const int g = lane32 / L;
   const int l = lane32 % L;
+  // This lane's weights (it always owns vectors l and l + L of a row), kept
+  // in registers when NR_QKB_WREG is set instead of read from shared memory
+  // for every head row.
+  float wqa[NR_QKB_WREG ? N : 1], wqb[NR_QKB_WREG ? N : 1];
+  float wka[NR_QKB_WREG ? N : 1], wkb[NR_QKB_WREG ? N : 1];
+  if (NR_QKB_WREG) {
+#pragma unroll
+    for (int e = 0; e < (NR_QKB_WREG ? N : 1); e++) {
+      wqa[e] = wsm[l * N + e];
+      wqb[e] = wsm[HALF + l * N + e];
+      wka[e] = wsm[D + l * N + e];
+      wkb[e] = wsm[D + HALF + l * N + e];
+    }
+  }
   int64_t j = 0;
   for (; j < ntok; j++) {
     const int64_t tok = t0 + j * C;
@@ -531,22 +577,39 @@ __global__ void __launch_bounds__(kBulkThreads) qk_norm_rope_bulk_kernel(const Q
       float oa[N], ob[N];
 #pragma unroll
       for (int e = 0; e < N; e++) {
-        const float na = xa[e] * inv * wa[e];
-        const float nb = xb[e] * inv * wb[e];
+        const float we_a = NR_QKB_WREG ? (is_q ? wqa[NR_QKB_WREG ? e : 0] : wka[NR_QKB_WREG ? e : 0])
+                                       : wa[e];
+        const float we_b = NR_QKB_WREG ? (is_q ? wqb[NR_QKB_WREG ? e : 0] : wkb[NR_QKB_WREG ? e : 0])
+                                       : wb[e];
+        const float na = xa[e] * inv * we_a;
+        const float nb = xb[e] * inv * we_b;
         oa[e] = fmaf(na, cs[e].x, -nb * cs[e].y);
         ob[e] = fmaf(na, cs[e].y, nb * cs[e].x);
       }
-      r[l] = Vec<T>::pack(oa);
-      r[l + L] = Vec<T>::pack(ob);
+      if (NR_QKB_STORE) {
+        uint4* o = reinterpret_cast<uint4*>(
+            is_q ? q_out + tok * a.q_stride + static_cast<int64_t>(row) * D
+                 : k_out + tok * a.k_stride + static_cast<int64_t>(row - a.hq) * D);
+        st_stream(o + l, Vec<T>::pack(oa));
+        st_stream(o + l + L, Vec<T>::pack(ob));
+      } else {
+        r[l] = Vec<T>::pack(oa);
+        r[l + L] = Vec<T>::pack(ob);
+      }
     }
     // the next token's angles, into the other table buffer
     if (tid < HALF && j + 1 < ntok) {
       angles(static_cast<int>((j + 1) & 1), pos_next);
       if (j + 2 < ntok) pos_next = a.pos[t0 + (j + 2) * C];
     }
-    fence_proxy_async_smem();
+    if (!NR_QKB_STORE) fence_proxy_async_smem();
     __syncthreads();
     if (*abort_flag) break;
+    if (NR_QKB_STORE) {
+      // every thread has read the stage: refill it with the token NST ahead
+      if (tid == 0 && j + NST < ntok) issue(j + NST);
+      continue;
+    }
     if (tid == 0) {
       if (NR_QKB_HINT & 2) {
         bulk_store_hint(q_out + tok * a.q_stride, smem_addr(st), geo.q_bytes, policy);
@@ -593,7 +656,6 @@ template <typename T, typename WT, int L, int NST>
 __global__ void __launch_bounds__(kBulkThreads, NR_QKV_MINB) qk_norm_rope_bulk_var_kernel(const QkArgs a,
                                                                        const RopeTurns turns,
                                                                        const BulkGeom geo) {
-  pdl_enter();  // before any global read: the previous kernel may still run
   using S = BulkSmem<T, L>;
   constexpr int N = Vec<T>::N;
   constexpr int HALF = S::HALF;
@@ -615,21 +677,14 @@ __global__ void __launch_bounds__(kBulkThreads, NR_QKV_MINB) qk_norm_rope_bulk_v
   const int lane32 = tid % kWarp;
   const WT* wq = static_cast<const WT*>(a.wq);
   const WT* wk = static_cast<const WT*>(a.wk);
-  for (int i = tid; i < 2 * D; i += kBulkThreads) {
-    float wv = 0.0f;
-    if (i < D)
-      wv = load_w<WT>(wq, i);
-    else if (a.hk > 0)
-      wv = load_w<WT>(wk, i - D);
-    wsm[i] = wv + a.w_add;
-  }
+  // Set-up from kernel parameters into shared memory (no global read), before
+  // the wait for the previous kernel: the rotary turns and the barriers.
   for (int i = tid; i < HALF; i += kBulkThreads) turn_sm[i] = turns.turn[i];
   if (tid == 0) {
     for (int st = 0; st < NST; st++) mbar_init(smem_addr(bars + st), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  __syncthreads();
 
   const int64_t C = gridDim.x;
   const int64_t t0 = blockIdx.x;
@@ -666,8 +721,20 @@ __global__ void __launch_bounds__(kBulkThreads, NR_QKV_MINB) qk_norm_rope_bulk_v
       if (geo.k_bytes) bulk_prefetch_l2(k + ptok * a.k_stride, geo.k_bytes);
     }
   };
+  pdl_enter();  // before any global read: the previous kernel may still run
+  // The first tokens' loads go out before the weights are read, so their
+  // latency overlaps the rest of the set-up.
   if (tid == 0)
     for (int64_t j = 0; j < NST - 1 && j < ntok; j++) issue(j);
+  for (int i = tid; i < 2 * D; i += kBulkThreads) {
+    float wv = 0.0f;
+    if (i < D)
+      wv = load_w<WT>(wq, i);
+    else if (a.hk > 0)
+      wv = load_w<WT>(wk, i - D);
+    wsm[i] = wv + a.w_add;
+  }
+  __syncthreads();  // weights, turns and barriers visible to every thread
 
   // Angle table of a token into table buffer b: pairs of the rotated block.
   const int rot_pairs = a.rot_vec * N / 2;

@@ -102,3 +102,29 @@ def test_large_offset_rows(nr):
     """Rows with a large common offset (mean >> sigma) stay within the bound."""
     x, _, _ = synth.ln_inputs(16, 2048, 9, torch.float32)
     run_case(nr, 16, 2048, dtype=torch.bfloat16, x=(x * 0.5 + 40.0).to(torch.bfloat16), seed=9)
+
+
+# Many rows (more than 64 per SM of a 152-SM GB300) at several row widths.
+MANY_ROWS = 64 * 152
+
+
+@pytest.mark.parametrize("hidden", [64, 1024, 2048, 3000, 3072, 4096])
+def test_many_rows_hidden_sizes(nr, hidden):
+    """One- and two-warp rows, a width that leaves lanes idle (3000 = 375
+    vectors), and the smallest row."""
+    run_case(nr, MANY_ROWS + 37, hidden, seed=hidden % 97, chunk=4096)
+
+
+def test_many_rows_in_place_and_modulation_rows(nr):
+    run_case(nr, MANY_ROWS + 5, 3072, seed=41, inplace=True, chunk=4096)
+    run_case(nr, MANY_ROWS, 1024, samples=MANY_ROWS, rps=1, seed=42, chunk=4096)
+    run_case(nr, MANY_ROWS + 3, 1024, samples=(MANY_ROWS + 3 + 99) // 100, rps=100, seed=43,
+             chunk=4096)
+
+
+def test_many_constant_rows_give_shift(nr):
+    hidden = 3072
+    _, shift, scale = synth.ln_inputs(1, hidden, 44, torch.bfloat16)
+    x = torch.full((MANY_ROWS, hidden), 0.7, dtype=torch.bfloat16)
+    out = nr.ln_modulate(dev(x), dev(shift), dev(scale)).cpu()
+    assert torch.equal(out, shift.expand(MANY_ROWS, hidden))

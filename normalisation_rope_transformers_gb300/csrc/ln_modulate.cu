@@ -64,6 +64,89 @@ __device__ __forceinline__ float row_group_sum(float v, float* scratch) {
   return total;
 }
 
+// 1: the bf16 LayerNorm row kernel widens its bf16 operands inside PTX
+// mixed-precision add/sub (.f32.bf16) instead of unpacking them first (a
+// build-time knob; the results are the same f32 operations).
+#ifndef NR_LN_MIXED
+#define NR_LN_MIXED 1
+#endif
+
+// The three per-vector steps of LayerNorm + modulation: add the values to a
+// running sum, add their squared deviations from mu, and modulate them.  For
+// bf16 with NR_LN_MIXED the bf16 operands enter PTX mixed-precision
+// instructions directly (same f32 results, fewer instructions).
+template <typename T, bool MIXED = (NR_LN_MIXED && sizeof(T) == 2)>
+struct RowMath {
+  static constexpr int N = Vec<T>::N;
+  __device__ __forceinline__ static float sum(const uint4& u, float acc) {
+    float v[N];
+    Vec<T>::unpack(u, v);
+#pragma unroll
+    for (int e = 0; e < N; e++) acc += v[e];
+    return acc;
+  }
+  __device__ __forceinline__ static float dev(const uint4& u, float mu, float acc) {
+    float v[N];
+    Vec<T>::unpack(u, v);
+#pragma unroll
+    for (int e = 0; e < N; e++) {
+      const float d = v[e] - mu;
+      acc = fmaf(d, d, acc);
+    }
+    return acc;
+  }
+  __device__ __forceinline__ static uint4 modulate(const uint4& u, float mu, float rstd,
+                                                   const uint4& shp, const uint4& scp) {
+    float v[N], sh[N], sc[N];
+    Vec<T>::unpack(u, v);
+    Vec<T>::unpack(shp, sh);
+    Vec<T>::unpack(scp, sc);
+#pragma unroll
+    for (int e = 0; e < N; e++) v[e] = fmaf((v[e] - mu) * rstd, 1.0f + sc[e], sh[e]);
+    return Vec<T>::pack(v);
+  }
+};
+
+template <typename T>
+struct RowMath<T, true> {
+  static constexpr int N = 8;
+  __device__ __forceinline__ static float sum(const uint4& u, float acc) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int q = 0; q < 4; q++) {
+      acc = add_bf16<false>(w[q], acc);
+      acc = add_bf16<true>(w[q], acc);
+    }
+    return acc;
+  }
+  __device__ __forceinline__ static float dev(const uint4& u, float mu, float acc) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int q = 0; q < 4; q++) {
+      const float d0 = sub_bf16<false>(w[q], mu);
+      acc = fmaf(d0, d0, acc);
+      const float d1 = sub_bf16<true>(w[q], mu);
+      acc = fmaf(d1, d1, acc);
+    }
+    return acc;
+  }
+  __device__ __forceinline__ static uint4 modulate(const uint4& u, float mu, float rstd,
+                                                   const uint4& shp, const uint4& scp) {
+    const uint32_t x[4] = {u.x, u.y, u.z, u.w};
+    const uint32_t h[4] = {shp.x, shp.y, shp.z, shp.w};
+    const uint32_t c[4] = {scp.x, scp.y, scp.z, scp.w};
+    float v[N];
+#pragma unroll
+    for (int q = 0; q < 4; q++) {
+      v[2 * q] = fmaf(sub_bf16<false>(x[q], mu) * rstd, add_bf16<false>(c[q], 1.0f),
+                      bf16_lo(h[q]));
+      v[2 * q + 1] = fmaf(sub_bf16<true>(x[q], mu) * rstd, add_bf16<true>(c[q], 1.0f),
+                          bf16_hi(h[q]));
+    }
+    return Vec<__nv_bfloat16>::pack(v);
+  }
+};
+
 // 1: cap the LayerNorm grid at the blocks resident at once, each looping over
 // its row groups (no block launches after the first wave); 0: one block per
 // row group (a build-time knob).
@@ -77,7 +160,6 @@ __global__ void __launch_bounds__(ln_row_threads<WPR>()) ln_modulate_rows_kernel
     const T* __restrict__ scale, int64_t rows, int nvec, int64_t rows_per_sample, float hidden_f,
     float eps) {
   pdl_enter();  // before any global read: the previous kernel may still run
-  constexpr int N = Vec<T>::N;
   constexpr int THREADS = ln_row_threads<WPR>();
   constexpr int TPR = kWarp * WPR;       // threads per row
   constexpr int RPB = THREADS / TPR;     // rows per block
@@ -109,12 +191,7 @@ __global__ void __launch_bounds__(ln_row_threads<WPR>()) ln_modulate_rows_kernel
 #pragma unroll
     for (int k = 0; k < VPT; k++) {
       const int vi = t + k * TPR;
-      if (active && vi < nvec) {
-        float v[N];
-        Vec<T>::unpack(xv[k], v);
-#pragma unroll
-        for (int e = 0; e < N; e++) sum += v[e];
-      }
+      if (active && vi < nvec) sum = RowMath<T>::sum(xv[k], sum);
     }
     const float mu = __fdiv_rn(row_group_sum<WPR>(sum, scratch_mean), hidden_f);
 
@@ -122,15 +199,7 @@ __global__ void __launch_bounds__(ln_row_threads<WPR>()) ln_modulate_rows_kernel
 #pragma unroll
     for (int k = 0; k < VPT; k++) {
       const int vi = t + k * TPR;
-      if (active && vi < nvec) {
-        float v[N];
-        Vec<T>::unpack(xv[k], v);
-#pragma unroll
-        for (int e = 0; e < N; e++) {
-          const float d = v[e] - mu;
-          dev = fmaf(d, d, dev);
-        }
-      }
+      if (active && vi < nvec) dev = RowMath<T>::dev(xv[k], mu, dev);
     }
     const float rstd =
         1.0f / sqrtf(__fdiv_rn(row_group_sum<WPR>(dev, scratch_var), hidden_f) + eps);
@@ -139,15 +208,9 @@ __global__ void __launch_bounds__(ln_row_threads<WPR>()) ln_modulate_rows_kernel
 #pragma unroll
     for (int k = 0; k < VPT; k++) {
       const int vi = t + k * TPR;
-      if (vi < nvec) {
-        float v[N], sh[N], sc[N];
-        Vec<T>::unpack(xv[k], v);
-        Vec<T>::unpack(ld_param(shv + vi), sh);
-        Vec<T>::unpack(ld_param(scv + vi), sc);
-#pragma unroll
-        for (int e = 0; e < N; e++) v[e] = fmaf((v[e] - mu) * rstd, 1.0f + sc[e], sh[e]);
-        st_stream(orow + vi, Vec<T>::pack(v));
-      }
+      if (vi < nvec)
+        st_stream(orow + vi,
+                  RowMath<T>::modulate(xv[k], mu, rstd, ld_param(shv + vi), ld_param(scv + vi)));
     }
   };
   if (NR_LN_PERSIST) {
@@ -190,18 +253,34 @@ struct GatedAdd<__nv_bfloat16> {
   // rounding that to nearest bf16 rounds the exact r + g*y once (Boldo and
   // Melquiond, "Emulation of FMA and correctly rounded sums: proved
   // algorithms using rounding to odd", IEEE Trans. Computers 57(4), 2008).
+  // With NR_LN_MIXED the two directed sums are mixed-precision fmas of the
+  // bf16 gate and y (an exact product) and the f32 residual.
   __device__ __forceinline__ static uint4 apply(const uint4& r, const uint4& g, const uint4& y) {
-    float rv[8], gv[8], yv[8];
-    Vec<__nv_bfloat16>::unpack(r, rv);
-    Vec<__nv_bfloat16>::unpack(g, gv);
-    Vec<__nv_bfloat16>::unpack(y, yv);
     float odd[8];
+    if constexpr (NR_LN_MIXED) {
+      const uint32_t rw[4] = {r.x, r.y, r.z, r.w};
+      const uint32_t gw[4] = {g.x, g.y, g.z, g.w};
+      const uint32_t yw[4] = {y.x, y.y, y.z, y.w};
 #pragma unroll
-    for (int e = 0; e < 8; e++) {
-      const float p = gv[e] * yv[e];
-      const float down = __fadd_rd(p, rv[e]);
-      const float up = __fadd_ru(p, rv[e]);
-      odd[e] = (down != up && (__float_as_uint(down) & 1u)) ? down : up;
+      for (int q = 0; q < 4; q++) {
+        float down, up;
+        fma_bf16_down_up<false>(gw[q], yw[q], bf16_lo(rw[q]), down, up);
+        odd[2 * q] = (down != up && (__float_as_uint(down) & 1u)) ? down : up;
+        fma_bf16_down_up<true>(gw[q], yw[q], bf16_hi(rw[q]), down, up);
+        odd[2 * q + 1] = (down != up && (__float_as_uint(down) & 1u)) ? down : up;
+      }
+    } else {
+      float rv[8], gv[8], yv[8];
+      Vec<__nv_bfloat16>::unpack(r, rv);
+      Vec<__nv_bfloat16>::unpack(g, gv);
+      Vec<__nv_bfloat16>::unpack(y, yv);
+#pragma unroll
+      for (int e = 0; e < 8; e++) {
+        const float p = gv[e] * yv[e];
+        const float down = __fadd_rd(p, rv[e]);
+        const float up = __fadd_ru(p, rv[e]);
+        odd[e] = (down != up && (__float_as_uint(down) & 1u)) ? down : up;
+      }
     }
     return Vec<__nv_bfloat16>::pack(odd);
   }
@@ -244,7 +323,6 @@ __global__ void __launch_bounds__(gated_threads<WPR>(), gated_min_blocks<T, VPT,
     const T* __restrict__ gate, const T* __restrict__ shift, const T* __restrict__ scale,
     int64_t rows, int nvec, int64_t rows_per_sample, float hidden_f, float eps) {
   pdl_enter();  // before any global read: the previous kernel may still run
-  constexpr int N = Vec<T>::N;
   constexpr int THREADS = gated_threads<WPR>();
   constexpr int TPR = kWarp * WPR;
   constexpr int RPB = THREADS / TPR;
@@ -279,10 +357,7 @@ __global__ void __launch_bounds__(gated_threads<WPR>(), gated_min_blocks<T, VPT,
     if (active && vi < nvec) {
       xv[k] = GatedAdd<T>::apply(xv[k], ld_param(gv + vi), yv[k]);
       st_stream(rr + vi, xv[k]);
-      float v[N];
-      Vec<T>::unpack(xv[k], v);
-#pragma unroll
-      for (int e = 0; e < N; e++) sum += v[e];
+      sum = RowMath<T>::sum(xv[k], sum);
     }
   }
   const float mu = __fdiv_rn(row_group_sum<WPR>(sum, scratch_mean), hidden_f);
@@ -290,30 +365,16 @@ __global__ void __launch_bounds__(gated_threads<WPR>(), gated_min_blocks<T, VPT,
 #pragma unroll
   for (int k = 0; k < VPT; k++) {
     const int vi = t + k * TPR;
-    if (active && vi < nvec) {
-      float v[N];
-      Vec<T>::unpack(xv[k], v);
-#pragma unroll
-      for (int e = 0; e < N; e++) {
-        const float d = v[e] - mu;
-        dev = fmaf(d, d, dev);
-      }
-    }
+    if (active && vi < nvec) dev = RowMath<T>::dev(xv[k], mu, dev);
   }
   const float rstd = 1.0f / sqrtf(__fdiv_rn(row_group_sum<WPR>(dev, scratch_var), hidden_f) + eps);
   if (!active) return;
 #pragma unroll
   for (int k = 0; k < VPT; k++) {
     const int vi = t + k * TPR;
-    if (vi < nvec) {
-      float v[N], sh[N], sc[N];
-      Vec<T>::unpack(xv[k], v);
-      Vec<T>::unpack(ld_param(shv + vi), sh);
-      Vec<T>::unpack(ld_param(scv + vi), sc);
-#pragma unroll
-      for (int e = 0; e < N; e++) v[e] = fmaf((v[e] - mu) * rstd, 1.0f + sc[e], sh[e]);
-      st_stream(orow + vi, Vec<T>::pack(v));
-    }
+    if (vi < nvec)
+      st_stream(orow + vi,
+                RowMath<T>::modulate(xv[k], mu, rstd, ld_param(shv + vi), ld_param(scv + vi)));
   }
 }
 

@@ -274,6 +274,49 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&h);
 }
 
+// Mixed-precision f32 arithmetic on one bf16 half of a packed pair (PTX
+// add/sub/fma with .f32.bf16 types): the bf16 operand is widened exactly, so
+// each result equals the same f32 operation on the unpacked value.
+// HI selects the high half (element 2k + 1).
+template <bool HI>
+__device__ __forceinline__ float add_bf16(uint32_t u, float c) {  // bf16 + c
+  float d;
+  if (HI)
+    asm("{\n .reg .b16 lo, hi;\n mov.b32 {lo, hi}, %1;\n add.rn.f32.bf16 %0, hi, %2;\n}"
+        : "=f"(d) : "r"(u), "f"(c));
+  else
+    asm("{\n .reg .b16 lo, hi;\n mov.b32 {lo, hi}, %1;\n add.rn.f32.bf16 %0, lo, %2;\n}"
+        : "=f"(d) : "r"(u), "f"(c));
+  return d;
+}
+template <bool HI>
+__device__ __forceinline__ float sub_bf16(uint32_t u, float c) {  // bf16 - c
+  float d;
+  if (HI)
+    asm("{\n .reg .b16 lo, hi;\n mov.b32 {lo, hi}, %1;\n sub.rn.f32.bf16 %0, hi, %2;\n}"
+        : "=f"(d) : "r"(u), "f"(c));
+  else
+    asm("{\n .reg .b16 lo, hi;\n mov.b32 {lo, hi}, %1;\n sub.rn.f32.bf16 %0, lo, %2;\n}"
+        : "=f"(d) : "r"(u), "f"(c));
+  return d;
+}
+
+// a*b + c for the same half of two packed pairs, rounded down (RM) and up
+// (RP): the product of two bf16 values is exact, so each is the exact
+// a*b + c rounded once in that direction.
+template <bool HI>
+__device__ __forceinline__ void fma_bf16_down_up(uint32_t a, uint32_t b, float c, float& down,
+                                                 float& up) {
+  if (HI)
+    asm("{\n .reg .b16 alo, ahi, blo, bhi;\n mov.b32 {alo, ahi}, %2;\n mov.b32 {blo, bhi}, %3;\n"
+        " fma.rm.f32.bf16 %0, ahi, bhi, %4;\n fma.rp.f32.bf16 %1, ahi, bhi, %4;\n}"
+        : "=f"(down), "=f"(up) : "r"(a), "r"(b), "f"(c));
+  else
+    asm("{\n .reg .b16 alo, ahi, blo, bhi;\n mov.b32 {alo, ahi}, %2;\n mov.b32 {blo, bhi}, %3;\n"
+        " fma.rm.f32.bf16 %0, alo, blo, %4;\n fma.rp.f32.bf16 %1, alo, blo, %4;\n}"
+        : "=f"(down), "=f"(up) : "r"(a), "r"(b), "f"(c));
+}
+
 template <>
 struct Vec<__nv_bfloat16> {
   static constexpr int N = 8;

@@ -363,7 +363,12 @@ __global__ void __launch_bounds__(kQkThreads) qk_norm_rope_kernel(const QkArgs a
 // head_dim 128 bf16) instead of reading them from shared memory for every
 // head row; a build-time knob.
 #ifndef NR_QKB_WREG
-#define NR_QKB_WREG 0
+#define NR_QKB_WREG 1
+#endif
+// Upper bound on the bulk kernels' resident blocks per SM used to size the
+// grid (a build-time knob; 0: as many as fit).
+#ifndef NR_QKB_MAXB
+#define NR_QKB_MAXB 0
 #endif
 
 // Minimum resident blocks per SM asked of the compiler for the full-head bulk
@@ -653,7 +658,17 @@ template <typename T, typename WT, int L, int NST>
 #ifndef NR_QKV_MINB
 #define NR_QKV_MINB 7
 #endif
-__global__ void __launch_bounds__(kBulkThreads, NR_QKV_MINB) qk_norm_rope_bulk_var_kernel(const QkArgs a,
+#if NR_QKV_MINB > 0
+#define NR_QKV_BOUNDS __launch_bounds__(kBulkThreads, NR_QKV_MINB)
+#else
+#define NR_QKV_BOUNDS __launch_bounds__(kBulkThreads)
+#endif
+// 1: the variant kernel keeps each lane's weights in registers (a build-time
+// knob, as NR_QKB_WREG for the full-head kernel).
+#ifndef NR_QKV_WREG
+#define NR_QKV_WREG 0
+#endif
+__global__ void NR_QKV_BOUNDS qk_norm_rope_bulk_var_kernel(const QkArgs a,
                                                                        const RopeTurns turns,
                                                                        const BulkGeom geo) {
   using S = BulkSmem<T, L>;
@@ -774,6 +789,16 @@ __global__ void __launch_bounds__(kBulkThreads, NR_QKV_MINB) qk_norm_rope_bulk_v
       rotates = false;
     }
   }
+#if NR_QKV_WREG
+  float wqa[N], wqb[N], wka[N], wkb[N];
+#pragma unroll
+  for (int e = 0; e < N; e++) {
+    wqa[e] = wsm[va_vec * N + e];
+    wqb[e] = wsm[vb_vec * N + e];
+    wka[e] = wsm[D + va_vec * N + e];
+    wkb[e] = wsm[D + vb_vec * N + e];
+  }
+#endif
   int64_t j = 0;
   for (; j < ntok; j++) {
     const int64_t tok = t0 + j * C;
@@ -822,8 +847,17 @@ __global__ void __launch_bounds__(kBulkThreads, NR_QKV_MINB) qk_norm_rope_bulk_v
       if (!valid) continue;
       const float inv = rsqrtf(ss * a.inv_d + a.eps);
       const float* w = wsm + (is_q ? 0 : D);
+#if NR_QKV_WREG
+      float wa[N], wb[N];
+#pragma unroll
+      for (int e = 0; e < N; e++) {
+        wa[e] = is_q ? wqa[e] : wka[e];
+        wb[e] = is_q ? wqb[e] : wkb[e];
+      }
+#else
       const float* wa = w + va_vec * N;
       const float* wb = w + vb_vec * N;
+#endif
       float oa[N], ob[N];
       if (!a.interleaved && rotates) {
 #pragma unroll
@@ -980,6 +1014,7 @@ cudaError_t launch_bulk(const QkArgs& a, const RopeTurns& turns, const BulkGeom&
     std::lock_guard<std::mutex> lock(mu);
     occupancy[{device, smem}] = per_sm;
   }
+  if (NR_QKB_MAXB > 0 && per_sm > NR_QKB_MAXB) per_sm = NR_QKB_MAXB;
   const int64_t resident = static_cast<int64_t>(sm_count(device)) * per_sm;
   const int64_t blocks = a.tokens < resident ? a.tokens : resident;
   return launch_pdl(kernel, dim3(static_cast<unsigned>(blocks)), dim3(kBulkThreads), smem, s, a,

@@ -59,6 +59,30 @@ __device__ __forceinline__ void store_normed(const StoreFp8& e, int64_t vec_inde
   }
 }
 
+// The residual add and the sum of squares of one 128-bit vector.
+template <typename T>
+struct RmsMath {
+  static constexpr int N = Vec<T>::N;
+  // round_T(x + r) elementwise: for bf16 the f32 sum is exact when the
+  // exponents differ by at most 15 and otherwise far from a bf16 midpoint, so
+  // one rounding of it equals rounding the exact sum.
+  __device__ __forceinline__ static uint4 add(const uint4& x, const uint4& r) {
+    float v[N], rv[N];
+    Vec<T>::unpack(x, v);
+    Vec<T>::unpack(r, rv);
+#pragma unroll
+    for (int e = 0; e < N; e++) v[e] += rv[e];
+    return Vec<T>::pack(v);
+  }
+  __device__ __forceinline__ static float sumsq(const uint4& u, float acc) {
+    float v[N];
+    Vec<T>::unpack(u, v);
+#pragma unroll
+    for (int e = 0; e < N; e++) acc = fmaf(v[e], v[e], acc);
+    return acc;
+  }
+};
+
 // One block per row; thread t owns vectors t, t + blockDim, ..., (VPT of them).
 // PW: load the weight together with the row (saves a dependent round trip when
 // there are few rows, e.g. decode; costs registers when there are many).
@@ -99,22 +123,13 @@ __global__ void __launch_bounds__((PW && VPT <= 2) ? kDecodeMaxThreads : kRowMax
   for (int k = 0; k < VPT; k++) {
     const int vi = threadIdx.x + k * blockDim.x;
     if (vi < nvec) {
-      float v[N];
-      Vec<T>::unpack(xv[k], v);
       if (RES) {
-        float r[N];
-        Vec<T>::unpack(rv[k], r);
-#pragma unroll
-        for (int e = 0; e < N; e++) v[e] += r[e];
-        // Round to the residual's storage dtype; the rounded value is both
-        // written back and squared.  (For bf16, f32 add then one rounding
-        // equals rounding the exact sum: f32 holds >= 2*8+2 bits.)
-        xv[k] = Vec<T>::pack(v);
+        // Rounded to the residual's storage dtype: the rounded value is both
+        // written back and squared.
+        xv[k] = RmsMath<T>::add(xv[k], rv[k]);
         st_stream(rr + vi, xv[k]);
-        Vec<T>::unpack(xv[k], v);
       }
-#pragma unroll
-      for (int e = 0; e < N; e++) sum_sq = fmaf(v[e], v[e], sum_sq);
+      sum_sq = RmsMath<T>::sumsq(xv[k], sum_sq);
     }
   }
 
@@ -219,6 +234,10 @@ cudaError_t launch_rows(const RowLaunch& g, const EPI& epi, const void* x, const
 #define NR_RMS_DECODE_GEOM 1
 #endif
 constexpr int64_t kDecodeGeomRows = 256;
+// Vectors per thread of the few-row geometry (a build-time knob: 1 or 2).
+#ifndef NR_RMS_DECODE_VPT
+#define NR_RMS_DECODE_VPT 2
+#endif
 
 // Launch the row kernel for the geometry picked for this row length; false
 // when the row is too long for it (the caller then needs the multi-pass kernel).
@@ -226,11 +245,12 @@ template <typename T, typename EPI>
 bool launch_row_kernel(cudaError_t& err, const EPI& epi, const void* x, const void* w, void* res,
                        int64_t rows, int64_t nvec, float hidden_f, float eps, float w_add,
                        cudaStream_t s) {
+  constexpr int DV = NR_RMS_DECODE_VPT;
   if (NR_RMS_DECODE_GEOM && rows <= kDecodeGeomRows && nvec > kRowMaxThreads &&
-      nvec <= 2 * kDecodeMaxThreads) {
+      nvec <= DV * kDecodeMaxThreads) {
     const int nv = static_cast<int>(nvec);
-    const RowLaunch g{2, static_cast<int>(((nvec + 1) / 2 + 31) / 32 * 32)};
-    err = launch_rows_pw<T, 2, true>(g, epi, x, w, res, rows, nv, hidden_f, eps, w_add, s);
+    const RowLaunch g{DV, static_cast<int>(((nvec + DV - 1) / DV + 31) / 32 * 32)};
+    err = launch_rows_pw<T, DV, true>(g, epi, x, w, res, rows, nv, hidden_f, eps, w_add, s);
     return true;
   }
   const RowLaunch g = pick_row_launch(nvec);

@@ -131,3 +131,32 @@ def test_zero_residual_equals_plain(nr):
     b = nr.rmsnorm(dev(x), dev(w))
     assert torch.equal(a, b)
     assert torch.equal(zero.cpu(), x)
+
+
+def test_residual_add_edge_values_bit_exact(nr):
+    """The stored residual is round_bf16(x + residual) bit for bit over the
+    whole bf16 range: exponent gaps from 0 to beyond 2^-24, subnormal
+    operands and sums, exact cancellations (x = -residual, +-0 mixes), and
+    ties between bf16 neighbours."""
+    rng = np.random.default_rng(71)
+    rows, hidden = 64, 1024
+    n = rows * hidden
+    mant = rng.uniform(1, 2, (2, n))
+    ex = rng.integers(-140, 30, (2, n))  # down into the bf16 subnormal range
+    sign = np.where(rng.random((2, n)) < 0.5, -1.0, 1.0)
+    vals = sign * mant * np.exp2(ex.astype(np.float64))
+    x = torch.from_numpy(vals[0]).to(torch.bfloat16)
+    r = torch.from_numpy(vals[1]).to(torch.bfloat16)
+    q = n // 8
+    r[:q] = -x[:q]                       # exact cancellations
+    x[q:2 * q] = 0.0                     # +0 + r
+    r[2 * q:3 * q] = -0.0                # x + -0
+    x[3 * q:3 * q + 64] = -0.0           # -0 + -0
+    r[3 * q:3 * q + 64] = -0.0
+    # ties: r is half an ulp of x (bf16 keeps 8 bits, so 2^-8 of x's binade)
+    xt = x[4 * q:5 * q].float()
+    r[4 * q:5 * q] = (torch.sign(xt) * torch.exp2(torch.floor(torch.log2(xt.abs().clamp_min(2.0 ** -120))) - 8)).to(torch.bfloat16)
+    x = x.view(rows, hidden)
+    r = r.view(rows, hidden)
+    w = torch.ones(hidden, dtype=torch.bfloat16)
+    run_case(nr, rows, hidden, torch.bfloat16, residual=True, x=x, res=r, w=w)

@@ -651,12 +651,13 @@ __global__ void NR_QKB_BOUNDS qk_norm_rope_bulk_kernel(const QkArgs a,
 // kernel, measured faster for it.)
 template <typename T, typename WT, int L, int NST>
 // Minimum resident blocks per SM asked of the compiler for the variant kernel
-// (a build-time knob): 7 caps it at 72 registers, as the full-head kernel
-// uses, without spills; measured 105.1 µs instead of 112.4 µs (79 registers)
-// for GPT-J pairs with a 64-dim rotary part at [26598, 24 + 24, 128], back to
-// back.
+// (a build-time knob; 0: none asked).  With the weights in shared memory a
+// cap of 7 (72 registers) ran GPT-J pairs with a 64-dim rotary part at
+// [26598, 24 + 24, 128] in 105.1 µs instead of 112.4 µs (79 registers); with
+// the weights in registers (NR_QKV_WREG) no cap (120 registers) runs it in
+// 102.2 µs against 104.4 µs for the capped shared-memory build.
 #ifndef NR_QKV_MINB
-#define NR_QKV_MINB 7
+#define NR_QKV_MINB 0
 #endif
 #if NR_QKV_MINB > 0
 #define NR_QKV_BOUNDS __launch_bounds__(kBulkThreads, NR_QKV_MINB)
@@ -666,7 +667,7 @@ template <typename T, typename WT, int L, int NST>
 // 1: the variant kernel keeps each lane's weights in registers (a build-time
 // knob, as NR_QKB_WREG for the full-head kernel).
 #ifndef NR_QKV_WREG
-#define NR_QKV_WREG 0
+#define NR_QKV_WREG 1
 #endif
 __global__ void NR_QKV_BOUNDS qk_norm_rope_bulk_var_kernel(const QkArgs a,
                                                                        const RopeTurns turns,

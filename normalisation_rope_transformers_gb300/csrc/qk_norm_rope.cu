@@ -847,7 +847,6 @@ __global__ void NR_QKV_BOUNDS qk_norm_rope_bulk_var_kernel(const QkArgs a,
       ss = group_sum<L>(ss);
       if (!valid) continue;
       const float inv = rsqrtf(ss * a.inv_d + a.eps);
-      const float* w = wsm + (is_q ? 0 : D);
 #if NR_QKV_WREG
       float wa[N], wb[N];
 #pragma unroll
@@ -856,6 +855,7 @@ __global__ void NR_QKV_BOUNDS qk_norm_rope_bulk_var_kernel(const QkArgs a,
         wb[e] = is_q ? wqb[e] : wkb[e];
       }
 #else
+      const float* w = wsm + (is_q ? 0 : D);
       const float* wa = w + va_vec * N;
       const float* wb = w + vb_vec * N;
 #endif

@@ -246,8 +246,13 @@ bool launch_row_kernel(cudaError_t& err, const EPI& epi, const void* x, const vo
                        int64_t rows, int64_t nvec, float hidden_f, float eps, float w_add,
                        cudaStream_t s) {
   constexpr int DV = NR_RMS_DECODE_VPT;
+  // Measured exception: 17-64 rows of at least 1024 vectors keep the
+  // many-row geometry ([32, 8192] bf16: 2.22 / 2.65 µs hot / cold against
+  // 2.60 / 2.88 µs with 2 vectors per thread; at 8 and at 128 rows the few-row
+  // geometry is as fast or faster).
+  const bool few_row_loses = rows > 16 && rows <= 64 && nvec >= 1024;
   if (NR_RMS_DECODE_GEOM && rows <= kDecodeGeomRows && nvec > kRowMaxThreads &&
-      nvec <= DV * kDecodeMaxThreads) {
+      nvec <= DV * kDecodeMaxThreads && !few_row_loses) {
     const int nv = static_cast<int>(nvec);
     const RowLaunch g{DV, static_cast<int>(((nvec + DV - 1) / DV + 31) / 32 * 32)};
     err = launch_rows_pw<T, DV, true>(g, epi, x, w, res, rows, nv, hidden_f, eps, w_add, s);

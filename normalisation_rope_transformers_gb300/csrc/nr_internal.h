@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <utility>
 
 namespace nr {
@@ -31,6 +32,28 @@ cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t 
   cfg.attrs = attr;
   cfg.numAttrs = NR_PDL ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+// Blocks of `kernel` (with `threads` threads, no dynamic shared memory)
+// resident at once over the current device's SMs, cached per device in
+// `cache` (64 entries; a racing thread at worst repeats the queries).
+template <typename Kernel>
+cudaError_t resident_blocks(Kernel kernel, int threads, std::atomic<int>* cache, int* blocks) {
+  int device = 0;
+  cudaError_t e = cudaGetDevice(&device);
+  if (e != cudaSuccess) return e;
+  if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
+  int n = cache[device].load(std::memory_order_relaxed);
+  if (n == 0) {
+    int sms = 0, per_sm = 0;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
+    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, 0);
+    if (e != cudaSuccess) return e;
+    n = sms * (per_sm > 0 ? per_sm : 1);
+    cache[device].store(n, std::memory_order_relaxed);
+  }
+  *blocks = n;
+  return cudaSuccess;
 }
 
 // Geometry of the row-resident kernels: one block per row, `threads` threads,

@@ -135,3 +135,28 @@ def test_zero_rows_is_a_no_op(nr):
     z = torch.empty(0, 64, dtype=torch.bfloat16, device="cuda")
     p = torch.zeros(1, 64, dtype=torch.bfloat16, device="cuda")
     assert nr.gated_residual_ln_modulate(z, z.clone(), p, p, p).shape == (0, 64)
+
+
+def test_bf16_subnormal_operands_and_products(nr):
+    """Gate and y down in the bf16 subnormal range and products that land
+    there (r = 0 then keeps a tiny nonzero residual, which flushing subnormals
+    to zero anywhere on the way would lose); bit-exact residual."""
+    hidden = 256
+    rng = np.random.default_rng(12)
+    ex = rng.integers(-135, -60, (3, hidden)).astype(np.float64)
+    sign = np.where(rng.random((3, hidden)) < 0.5, -1.0, 1.0)
+    vals = sign * rng.uniform(1, 2, (3, hidden)) * np.exp2(ex)
+    g = torch.from_numpy(vals[0][None]).to(torch.bfloat16)
+    y = torch.from_numpy(vals[1][None]).to(torch.bfloat16)
+    r = torch.from_numpy(vals[2][None]).to(torch.bfloat16)
+    r[0, : hidden // 2] = 0.0                                 # residual 0: the product alone
+    g[0, : hidden // 4] = torch.tensor(2.0 ** -70)            # products near 2^-130..2^-125
+    y[0, : hidden // 4] = (torch.from_numpy(rng.uniform(1, 2, hidden // 4) * 2.0 ** -60)
+                           .to(torch.bfloat16))
+    zero = torch.zeros(1, hidden, dtype=torch.bfloat16)
+    _, o_res, _, _ = oracle.gated_ln_modulate(host_bits(r), host_bits(y), host_bits(g),
+                                              host_bits(zero), host_bits(zero))
+    tiny = (o_res[0] & 0x7F80) == 0                           # bf16 subnormal or zero
+    assert ((o_res[0] & 0x7FFF) != 0)[: hidden // 4].sum() >= hidden // 8  # nonzero tiny results
+    assert tiny.sum() >= hidden // 8
+    run_case(nr, r, y, g, zero, zero)

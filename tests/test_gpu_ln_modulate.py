@@ -128,3 +128,14 @@ def test_many_constant_rows_give_shift(nr):
     x = torch.full((MANY_ROWS, hidden), 0.7, dtype=torch.bfloat16)
     out = nr.ln_modulate(dev(x), dev(shift), dev(scale)).cpu()
     assert torch.equal(out, shift.expand(MANY_ROWS, hidden))
+
+
+def test_bf16_subnormal_inputs(nr):
+    """Rows mixing bf16 subnormals with normal values, and rows of subnormals
+    only (whose variance underflows to 0 in f32, leaving the shift)."""
+    hidden = 1024
+    rng = np.random.default_rng(45)
+    x = rng.standard_normal((4, hidden))
+    x[:, ::3] = np.sign(x[:, ::3]) * rng.uniform(1, 2, (4, (hidden + 2) // 3)) * 2.0 ** -130
+    x[2:] = np.sign(x[2:]) * rng.uniform(1, 2, (2, hidden)) * 2.0 ** -128
+    run_case(nr, 4, hidden, seed=46, x=torch.from_numpy(x).to(torch.bfloat16))

@@ -57,7 +57,8 @@ KERNEL_SOURCES = {
 def parse_args():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=3000)
+    p.add_argument("--steps", "--iters", dest="steps", type=int, default=3000,
+                   help="timed steps (--iters is the same flag)")
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--e2e-steps", type=int, default=10)

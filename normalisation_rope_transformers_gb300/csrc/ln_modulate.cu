@@ -147,16 +147,13 @@ struct RowMath<T, true> {
   }
 };
 
-// Rows ahead of its own whose input a row group asks L2 to prefetch, as a
-// multiple of the row groups resident at once (build-time knobs; 0: none), for
-// LayerNorm + modulation and for the gated kernel.  A block launched later for
-// that row then finds it in L2, so HBM keeps a resident set's worth of rows
-// more in flight than registers alone allow.  Measured at [26598, 3072]: the
-// gated kernel 98.5 -> 97.1 µs with one set ahead (two: 114.5 µs); LayerNorm
-// 53.7 -> 54.7 µs, so it prefetches nothing.
-#ifndef NR_LN_L2PF
-#define NR_LN_L2PF 0
-#endif
+// Rows ahead of its own whose inputs a gated row group asks L2 to prefetch,
+// as a multiple of the row groups resident at once (a build-time knob; 0:
+// none).  A block launched later for that row then finds it in L2, so HBM
+// keeps a resident set's worth of rows more in flight than registers alone
+// allow.  Measured at [26598, 3072]: 98.5 -> 97.1 µs with one set ahead (two:
+// 114.5 µs); the same prefetch slowed LayerNorm + modulation (53.7 -> 54.7 µs),
+// which has none.
 #ifndef NR_GATED_L2PF
 #define NR_GATED_L2PF 1
 #endif
@@ -165,7 +162,7 @@ template <typename T, int VPT, int WPR>
 __global__ void __launch_bounds__(ln_row_threads<WPR>()) ln_modulate_rows_kernel(
     T* __restrict__ out, const T* __restrict__ x, const T* __restrict__ shift,
     const T* __restrict__ scale, int64_t rows, int nvec, int64_t rows_per_sample, float hidden_f,
-    float eps, int64_t prefetch_rows) {
+    float eps) {
   pdl_enter();  // before any global read: the previous kernel may still run
   constexpr int THREADS = ln_row_threads<WPR>();
   constexpr int TPR = kWarp * WPR;       // threads per row
@@ -191,8 +188,6 @@ __global__ void __launch_bounds__(ln_row_threads<WPR>()) ln_modulate_rows_kernel
       const int vi = t + k * TPR;
       if (active && vi < nvec) xv[k] = ld_stream(xr + vi);
     }
-    if (prefetch_rows > 0 && t == 0 && row + prefetch_rows < rows)
-      bulk_prefetch_l2(xr + prefetch_rows * nvec, static_cast<unsigned>(nvec) * 16u);
 
     float sum = 0.0f;
 #pragma unroll
@@ -448,19 +443,10 @@ cudaError_t launch_rows(const LnArgs& a, cudaStream_t s) {
   constexpr int RPB = THREADS / (kWarp * WPR);
   static_assert(RPB >= 1, "row groups must fit the block");
   const int64_t blocks = (a.rows + RPB - 1) / RPB;
-  int64_t prefetch_rows = 0;
-  if (NR_LN_L2PF > 0) {
-    static std::atomic<int> cache[64];
-    int resident = 0;
-    const cudaError_t e =
-        resident_blocks(ln_modulate_rows_kernel<T, VPT, WPR>, THREADS, cache, &resident);
-    if (e != cudaSuccess) return e;
-    prefetch_rows = static_cast<int64_t>(NR_LN_L2PF) * resident * RPB;
-  }
   return launch_pdl(ln_modulate_rows_kernel<T, VPT, WPR>, dim3(static_cast<unsigned>(blocks)),
                     dim3(THREADS), 0, s,
       static_cast<T*>(a.out), static_cast<const T*>(a.x), static_cast<const T*>(a.shift),
-      static_cast<const T*>(a.scale), a.rows, a.nvec, a.rps, a.hidden_f, a.eps, prefetch_rows);
+      static_cast<const T*>(a.scale), a.rows, a.nvec, a.rps, a.hidden_f, a.eps);
 }
 
 // Vectors per thread offered for one-warp rows, and for rows spread over

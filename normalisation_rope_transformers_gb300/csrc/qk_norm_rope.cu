@@ -345,11 +345,6 @@ __global__ void __launch_bounds__(kQkThreads) qk_norm_rope_kernel(const QkArgs a
 #ifndef NR_QK_PATH
 #define NR_QK_PATH 1
 #endif
-// Tokens ahead of the stages that the producer also asks L2 to prefetch (0:
-// none); a build-time knob.
-#ifndef NR_QKB_L2PF
-#define NR_QKB_L2PF 0
-#endif
 // L2 evict-first policy on the bulk loads (bit 0) and stores (bit 1); a
 // build-time knob.  Both (3): the token blocks are touched once, and written
 // lines leave L2 during this kernel instead of being written back while the
@@ -381,15 +376,6 @@ __global__ void __launch_bounds__(kQkThreads) qk_norm_rope_kernel(const QkArgs a
 #define NR_QKB_BOUNDS __launch_bounds__(kBulkThreads, NR_QKB_MINB)
 #else
 #define NR_QKB_BOUNDS __launch_bounds__(kBulkThreads)
-#endif
-
-// Where the full-head bulk kernel writes its results (a build-time knob):
-// 0: back into the stage, then two bulk stores per token, the stage refilled
-// once the stores have read it; 1: straight from registers to global memory
-// (streaming stores), so a stage is refilled as soon as the block has read
-// it and NST tokens stay in flight instead of NST - 1.
-#ifndef NR_QKB_STORE
-#define NR_QKB_STORE 0
 #endif
 
 // Warps per block (they split each token's head rows); a build-time knob.
@@ -484,17 +470,12 @@ __global__ void NR_QKB_BOUNDS qk_norm_rope_bulk_kernel(const QkArgs a,
                                  geo.k_bytes, bar);
     }
     issued = j + 1;
-    if (NR_QKB_L2PF > 0 && j + NR_QKB_L2PF < ntok) {
-      const int64_t ptok = t0 + (j + NR_QKB_L2PF) * C;
-      bulk_prefetch_l2(q + ptok * a.q_stride, geo.q_bytes);
-      if (geo.k_bytes) bulk_prefetch_l2(k + ptok * a.k_stride, geo.k_bytes);
-    }
   };
   pdl_enter();  // before any global read: the previous kernel may still run
   // The first tokens' loads go out before the weights are read, so their
   // latency overlaps the rest of the set-up.
   if (tid == 0)
-    for (int64_t j = 0; j < (NR_QKB_STORE ? NST : NST - 1) && j < ntok; j++) issue(j);
+    for (int64_t j = 0; j < NST - 1 && j < ntok; j++) issue(j);
   for (int i = tid; i < 2 * D; i += kBulkThreads) {
     float wv = 0.0f;
     if (i < D)
@@ -591,30 +572,17 @@ __global__ void NR_QKB_BOUNDS qk_norm_rope_bulk_kernel(const QkArgs a,
         oa[e] = fmaf(na, cs[e].x, -nb * cs[e].y);
         ob[e] = fmaf(na, cs[e].y, nb * cs[e].x);
       }
-      if (NR_QKB_STORE) {
-        uint4* o = reinterpret_cast<uint4*>(
-            is_q ? q_out + tok * a.q_stride + static_cast<int64_t>(row) * D
-                 : k_out + tok * a.k_stride + static_cast<int64_t>(row - a.hq) * D);
-        st_stream(o + l, Vec<T>::pack(oa));
-        st_stream(o + l + L, Vec<T>::pack(ob));
-      } else {
-        r[l] = Vec<T>::pack(oa);
-        r[l + L] = Vec<T>::pack(ob);
-      }
+      r[l] = Vec<T>::pack(oa);
+      r[l + L] = Vec<T>::pack(ob);
     }
     // the next token's angles, into the other table buffer
     if (tid < HALF && j + 1 < ntok) {
       angles(static_cast<int>((j + 1) & 1), pos_next);
       if (j + 2 < ntok) pos_next = a.pos[t0 + (j + 2) * C];
     }
-    if (!NR_QKB_STORE) fence_proxy_async_smem();
+    fence_proxy_async_smem();
     __syncthreads();
     if (*abort_flag) break;
-    if (NR_QKB_STORE) {
-      // every thread has read the stage: refill it with the token NST ahead
-      if (tid == 0 && j + NST < ntok) issue(j + NST);
-      continue;
-    }
     if (tid == 0) {
       if (NR_QKB_HINT & 2) {
         bulk_store_hint(q_out + tok * a.q_stride, smem_addr(st), geo.q_bytes, policy);
@@ -731,11 +699,6 @@ __global__ void NR_QKV_BOUNDS qk_norm_rope_bulk_var_kernel(const QkArgs a,
                                  geo.k_bytes, bar);
     }
     issued = j + 1;
-    if (NR_QKB_L2PF > 0 && j + NR_QKB_L2PF < ntok) {
-      const int64_t ptok = t0 + (j + NR_QKB_L2PF) * C;
-      bulk_prefetch_l2(q + ptok * a.q_stride, geo.q_bytes);
-      if (geo.k_bytes) bulk_prefetch_l2(k + ptok * a.k_stride, geo.k_bytes);
-    }
   };
   pdl_enter();  // before any global read: the previous kernel may still run
   // The first tokens' loads go out before the weights are read, so their

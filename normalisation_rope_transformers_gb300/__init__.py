@@ -247,7 +247,8 @@ def _check_qk(q, k, wq, wk, q_out, k_out):
     if not isinstance(wq, torch.Tensor) or wq.dtype not in (torch.float32, torch.bfloat16):
         raise TypeError("wq must be a float32 or bfloat16 tensor")
     _expect(wq, "wq", wq.dtype, (q.shape[2],))
-    _expect(wk, "wk", wq.dtype, (q.shape[2],))
+    if wk is not None or k.shape[1] > 0:  # wk may be None when k has no heads
+        _expect(wk, "wk", wq.dtype, (q.shape[2],))
     for o, i, name in ((q_out, q, "q_out"), (k_out, k, "k_out")):
         if o is None:
             continue

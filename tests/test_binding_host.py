@@ -102,6 +102,8 @@ MISMATCHED = {
                                                      torch.zeros(8, dtype=torch.int32)[::2]),
     "qk short wq": lambda b: b.qk_norm_rope(_bf(4, 2, 64), _bf(4, 1, 64), torch.ones(32),
                                             torch.ones(64), torch.zeros(4, dtype=torch.int32)),
+    "qk wk None with K heads": lambda b: b.qk_norm_rope(_bf(4, 2, 64), _bf(4, 1, 64), torch.ones(64),
+                                                         None, torch.zeros(4, dtype=torch.int32)),
     "qk wq wk dtypes": lambda b: b.qk_norm_rope(_bf(4, 2, 64), _bf(4, 1, 64), torch.ones(64),
                                                 _bf(64), torch.zeros(4, dtype=torch.int32)),
     "qk q k dtypes": lambda b: b.qk_norm_rope(_bf(4, 2, 64), torch.zeros(4, 1, 64), torch.ones(64),
@@ -169,6 +171,8 @@ def test_well_formed_operands_reach_the_device_check(binding):
         lambda: binding.gated_residual_ln_modulate(_bf(6, 64), _bf(6, 64), _bf(6, 64), _bf(6, 64),
                                                    _bf(6, 64), rows_per_sample=1),
         lambda: binding.silu_and_mul(_bf(4, 128), out=_bf(4, 64)),
+        # no K heads: wk may be None
+        lambda: binding.qk_norm_rope(_bf(4, 2, 64), _bf(4, 0, 64), torch.ones(64), None, p4),
     ]
     for call in calls:
         with pytest.raises(ValueError, match="CUDA"):

@@ -172,3 +172,14 @@ def test_zero_tokens_is_a_no_op(nr):
     p = torch.empty(0, dtype=torch.int32, device="cuda")
     qo, ko = nr.qk_norm_rope(q, q.clone(), w, w, p)
     assert qo.shape == (0, 2, 128)
+
+
+def test_no_k_heads_without_wk(nr):
+    """With no K heads the K weight may be None (a NULL pointer through the
+    C ABI): Q is the same as with a K weight given."""
+    q, k, wq, wk, p = synth.qk_inputs(17, 3, 0, 128, 5, torch.bfloat16, torch.float32)
+    qo, ko = nr.qk_norm_rope(dev(q), dev(k), dev(wq), None, dev(p))
+    qo2, _ = nr.qk_norm_rope(dev(q), dev(k), dev(wq), dev(wk), dev(p))
+    torch.cuda.synchronize()
+    assert ko.shape == (17, 0, 128)
+    assert torch.equal(qo.cpu(), qo2.cpu())

@@ -14,8 +14,10 @@
 // own block).  The row is loaded once into registers, the mean and the centred
 // variance are two reductions over the register-resident values (warp
 // shuffles, plus one shared-memory step when WPR > 1), and the output is
-// written once.  Rows beyond 16 vectors per thread at 8 warps use a
-// three-pass kernel that re-reads the (L2-resident) row.  (Measured slower
+// written once.  bf16 values enter PTX mixed-precision add/sub (.f32.bf16)
+// without being unpacked first (RowMath).  Rows beyond 16 vectors per thread
+// at 8 warps use a three-pass kernel that re-reads the (L2-resident) row.
+// (Measured slower
 // here and not used: a persistent variant streaming rows through a cp.async
 // ring, which trades resident warps for ring depth; staging (1 + scale) and
 // shift per block in shared memory, which re-reads them from L2 for every
@@ -283,10 +285,10 @@ struct GatedAdd<__nv_bfloat16> {
 
 // Resident 128-thread equivalents per SM asked of the compiler for the gated
 // kernel with bf16 rows of at most 6 vectors per thread and stream (a
-// build-time knob): 7 caps it at 72 registers without spills, so 14 rows of
-// 3072 are in flight per SM instead of 12 with the 85-register build
-// (measured 3% faster at [26598, 3072]); 8 (64 registers) spills.  Other
-// geometries ask for 4, which leaves them unspilled.
+// build-time knob): 7 caps it at 72 registers without spills (70 used), so
+// 14 rows of 3072 are in flight per SM instead of 12 with the 85-register
+// build of the TwoSum rounding (measured 3% faster at [26598, 3072]); 8 (64
+// registers) spills.  Other geometries ask for 4, which leaves them unspilled.
 #ifndef NR_GATED_MINB
 #define NR_GATED_MINB 7
 #endif

@@ -73,6 +73,18 @@ __device__ __forceinline__ float row_group_sum(float v, float* scratch) {
 #define NR_LN_MIXED 1
 #endif
 
+// Vector offset of row r's modulation sample, r / rows_per_sample * nvec:
+// 0 without a division when one sample covers every row (the common case),
+// a 32-bit division when both fit, else the 64-bit one.
+__device__ __forceinline__ int64_t sample_offset(int64_t r, int64_t rows_per_sample,
+                                                 int64_t rows, int nvec) {
+  if (rows_per_sample >= rows) return 0;
+  if (((r | rows_per_sample) >> 31) == 0)
+    return static_cast<int64_t>(static_cast<uint32_t>(r) /
+                                static_cast<uint32_t>(rows_per_sample)) * nvec;
+  return (r / rows_per_sample) * nvec;
+}
+
 // The three per-vector steps of LayerNorm + modulation: add the values to a
 // running sum, add their squared deviations from mu, and modulate them.  For
 // bf16 with NR_LN_MIXED the bf16 operands enter PTX mixed-precision
@@ -180,7 +192,7 @@ __global__ void __launch_bounds__(ln_row_threads<WPR>()) ln_modulate_rows_kernel
     const int64_t r = active ? row : 0;
     const uint4* xr = reinterpret_cast<const uint4*>(x) + r * nvec;
     uint4* orow = reinterpret_cast<uint4*>(out) + r * nvec;
-    const int64_t sample_off = (r / rows_per_sample) * nvec;
+    const int64_t sample_off = sample_offset(r, rows_per_sample, rows, nvec);
     const uint4* shv = reinterpret_cast<const uint4*>(shift) + sample_off;
     const uint4* scv = reinterpret_cast<const uint4*>(scale) + sample_off;
 
@@ -334,7 +346,7 @@ __global__ void __launch_bounds__(gated_threads<WPR>(), gated_min_blocks<T, VPT,
   uint4* rr = reinterpret_cast<uint4*>(residual) + r * nvec;
   const uint4* yr = reinterpret_cast<const uint4*>(y) + r * nvec;
   uint4* orow = reinterpret_cast<uint4*>(out) + r * nvec;
-  const int64_t sample_off = (r / rows_per_sample) * nvec;
+  const int64_t sample_off = sample_offset(r, rows_per_sample, rows, nvec);
   const uint4* gv = reinterpret_cast<const uint4*>(gate) + sample_off;
   const uint4* shv = reinterpret_cast<const uint4*>(shift) + sample_off;
   const uint4* scv = reinterpret_cast<const uint4*>(scale) + sample_off;

@@ -176,7 +176,7 @@ template <typename T, int VPT, int WPR>
 __global__ void __launch_bounds__(ln_row_threads<WPR>()) ln_modulate_rows_kernel(
     T* __restrict__ out, const T* __restrict__ x, const T* __restrict__ shift,
     const T* __restrict__ scale, int64_t rows, int nvec, int64_t rows_per_sample, float hidden_f,
-    float eps) {
+    float inv_hidden, float eps) {
   pdl_enter();  // before any global read: the previous kernel may still run
   constexpr int THREADS = ln_row_threads<WPR>();
   constexpr int TPR = kWarp * WPR;       // threads per row
@@ -188,43 +188,39 @@ __global__ void __launch_bounds__(ln_row_threads<WPR>()) ln_modulate_rows_kernel
   {
     const int64_t row = static_cast<int64_t>(blockIdx.x) * RPB + threadIdx.x / TPR;
     // Rows past the end still take part in the reductions' barriers (WPR > 1).
-    const bool active = row < rows;
+    // A block of one row group is never past the end (one block per row).
+    const bool active = RPB == 1 || row < rows;
     const int64_t r = active ? row : 0;
     const uint4* xr = reinterpret_cast<const uint4*>(x) + r * nvec;
     uint4* orow = reinterpret_cast<uint4*>(out) + r * nvec;
     const int64_t sample_off = sample_offset(r, rows_per_sample, rows, nvec);
     const uint4* shv = reinterpret_cast<const uint4*>(shift) + sample_off;
     const uint4* scv = reinterpret_cast<const uint4*>(scale) + sample_off;
+    auto in_row = [&](int k) { return t + k * TPR < nvec; };
 
     uint4 xv[VPT];
 #pragma unroll
-    for (int k = 0; k < VPT; k++) {
-      const int vi = t + k * TPR;
-      if (active && vi < nvec) xv[k] = ld_stream(xr + vi);
-    }
+    for (int k = 0; k < VPT; k++)
+      if (active && in_row(k)) xv[k] = ld_stream(xr + t + k * TPR);
 
     float sum = 0.0f;
 #pragma unroll
-    for (int k = 0; k < VPT; k++) {
-      const int vi = t + k * TPR;
-      if (active && vi < nvec) sum = RowMath<T>::sum(xv[k], sum);
-    }
-    const float mu = __fdiv_rn(row_group_sum<WPR>(sum, scratch_mean), hidden_f);
+    for (int k = 0; k < VPT; k++)
+      if (active && in_row(k)) sum = RowMath<T>::sum(xv[k], sum);
+    const float mu = row_mean_of(row_group_sum<WPR>(sum, scratch_mean), hidden_f, inv_hidden);
 
     float dev = 0.0f;
 #pragma unroll
-    for (int k = 0; k < VPT; k++) {
-      const int vi = t + k * TPR;
-      if (active && vi < nvec) dev = RowMath<T>::dev(xv[k], mu, dev);
-    }
-    const float rstd =
-        1.0f / sqrtf(__fdiv_rn(row_group_sum<WPR>(dev, scratch_var), hidden_f) + eps);
+    for (int k = 0; k < VPT; k++)
+      if (active && in_row(k)) dev = RowMath<T>::dev(xv[k], mu, dev);
+    const float rstd = row_rstd_of(
+        row_mean_of(row_group_sum<WPR>(dev, scratch_var), hidden_f, inv_hidden), eps);
     if (!active) return;
 
 #pragma unroll
     for (int k = 0; k < VPT; k++) {
       const int vi = t + k * TPR;
-      if (vi < nvec)
+      if (in_row(k))
         st_stream(orow + vi,
                   RowMath<T>::modulate(xv[k], mu, rstd, ld_param(shv + vi), ld_param(scv + vi)));
     }
@@ -330,7 +326,7 @@ __global__ void __launch_bounds__(gated_threads<WPR>(), gated_min_blocks<T, VPT,
     gated_ln_modulate_kernel(
     T* __restrict__ out, T* __restrict__ residual, const T* __restrict__ y,
     const T* __restrict__ gate, const T* __restrict__ shift, const T* __restrict__ scale,
-    int64_t rows, int nvec, int64_t rows_per_sample, float hidden_f, float eps,
+    int64_t rows, int nvec, int64_t rows_per_sample, float hidden_f, float inv_hidden, float eps,
     int64_t prefetch_rows) {
   pdl_enter();  // before any global read: the previous kernel may still run
   constexpr int THREADS = gated_threads<WPR>();
@@ -374,14 +370,15 @@ __global__ void __launch_bounds__(gated_threads<WPR>(), gated_min_blocks<T, VPT,
       sum = RowMath<T>::sum(xv[k], sum);
     }
   }
-  const float mu = __fdiv_rn(row_group_sum<WPR>(sum, scratch_mean), hidden_f);
+  const float mu = row_mean_of(row_group_sum<WPR>(sum, scratch_mean), hidden_f, inv_hidden);
   float dev = 0.0f;
 #pragma unroll
   for (int k = 0; k < VPT; k++) {
     const int vi = t + k * TPR;
     if (active && vi < nvec) dev = RowMath<T>::dev(xv[k], mu, dev);
   }
-  const float rstd = 1.0f / sqrtf(__fdiv_rn(row_group_sum<WPR>(dev, scratch_var), hidden_f) + eps);
+  const float rstd = row_rstd_of(
+      row_mean_of(row_group_sum<WPR>(dev, scratch_var), hidden_f, inv_hidden), eps);
   if (!active) return;
 #pragma unroll
   for (int k = 0; k < VPT; k++) {
@@ -396,7 +393,7 @@ template <typename T>
 __global__ void __launch_bounds__(1024) ln_modulate_long_row_kernel(
     T* __restrict__ out, const T* __restrict__ x, const T* __restrict__ shift,
     const T* __restrict__ scale, int64_t nvec, int64_t rows_per_sample, float hidden_f,
-    float eps) {
+    float inv_hidden, float eps) {
   pdl_enter();  // before any global read: the previous kernel may still run
   constexpr int N = Vec<T>::N;
   __shared__ float scratch_mean[32];
@@ -415,7 +412,7 @@ __global__ void __launch_bounds__(1024) ln_modulate_long_row_kernel(
 #pragma unroll
     for (int e = 0; e < N; e++) sum += v[e];
   }
-  const float mu = __fdiv_rn(block_sum(sum, scratch_mean), hidden_f);
+  const float mu = row_mean_of(block_sum(sum, scratch_mean), hidden_f, inv_hidden);
   float dev = 0.0f;
   for (int64_t vi = threadIdx.x; vi < nvec; vi += blockDim.x) {
     float v[N];
@@ -426,7 +423,8 @@ __global__ void __launch_bounds__(1024) ln_modulate_long_row_kernel(
       dev = fmaf(d, d, dev);
     }
   }
-  const float rstd = 1.0f / sqrtf(__fdiv_rn(block_sum(dev, scratch_var), hidden_f) + eps);
+  const float rstd =
+      row_rstd_of(row_mean_of(block_sum(dev, scratch_var), hidden_f, inv_hidden), eps);
   // out may alias x: each thread overwrites only vectors it has finished reading.
   for (int64_t vi = threadIdx.x; vi < nvec; vi += blockDim.x) {
     float v[N], sh[N], sc[N];
@@ -448,6 +446,7 @@ struct LnArgs {
   int nvec;
   int64_t rps;
   float hidden_f;
+  float inv_hidden;
   float eps;
 };
 
@@ -457,10 +456,9 @@ cudaError_t launch_rows(const LnArgs& a, cudaStream_t s) {
   constexpr int RPB = THREADS / (kWarp * WPR);
   static_assert(RPB >= 1, "row groups must fit the block");
   const int64_t blocks = (a.rows + RPB - 1) / RPB;
-  return launch_pdl(ln_modulate_rows_kernel<T, VPT, WPR>, dim3(static_cast<unsigned>(blocks)),
-                    dim3(THREADS), 0, s,
+  return launch_pdl(ln_modulate_rows_kernel<T, VPT, WPR>, dim3(static_cast<unsigned>(blocks)), dim3(THREADS), 0, s,
       static_cast<T*>(a.out), static_cast<const T*>(a.x), static_cast<const T*>(a.shift),
-      static_cast<const T*>(a.scale), a.rows, a.nvec, a.rps, a.hidden_f, a.eps);
+      static_cast<const T*>(a.scale), a.rows, a.nvec, a.rps, a.hidden_f, a.inv_hidden, a.eps);
 }
 
 // Vectors per thread offered for one-warp rows, and for rows spread over
@@ -506,7 +504,7 @@ cudaError_t launch_typed(const LnArgs& a, cudaStream_t s) {
   return launch_pdl(ln_modulate_long_row_kernel<T>, dim3(static_cast<unsigned>(a.rows)), dim3(1024),
                     0, s,
       static_cast<T*>(a.out), static_cast<const T*>(a.x), static_cast<const T*>(a.shift),
-      static_cast<const T*>(a.scale), nvec, a.rps, a.hidden_f, a.eps);
+      static_cast<const T*>(a.scale), nvec, a.rps, a.hidden_f, a.inv_hidden, a.eps);
 }
 
 struct GatedArgs {
@@ -520,6 +518,7 @@ struct GatedArgs {
   int nvec;
   int64_t rps;
   float hidden_f;
+  float inv_hidden;
   float eps;
 };
 
@@ -541,7 +540,8 @@ cudaError_t launch_gated_rows(const GatedArgs& a, cudaStream_t s) {
                     dim3(THREADS), 0, s,
       static_cast<T*>(a.out), static_cast<T*>(a.residual), static_cast<const T*>(a.y),
       static_cast<const T*>(a.gate), static_cast<const T*>(a.shift),
-      static_cast<const T*>(a.scale), a.rows, a.nvec, a.rps, a.hidden_f, a.eps, prefetch_rows);
+      static_cast<const T*>(a.scale), a.rows, a.nvec, a.rps, a.hidden_f, a.inv_hidden, a.eps,
+      prefetch_rows);
 }
 
 template <typename T>
@@ -581,6 +581,7 @@ cudaError_t launch_gated_ln_modulate(void* out, void* residual, const void* y, c
   a.nvec = static_cast<int>(hidden / (is_bf16 ? 8 : 4));
   a.rps = rows_per_sample;
   a.hidden_f = static_cast<float>(hidden);
+  a.inv_hidden = 1.0f / a.hidden_f;
   a.eps = eps;
   if (is_bf16) return launch_gated_typed<__nv_bfloat16>(a, stream);
   return launch_gated_typed<float>(a, stream);
@@ -598,6 +599,7 @@ cudaError_t launch_ln_modulate(void* out, const void* x, const void* shift, cons
   a.nvec = static_cast<int>(hidden / (is_bf16 ? 8 : 4));
   a.rps = rows_per_sample;
   a.hidden_f = static_cast<float>(hidden);
+  a.inv_hidden = 1.0f / a.hidden_f;
   a.eps = eps;
   if (is_bf16) return launch_typed<__nv_bfloat16>(a, stream);
   return launch_typed<float>(a, stream);

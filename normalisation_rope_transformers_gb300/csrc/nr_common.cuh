@@ -373,4 +373,32 @@ __device__ __forceinline__ float block_sum(float v, float* scratch) {
   return total;
 }
 
+// ---------------------------------------------------------------------------
+// Row statistics from a row's totals (the LayerNorm mean and variance, the
+// RMSNorm mean square).  With NR_FAST_STATS (a build-time knob) a mean is
+// total * (1/n) refined by one fma step -- the remainder total - q*n is exact,
+// so a quotient that is a float comes out exactly -- and the reciprocal
+// square root is the hardware approximation; otherwise an IEEE division and
+// 1 / sqrtf.
+// ---------------------------------------------------------------------------
+#ifndef NR_FAST_STATS
+#define NR_FAST_STATS 1
+#endif
+__device__ __forceinline__ float row_mean_of(float total, float n, float inv_n) {
+#if NR_FAST_STATS
+  const float q = total * inv_n;
+  return fmaf(fmaf(-q, n, total), inv_n, q);
+#else
+  (void)inv_n;
+  return __fdiv_rn(total, n);
+#endif
+}
+__device__ __forceinline__ float row_rstd_of(float mean_square, float eps) {
+#if NR_FAST_STATS
+  return rsqrtf(mean_square + eps);
+#else
+  return 1.0f / sqrtf(mean_square + eps);
+#endif
+}
+
 }  // namespace nr

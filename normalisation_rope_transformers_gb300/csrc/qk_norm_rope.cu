@@ -30,6 +30,7 @@
 #include <atomic>
 #include <map>
 #include <mutex>
+#include <type_traits>
 #include <utility>
 
 #include "nr_common.cuh"
@@ -535,12 +536,17 @@ __global__ void NR_QKB_BOUNDS qk_norm_rope_bulk_kernel(const QkArgs a,
     float2 cs[N];
 #pragma unroll
     for (int e = 0; e < N; e++) cs[e] = table[(j & 1) * HALF + l * N + e];
-    for (int it = warp; it < IT; it += kBulkWarps) {  // uniform across the warp
+    // One pass: head rows it*GW .. it*GW + GW - 1, one per lane group.  KIND 0:
+    // every row of the pass is a Q head, 1: every row a K head (the lane's
+    // weights are then fixed for the pass); 2: a pass that straddles the Q/K
+    // boundary or runs past the last head (each lane group picks its own).
+    auto pass = [&](auto kind, int it) {
+      constexpr int KIND = decltype(kind)::value;
       const int row = it * GW + g;
       // Lanes of a row past the last head carry zeros but still join the
       // butterfly: the shuffles take the full warp.
-      const bool valid = row < H;
-      const bool is_q = row < a.hq;
+      const bool valid = KIND != 2 || row < H;
+      const bool is_q = KIND == 0 || (KIND == 2 && row < a.hq);
       uint4* r = reinterpret_cast<uint4*>(
           st + (is_q ? 0u : geo.q_bytes) +
           static_cast<size_t>(valid ? (is_q ? row : row - a.hq) : 0) * D * sizeof(T));
@@ -556,17 +562,22 @@ __global__ void NR_QKB_BOUNDS qk_norm_rope_bulk_kernel(const QkArgs a,
         }
       }
       ss = group_sum<L>(ss);
-      if (!valid) continue;
+      if (!valid) return;
       const float inv = rsqrtf(ss * a.inv_d + a.eps);
       const float* wa = wsm + (is_q ? 0 : D) + l * N;
       const float* wb = wa + HALF;
       float oa[N], ob[N];
 #pragma unroll
       for (int e = 0; e < N; e++) {
-        const float we_a = NR_QKB_WREG ? (is_q ? wqa[NR_QKB_WREG ? e : 0] : wka[NR_QKB_WREG ? e : 0])
-                                       : wa[e];
-        const float we_b = NR_QKB_WREG ? (is_q ? wqb[NR_QKB_WREG ? e : 0] : wkb[NR_QKB_WREG ? e : 0])
-                                       : wb[e];
+        constexpr int E = NR_QKB_WREG ? 1 : 0;
+        const float we_a = !NR_QKB_WREG ? wa[e]
+                           : KIND == 0  ? wqa[E * e]
+                           : KIND == 1  ? wka[E * e]
+                                        : (is_q ? wqa[E * e] : wka[E * e]);
+        const float we_b = !NR_QKB_WREG ? wb[e]
+                           : KIND == 0  ? wqb[E * e]
+                           : KIND == 1  ? wkb[E * e]
+                                        : (is_q ? wqb[E * e] : wkb[E * e]);
         const float na = xa[e] * inv * we_a;
         const float nb = xb[e] * inv * we_b;
         oa[e] = fmaf(na, cs[e].x, -nb * cs[e].y);
@@ -574,6 +585,15 @@ __global__ void NR_QKB_BOUNDS qk_norm_rope_bulk_kernel(const QkArgs a,
       }
       r[l] = Vec<T>::pack(oa);
       r[l + L] = Vec<T>::pack(ob);
+    };
+    for (int it = warp; it < IT; it += kBulkWarps) {  // uniform across the warp
+      const int first = it * GW;
+      if (first + GW <= a.hq)
+        pass(std::integral_constant<int, 0>(), it);
+      else if (first >= a.hq && first + GW <= H)
+        pass(std::integral_constant<int, 1>(), it);
+      else
+        pass(std::integral_constant<int, 2>(), it);
     }
     // the next token's angles, into the other table buffer
     if (tid < HALF && j + 1 < ntok) {

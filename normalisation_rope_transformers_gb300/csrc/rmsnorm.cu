@@ -97,8 +97,8 @@ __global__ void __launch_bounds__((PW && VPT <= 2) ? kDecodeMaxThreads : kRowMax
                                                            const T* __restrict__ x,
                                                            const T* __restrict__ w,
                                                            T* __restrict__ res, int nvec,
-                                                           float hidden_f, float eps,
-                                                           float w_add, int64_t rows,
+                                                           float hidden_f, float inv_hidden,
+                                                           float eps, float w_add, int64_t rows,
                                                            int64_t prefetch_rows) {
   pdl_enter();  // before any global read: the previous kernel may still run
   constexpr int N = Vec<T>::N;
@@ -141,7 +141,7 @@ __global__ void __launch_bounds__((PW && VPT <= 2) ? kDecodeMaxThreads : kRowMax
   }
 
   const float total = block_sum(sum_sq, scratch);
-  const float inv = 1.0f / sqrtf(__fdiv_rn(total, hidden_f) + eps);
+  const float inv = row_rstd_of(row_mean_of(total, hidden_f, inv_hidden), eps);
 
 #pragma unroll
   for (int k = 0; k < VPT; k++) {
@@ -164,7 +164,8 @@ __global__ void __launch_bounds__(1024) rmsnorm_long_row_kernel(T* __restrict__ 
                                                                 const T* __restrict__ x,
                                                                 const T* __restrict__ w,
                                                                 T* __restrict__ res, int64_t nvec,
-                                                                float hidden_f, float eps,
+                                                                float hidden_f,
+                                                                float inv_hidden, float eps,
                                                                 float w_add) {
   pdl_enter();  // before any global read: the previous kernel may still run
   constexpr int N = Vec<T>::N;
@@ -192,7 +193,7 @@ __global__ void __launch_bounds__(1024) rmsnorm_long_row_kernel(T* __restrict__ 
     for (int e = 0; e < N; e++) sum_sq = fmaf(v[e], v[e], sum_sq);
   }
   const float total = block_sum(sum_sq, scratch);
-  const float inv = 1.0f / sqrtf(__fdiv_rn(total, hidden_f) + eps);
+  const float inv = row_rstd_of(row_mean_of(total, hidden_f, inv_hidden), eps);
   // Each thread re-reads only the vectors it wrote itself, so program order
   // makes its own residual stores visible to it.
   for (int64_t vi = threadIdx.x; vi < nvec; vi += blockDim.x) {
@@ -233,7 +234,7 @@ cudaError_t launch_rows_res(const RowLaunch& g, const EPI& epi, const void* x, c
   }
   return launch_pdl(kernel, dim3(static_cast<unsigned>(rows)), dim3(g.threads), 0, s, epi,
                     static_cast<const T*>(x), static_cast<const T*>(w), static_cast<T*>(res), nvec,
-                    hidden_f, eps, w_add, rows, prefetch_rows);
+                    hidden_f, 1.0f / hidden_f, eps, w_add, rows, prefetch_rows);
 }
 
 template <typename T, int VPT, bool PW, typename EPI>
@@ -330,11 +331,11 @@ cudaError_t launch_typed(void* out, const void* x, const void* w, void* res, int
   if (res != nullptr)
     return launch_pdl(rmsnorm_long_row_kernel<T, true>, grid, dim3(1024), 0, s,
         static_cast<T*>(out), static_cast<const T*>(x), static_cast<const T*>(w),
-        static_cast<T*>(res), nvec, hidden_f, eps, w_add);
+        static_cast<T*>(res), nvec, hidden_f, 1.0f / hidden_f, eps, w_add);
   else
     return launch_pdl(rmsnorm_long_row_kernel<T, false>, grid, dim3(1024), 0, s,
         static_cast<T*>(out), static_cast<const T*>(x), static_cast<const T*>(w), nullptr, nvec,
-        hidden_f, eps, w_add);
+        hidden_f, 1.0f / hidden_f, eps, w_add);
 }
 
 }  // namespace

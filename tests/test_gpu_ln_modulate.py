@@ -8,7 +8,8 @@ mag = (|x - mu| + mean|x|) * rstd * |1 + scale| + |shift| from the oracle.  K
 counts the f32 roundings on the kernel's path: the row sum behind mu (up to
 16 per thread + 5 butterfly + 6 cross-warp levels at hidden 3072, giving an
 absolute error of ~27 * mean|x| in mu), the centred sum of squares and the
-division/sqrt behind rstd (~15 relative), and the final products and fma.
+quotient and reciprocal square root behind rstd (~15 relative), and the final
+products and fma.
 The pages name the fusion (FastVideo PAN2 docs, "Performance switches",
 dit_fused_kernels) without printing its formula.
 """

@@ -520,6 +520,7 @@ def run_ours(args):
     breakdown_steps = min(K, 300)
     samples = per_call_samples(breakdown_steps)
     per_call_ms = [statistics.fmean(v) for v in samples]
+    b2b_ms = {c.name: back_to_back_ms(torch, c.fn) for c in calls if c.nbytes > 2 * L2_BYTES}
 
     ms_per_step = elapsed_ms / K
     value = world * step_bytes * K / (elapsed_ms * 1e-3) / 1e9
@@ -533,6 +534,11 @@ def run_ours(args):
                            "frac_of_measured": round(gbs / peak, 4),
                            "frac_of_nominal_8TBs": round(gbs / NOMINAL_HBM_GBS, 4),
                            "rows_per_s": round(c.rows / (ms * 1e-3), 1), "rows_unit": c.rows_unit}
+        if c.name in b2b_ms:
+            gbs_b2b = c.nbytes / (b2b_ms[c.name] * 1e-3) / 1e9
+            kernels[c.name].update({"us_b2b": round(b2b_ms[c.name] * 1e3, 2),
+                                    "GB_s_b2b": round(gbs_b2b, 1),
+                                    "frac_of_measured_b2b": round(gbs_b2b / peak, 4)})
     dc = calls[dom]
     achieved = dc.nbytes / (dom_ms * 1e-3) / 1e9
     traffic = ncu_traffic(dc.kernel, dc.rows)
@@ -554,13 +560,20 @@ def run_ours(args):
                           "duration_us": round(dom_ms * 1e3, 2),
                           "duration_us_median": round(statistics.median(dom_samples) * 1e3, 2),
                           "duration_us_min": round(min(dom_samples) * 1e3, 2),
+                          "duration_us_b2b": (round(b2b_ms[dc.name] * 1e3, 2)
+                                              if dc.name in b2b_ms else None),
+                          "frac_b2b": (round(dc.nbytes / (b2b_ms[dc.name] * 1e-3) / 1e9 / peak, 4)
+                                       if dc.name in b2b_ms else None),
                           "copy_same_bytes_GB_s": copy_gbs,
                           "frac_of_copy_same_bytes": (round(achieved / copy_gbs, 4)
                                                       if copy_gbs else None)},
                          **(traffic or {})),
         "kernels": kernels,
-        "kernels_timing": "per-call CUDA events over %d steps after the timed region (the "
-                          "timed region brackets only the dominant call)" % breakdown_steps,
+        "kernels_timing": ("per-call CUDA events over %d steps after the timed region (the "
+                           "timed region brackets only the dominant call); *_b2b: the call "
+                           "alone, %d launches back to back between two CUDA events (median "
+                           "of %d), as the next rows are timed, for calls whose operands "
+                           "exceed twice the L2" % (breakdown_steps, B2B_LAUNCHES, B2B_REPS)),
         "rows_per_s": round(world * sum(c.rows for c in calls) / (ms_per_step * 1e-3), 1),
         "e2e": e2e,
         "gpu_launches": K * len(calls),
@@ -734,6 +747,30 @@ def next_row_cases(nr, synth, torch, device, rows_override=None):
                 rotary_dim=64, interleaved=True)),
             ("qk_norm_rope_llama3_bf16_26598x24x128", rope_variant(
                 theta=500000.0, llama3=(8.0, 1.0, 4.0, 8192.0)))]
+
+
+B2B_LAUNCHES = 20
+B2B_REPS = 5
+
+
+def back_to_back_ms(torch, fn):
+    """Device time per launch of `fn` run alone, B2B_LAUNCHES launches back to
+    back between two CUDA events (median over B2B_REPS): each launch's start
+    overlaps the previous one's drain (programmatic dependent launch), which an
+    event recorded between two launches prevents."""
+    for _ in range(3):
+        fn()
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    out = []
+    for _ in range(B2B_REPS):
+        s.record()
+        for _ in range(B2B_LAUNCHES):
+            fn()
+        e.record()
+        torch.cuda.synchronize()
+        out.append(s.elapsed_time(e) / B2B_LAUNCHES)
+    return statistics.median(out)
 
 
 def next_rows(nr, synth, torch, device, peak):

@@ -64,6 +64,8 @@ def parse_args():
     p.add_argument("--e2e-steps", type=int, default=10)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-decode-sweep", action="store_true")
+    p.add_argument("--no-back-to-back", action="store_true",
+                   help="skip the per-call back-to-back times (e.g. for an ncu launch list)")
     p.add_argument("--no-next-rows", action="store_true")
     p.add_argument("--profile", default=None,
                    help="run only the named call of the step or of the next rows (e.g. qk_norm_rope, "
@@ -520,7 +522,8 @@ def run_ours(args):
     breakdown_steps = min(K, 300)
     samples = per_call_samples(breakdown_steps)
     per_call_ms = [statistics.fmean(v) for v in samples]
-    b2b_ms = {c.name: back_to_back_ms(torch, c.fn) for c in calls if c.nbytes > 2 * L2_BYTES}
+    b2b_ms = ({} if args.no_back_to_back else
+              {c.name: back_to_back_ms(torch, c.fn) for c in calls if c.nbytes > 2 * L2_BYTES})
 
     ms_per_step = elapsed_ms / K
     value = world * step_bytes * K / (elapsed_ms * 1e-3) / 1e9

@@ -408,7 +408,7 @@ struct BulkSmem {
   }
 };
 
-template <typename T, typename WT, int L, int NST>
+template <typename T, typename WT, int L, int NST, bool MROPE>
 __global__ void NR_QKB_BOUNDS qk_norm_rope_bulk_kernel(const QkArgs a,
                                                                        const RopeTurns turns,
                                                                        const BulkGeom geo) {
@@ -498,11 +498,14 @@ __global__ void NR_QKB_BOUNDS qk_norm_rope_bulk_kernel(const QkArgs a,
       table[b * HALF + i] = make_float2(cn, sn);
     }
   };
+  // M-RoPE (MROPE): thread i computes pair i's angle from position row
+  // axis[i] (the launcher ensures one pair per thread); otherwise row 0.
+  const int64_t pos_row = (MROPE && tid < HALF) ? turns.axis[tid] * a.pos_row_stride : 0;
   int pos_next = 0;  // position of local token j + 1, loaded one token ahead
   if (ntok > 0) {
     if (tid < HALF) {
-      angles(0, a.pos[t0]);
-      if (ntok > 1) pos_next = a.pos[t0 + C];
+      angles(0, a.pos[pos_row + t0]);
+      if (ntok > 1) pos_next = a.pos[pos_row + t0 + C];
     }
   }
   __syncthreads();
@@ -598,7 +601,7 @@ __global__ void NR_QKB_BOUNDS qk_norm_rope_bulk_kernel(const QkArgs a,
     // the next token's angles, into the other table buffer
     if (tid < HALF && j + 1 < ntok) {
       angles(static_cast<int>((j + 1) & 1), pos_next);
-      if (j + 2 < ntok) pos_next = a.pos[t0 + (j + 2) * C];
+      if (j + 2 < ntok) pos_next = a.pos[pos_row + t0 + (j + 2) * C];
     }
     fence_proxy_async_smem();
     __syncthreads();
@@ -635,8 +638,9 @@ __global__ void NR_QKB_BOUNDS qk_norm_rope_bulk_kernel(const QkArgs a,
 // full-head NeoX kernel above is compiled exactly as measured): a rotary
 // dimension below head_dim (lanes past the rotated block carry two normed,
 // unrotated vectors) and GPT-J interleaved pairs.  The stages, the producer
-// and the bounded waits are those of the kernel above.  (M-RoPE runs the ring
-// kernel, measured faster for it.)
+// and the bounded waits are those of the kernel above.  (M-RoPE over the
+// whole head runs the kernel above with MROPE set; other M-RoPE layouts run
+// the ring kernel.)
 template <typename T, typename WT, int L, int NST>
 // Minimum resident blocks per SM asked of the compiler for the variant kernel
 // (a build-time knob; 0: none asked).  With the weights in shared memory a
@@ -960,16 +964,23 @@ cudaError_t launch_g(const QkArgs& a, const RopeTurns& turns, cudaStream_t s) {
                     dim3(kQkThreads), QkSmem<T, L>::bytes(RING, GEN ? 3 : 1), s, a, turns);
 }
 
+// 1: M-RoPE over the whole head runs the full-head bulk kernel (a build-time
+// knob; 0: the ring kernel).  Measured at [26598, 24+24, 128], sections
+// (16, 24, 24): 100.4 us against 107.0 us on the ring kernel.
+#ifndef NR_MROPE_BULK
+#define NR_MROPE_BULK 1
+#endif
+
 // Largest shared memory the bulk variant may take per block (stages plus
 // tables): beyond it (very many heads per token) the ring kernel runs.
 constexpr size_t kBulkMaxSmem = 112 * 1024;
 
-template <typename T, typename WT, int L, bool VAR>
+template <typename T, typename WT, int L, bool VAR, bool MROPE>
 cudaError_t launch_bulk(const QkArgs& a, const RopeTurns& turns, const BulkGeom& geo,
                         size_t smem, cudaStream_t s) {
   constexpr int NST = NR_QKB_STAGES;
   auto kernel = VAR ? qk_norm_rope_bulk_var_kernel<T, WT, L, NST>
-                    : qk_norm_rope_bulk_kernel<T, WT, L, NST>;
+                    : qk_norm_rope_bulk_kernel<T, WT, L, NST, MROPE>;
   int device = 0;
   cudaError_t e = cudaGetDevice(&device);
   if (e != cudaSuccess) return e;
@@ -1008,8 +1019,13 @@ cudaError_t launch_bulk(const QkArgs& a, const RopeTurns& turns, const BulkGeom&
 template <typename T, typename WT, int L>
 cudaError_t launch_l(const QkArgs& a, const RopeTurns& turns, cudaStream_t s) {
   const bool general = a.rot_vec != 2 * L || a.interleaved || a.mrope;
-  // M-RoPE: the ring kernel (measured faster for it than the bulk copies).
-  if (a.mrope) return launch_g<T, WT, L, true>(a, turns, s);
+  // M-RoPE over the whole head with rotate-half pairs, one pair per thread:
+  // the full-head bulk kernel, each thread reading its pair's position row;
+  // any other M-RoPE: the ring kernel.
+  constexpr int HALF = L * Vec<T>::N;
+  const bool mrope_bulk = NR_MROPE_BULK && a.mrope && a.rot_vec == 2 * L && !a.interleaved &&
+                          HALF <= kBulkThreads;
+  if (a.mrope && !mrope_bulk) return launch_g<T, WT, L, true>(a, turns, s);
   // Whole tokens through shared memory when a token's rows fit the stages.
   constexpr int D = 2 * L * Vec<T>::N;
   BulkGeom geo;
@@ -1017,9 +1033,11 @@ cudaError_t launch_l(const QkArgs& a, const RopeTurns& turns, cudaStream_t s) {
   geo.k_bytes = static_cast<unsigned>(a.hk * D * sizeof(T));
   geo.stage_bytes = (geo.q_bytes + geo.k_bytes + 127u) & ~127u;
   const size_t smem = BulkSmem<T, L>::bytes(NR_QKB_STAGES, geo.stage_bytes);
-  if (NR_QK_PATH == 1 && smem <= kBulkMaxSmem)
-    return general ? launch_bulk<T, WT, L, true>(a, turns, geo, smem, s)
-                   : launch_bulk<T, WT, L, false>(a, turns, geo, smem, s);
+  if (NR_QK_PATH == 1 && smem <= kBulkMaxSmem) {
+    if (mrope_bulk) return launch_bulk<T, WT, L, false, true>(a, turns, geo, smem, s);
+    return general ? launch_bulk<T, WT, L, true, false>(a, turns, geo, smem, s)
+                   : launch_bulk<T, WT, L, false, false>(a, turns, geo, smem, s);
+  }
   return general ? launch_g<T, WT, L, true>(a, turns, s) : launch_g<T, WT, L, false>(a, turns, s);
 }
 

@@ -161,6 +161,13 @@ __device__ __forceinline__ bool mbar_test_wait(unsigned bar, unsigned parity) {
   return done != 0;
 }
 
+// Nanoseconds a waiting thread sleeps between two polls (a build-time knob).
+// Measured on the Q/K bulk kernel at [26598, 24+24, 128]: 8 ns ties 32 ns,
+// 128 ns is 0.5-1 us slower (the wake-up comes late).
+#ifndef NR_MBAR_SLEEP_NS
+#define NR_MBAR_SLEEP_NS 32
+#endif
+
 // Polls the phase (with a short sleep between polls) for at most `limit` SM
 // clock cycles; false if it gave up (the caller records the failure and winds
 // down).  Every poll returns at once, so the bound always holds.
@@ -168,7 +175,7 @@ __device__ __forceinline__ bool mbar_wait_bounded(unsigned bar, unsigned parity,
   if (mbar_test_wait(bar, parity)) return true;
   const long long t0 = clock64();
   do {
-    __nanosleep(32);
+    __nanosleep(NR_MBAR_SLEEP_NS);
     if (mbar_test_wait(bar, parity)) return true;
   } while (clock64() - t0 <= limit);
   return false;

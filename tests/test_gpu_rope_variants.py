@@ -71,6 +71,36 @@ def test_mrope_sections(nr, interleaved):
                 mrope_interleaved=interleaved, theta=1e6)
 
 
+def _mrope_positions(T, seed):
+    rng = np.random.default_rng(seed)
+    return torch.from_numpy(rng.integers(0, 8192, (3, T)).astype(np.int32))
+
+
+@pytest.mark.parametrize("D,dtype,hq,hk,T", [
+    (256, torch.bfloat16, 3, 1, 45),    # 128 pairs: one per thread of the bulk kernel
+    (512, torch.bfloat16, 2, 1, 19),    # 256 pairs: more than its threads, the ring kernel
+    (64, torch.float32, 3, 1, 21),
+    (256, torch.float32, 2, 2, 17),     # f32, 128 pairs
+    (128, torch.bfloat16, 7, 3, 3001),  # GQA, passes that straddle Q/K or end past the heads
+], ids=["bf16_256", "bf16_512_ring", "f32_64", "f32_256", "gqa_many_tokens"])
+def test_mrope_whole_head_sizes_and_paths(nr, D, dtype, hq, hk, T):
+    """M-RoPE over the whole head at each kernel's edge, sections in the
+    16:24:24 proportion of the benchmark."""
+    half = D // 2
+    sections = (half // 4, 3 * half // 8, half - half // 4 - 3 * half // 8)
+    run_variant(nr, T, hq, hk, D, dtype=dtype, seed=D + T, pos=_mrope_positions(T, D),
+                mrope_sections=sections, theta=1e6)
+
+
+@pytest.mark.parametrize("interleaved", [False, True])
+def test_mrope_partial_rotary_runs_the_ring_kernel(nr, interleaved):
+    """M-RoPE on the first 64 of 128 dims (sections sum to 32 pairs), with
+    rotate-half or GPT-J pairs: layouts the full-head kernel does not take."""
+    T = 41
+    run_variant(nr, T, 4, 2, 128, seed=23, pos=_mrope_positions(T, 23), rotary_dim=64,
+                interleaved=interleaved, mrope_sections=(8, 12, 12), theta=1e6)
+
+
 @pytest.mark.parametrize("kw", [dict(rotary_dim=64), dict(interleaved=True),
                                 dict(rotary_dim=32, interleaved=True)])
 def test_f32_variants(nr, kw):

@@ -543,6 +543,11 @@ __global__ void NR_QKB_BOUNDS qk_norm_rope_bulk_kernel(const QkArgs a,
     // every row of the pass is a Q head, 1: every row a K head (the lane's
     // weights are then fixed for the pass); 2: a pass that straddles the Q/K
     // boundary or runs past the last head (each lane group picks its own).
+    // The stage holds the token's Q rows and then its K rows, contiguously,
+    // so head row `row` (Q rows first) starts at row * D elements.
+    auto row_ptr = [&](int row) {
+      return reinterpret_cast<uint4*>(st + static_cast<size_t>(row) * D * sizeof(T));
+    };
     auto pass = [&](auto kind, int it) {
       constexpr int KIND = decltype(kind)::value;
       const int row = it * GW + g;
@@ -550,9 +555,7 @@ __global__ void NR_QKB_BOUNDS qk_norm_rope_bulk_kernel(const QkArgs a,
       // butterfly: the shuffles take the full warp.
       const bool valid = KIND != 2 || row < H;
       const bool is_q = KIND == 0 || (KIND == 2 && row < a.hq);
-      uint4* r = reinterpret_cast<uint4*>(
-          st + (is_q ? 0u : geo.q_bytes) +
-          static_cast<size_t>(valid ? (is_q ? row : row - a.hq) : 0) * D * sizeof(T));
+      uint4* r = row_ptr(valid ? row : 0);
       float xa[N], xb[N];
       float ss = 0.0f;
       if (valid) {

@@ -539,15 +539,15 @@ __global__ void NR_QKB_BOUNDS qk_norm_rope_bulk_kernel(const QkArgs a,
     float2 cs[N];
 #pragma unroll
     for (int e = 0; e < N; e++) cs[e] = table[(j & 1) * HALF + l * N + e];
-    // One pass: head rows it*GW .. it*GW + GW - 1, one per lane group.  KIND 0:
-    // every row of the pass is a Q head, 1: every row a K head (the lane's
-    // weights are then fixed for the pass); 2: a pass that straddles the Q/K
-    // boundary or runs past the last head (each lane group picks its own).
     // The stage holds the token's Q rows and then its K rows, contiguously,
     // so head row `row` (Q rows first) starts at row * D elements.
     auto row_ptr = [&](int row) {
       return reinterpret_cast<uint4*>(st + static_cast<size_t>(row) * D * sizeof(T));
     };
+    // One pass: head rows it*GW .. it*GW + GW - 1, one per lane group.  KIND 0:
+    // every row of the pass is a Q head, 1: every row a K head (the lane's
+    // weights are then fixed for the pass); 2: a pass that straddles the Q/K
+    // boundary or runs past the last head (each lane group picks its own).
     auto pass = [&](auto kind, int it) {
       constexpr int KIND = decltype(kind)::value;
       const int row = it * GW + g;
